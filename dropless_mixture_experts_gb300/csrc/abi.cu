@@ -1,0 +1,264 @@
+// The C ABI (include/moe.h): argument validation and the launch sequence of
+// each call.  Nothing here computes; every step runs in the kernels.
+#include "kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+bool dims_ok(const moe_dims* d) {
+  if (!d) return false;
+  if (d->tokens < 0 || d->tokens > (int64_t(1) << 31) / 64) return false;
+  if (d->experts < 1 || d->experts > kMaxExperts) return false;
+  if (d->top_k < 1 || d->top_k > d->experts || d->top_k > kMaxTopK) return false;
+  if (d->d_model < 64 || d->d_hidden < 64 || d->shared_hidden < 0) return false;
+  if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return false;
+  if (d->tokens * (int64_t)d->top_k + (int64_t)d->experts * kRowPad >= (int64_t(1) << 31))
+    return false;
+  return true;
+}
+
+moe_status shape_supported(const moe_dims* d) {
+  if (d->d_model % 64 || d->d_hidden % 64 || d->shared_hidden % 64) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_dims* d, int mode, const void* ws, size_t bytes) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return MOE_ERR_WORKSPACE;
+  if (bytes < make_layout(*d, mode).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status cuda_status() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+#define MOE_TRY(expr)                 \
+  do {                                \
+    moe_status _s = (expr);           \
+    if (_s != MOE_OK) return _s;      \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "device: a bounded wait ran out";
+    case MOE_ERR_DEVICE_CHECK: return "device: an index check failed";
+  }
+  return "unknown status";
+}
+
+moe_status moe_workspace_bytes(const moe_dims* dims, int mode, size_t* bytes) {
+  if (!dims_ok(dims) || !bytes) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*dims, mode).total;
+  return MOE_OK;
+}
+
+moe_status moe_padded_rows(const moe_dims* dims, int64_t* rows) {
+  if (!dims_ok(dims) || !rows) return MOE_ERR_INVALID_ARG;
+  *rows = padded_rows(*dims);
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
+                     const float* logits_in, float* logits_out, int32_t* topk_idx, float* gates,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
+  if (dims->tokens > 0) {
+    if (!topk_idx || !gates) return MOE_ERR_INVALID_ARG;
+    if (!logits_in && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(shape_supported(dims));
+  MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
+  const Layout L = make_layout(*dims, MOE_FWD_ONLY);
+  const int64_t T = dims->tokens;
+  const int E = dims->experts;
+  if (T == 0) return MOE_OK;
+  const float* logits = logits_in;
+  if (!logits_in) {
+    float* dst = logits_out ? logits_out : at<float>(workspace, L.logits);
+    LayerPtrs p;
+    p.x = x;
+    p.w_router = w_router;
+    simt_router_logits(*dims, p, dst, stream);
+    logits = dst;
+  } else if (logits_out && logits_out != logits_in) {
+    if (cudaMemcpyAsync(logits_out, logits_in, sizeof(float) * T * E, cudaMemcpyDeviceToDevice,
+                        stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  launch_topk_softmax(logits, T, E, dims->top_k, topk_idx, gates, stream);
+  return cuda_status();
+}
+
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(dims) || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (dims->tokens > 0 && (!topk_idx || !perm || !inv_perm)) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(shape_supported(dims));
+  MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
+  const Layout L = make_layout(*dims, MOE_FWD_ONLY);
+  clear_status(at<int>(workspace, L.status), stream);
+  launch_permute(*dims, L, topk_idx, counts, offsets, perm, inv_perm, workspace, stream);
+  return cuda_status();
+}
+
+moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x, const float* gates,
+                               const void* w_gate, const void* w_up, const void* w_down,
+                               void* h_buf, void* a_gate_saved, void* a_up_saved, float* y_acc,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
+  if (dims->tokens > 0) {
+    if (!x || !gates || !w_gate || !w_up || !w_down || !h_buf || !y_acc)
+      return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_SAVE_FOR_BWD && (!a_gate_saved || !a_up_saved)) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(shape_supported(dims));
+  MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
+  if (dims->tokens == 0) return MOE_OK;
+  const Layout L = make_layout(*dims, MOE_FWD_ONLY);
+  LayerPtrs p;
+  p.x = x;
+  p.gates = gates;
+  p.w_gate = w_gate;
+  p.w_up = w_up;
+  p.w_down = w_down;
+  p.h_buf = h_buf;
+  p.a_gate = a_gate_saved;
+  p.a_up = a_up_saved;
+  p.y_acc = y_acc;
+  simt_grouped_fwd(*dims, L, mode, p, workspace, stream);
+  return cuda_status();
+}
+
+moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
+                       const void* ws_up, const void* ws_down, float* y_acc, void* y,
+                       void* hs_buf, void* as_gate_saved, void* as_up_saved, const void* upstream,
+                       float* loss, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
+  const bool shared = dims->shared_hidden > 0;
+  if (dims->tokens > 0) {
+    if (!y_acc || !y) return MOE_ERR_INVALID_ARG;
+    if (shared && (!x || !ws_gate || !ws_up || !ws_down || !hs_buf)) return MOE_ERR_INVALID_ARG;
+    if (shared && mode == MOE_SAVE_FOR_BWD && (!as_gate_saved || !as_up_saved))
+      return MOE_ERR_INVALID_ARG;
+  }
+  if (upstream && !loss) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(shape_supported(dims));
+  MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
+  const Layout L = make_layout(*dims, MOE_FWD_ONLY);
+  if (shared && dims->tokens > 0) {
+    LayerPtrs p;
+    p.x = x;
+    p.ws_gate = ws_gate;
+    p.ws_up = ws_up;
+    p.ws_down = ws_down;
+    p.hs_buf = hs_buf;
+    p.as_gate = as_gate_saved;
+    p.as_up = as_up_saved;
+    p.y_acc = y_acc;
+    simt_shared_fwd(*dims, L, mode, p, workspace, stream);
+  }
+  launch_finalize_y(*dims, L, y_acc, y, upstream, loss, workspace, stream);
+  return cuda_status();
+}
+
+moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, const void* w_router,
+                        const void* w_gate, const void* w_up, const void* w_down,
+                        const void* ws_gate, const void* ws_up, const void* ws_down,
+                        const int32_t* topk_idx, const float* gates, const void* a_gate_saved,
+                        const void* a_up_saved, const void* as_gate_saved, const void* as_up_saved,
+                        void* dx, float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
+                        float* dws_gate, float* dws_up, float* dws_down, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
+  const bool shared = dims->shared_hidden > 0;
+  if (!dw_router || !dw_gate || !dw_up || !dw_down || !w_router) return MOE_ERR_INVALID_ARG;
+  if (shared && (!dws_gate || !dws_up || !dws_down || !ws_gate || !ws_up || !ws_down))
+    return MOE_ERR_INVALID_ARG;
+  if (dims->tokens > 0) {
+    if (!dy || !x || !w_gate || !w_up || !w_down || !topk_idx || !gates || !a_gate_saved ||
+        !a_up_saved || !dx)
+      return MOE_ERR_INVALID_ARG;
+    if (shared && (!as_gate_saved || !as_up_saved)) return MOE_ERR_INVALID_ARG;
+  }
+  MOE_TRY(shape_supported(dims));
+  // the router backward keeps W_r^T and one dW_r column block in shared memory
+  if ((int64_t)dims->d_model * dims->experts > 49152 || dims->experts > 192)
+    return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_ws(dims, MOE_SAVE_FOR_BWD, workspace, workspace_bytes));
+  const Layout L = make_layout(*dims, MOE_SAVE_FOR_BWD);
+  const int64_t E = dims->experts, dm = dims->d_model, h = dims->d_hidden,
+                hs = dims->shared_hidden;
+  if (dims->tokens == 0) {
+    zero_fill_f32(dw_router, dm * E, stream);
+    zero_fill_f32(dw_gate, E * dm * h, stream);
+    zero_fill_f32(dw_up, E * dm * h, stream);
+    zero_fill_f32(dw_down, E * h * dm, stream);
+    if (shared) {
+      zero_fill_f32(dws_gate, dm * hs, stream);
+      zero_fill_f32(dws_up, dm * hs, stream);
+      zero_fill_f32(dws_down, hs * dm, stream);
+    }
+    return cuda_status();
+  }
+  LayerPtrs p;
+  p.dy = dy;
+  p.x = x;
+  p.w_router = w_router;
+  p.w_gate = w_gate;
+  p.w_up = w_up;
+  p.w_down = w_down;
+  p.ws_gate = ws_gate;
+  p.ws_up = ws_up;
+  p.ws_down = ws_down;
+  p.topk_idx = topk_idx;
+  p.gates = gates;
+  p.a_gate = const_cast<void*>(a_gate_saved);
+  p.a_up = const_cast<void*>(a_up_saved);
+  p.as_gate = const_cast<void*>(as_gate_saved);
+  p.as_up = const_cast<void*>(as_up_saved);
+  p.dx = dx;
+  p.dw_router = dw_router;
+  p.dw_gate = dw_gate;
+  p.dw_up = dw_up;
+  p.dw_down = dw_down;
+  p.dws_gate = dws_gate;
+  p.dws_up = dws_up;
+  p.dws_down = dws_down;
+  simt_backward_gemms(*dims, L, p, workspace, stream);
+  const int nt = (int)(h / 64);
+  launch_router_backward(*dims, L, p, nt, nt, workspace, stream);
+  return cuda_status();
+}
+
+moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                                  int32_t* detail) {
+  if (!workspace || workspace_bytes < 64) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int host[2] = {0, 0};
+  if (cudaMemcpy(host, workspace, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (host[0] != 0) {
+    const int zero[2] = {0, 0};
+    if (cudaMemcpy(workspace, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (detail) *detail = host[1];
+  return (moe_status)host[0];
+}
+
+}  // extern "C"

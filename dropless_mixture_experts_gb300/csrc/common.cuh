@@ -1,0 +1,105 @@
+// Shared definitions of the CUDA side of the MoE layer: element access for
+// the two storage types, the workspace layout and the device status word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kRowPad = 128;      // each expert's sorted rows start on a multiple of this
+constexpr int kPermRounds = 16;   // 32-pair rounds per warp chunk in the counting sort
+constexpr int kPermChunk = 32 * kPermRounds;
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+constexpr int kLossBlocks = 512;  // fixed partial count of the loss reduction
+constexpr int kRouterBwdRanges = 128;  // token ranges of the router-weight gradient partials
+
+// ---- element access ---------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+// ---- device status word ---------------------------------------------------
+// status[0] = first error code (moe_status), status[1] = detail word.
+__device__ __forceinline__ void report_error(int* status, int code, int detail) {
+  if (atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// ---- workspace layout -------------------------------------------------------
+struct Layout {
+  size_t status, warp_counts, warp_base, counts, poff, rowpair, pad_inv, tiles, ntiles,
+      loss_part, logits;
+  size_t dg_part, dA, gH, dx_acc, dAs, gHs, dsel, dwr_part;
+  size_t total;
+  int64_t P, PPcap, MTcap, NWc;
+  int elem;  // bytes per storage element
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int64_t padded_rows(const moe_dims& d) {
+  int64_t P = d.tokens * (int64_t)d.top_k;
+  int64_t cap = P + (int64_t)d.experts * (kRowPad - 1);
+  return (cap + kRowPad - 1) / kRowPad * kRowPad;
+}
+
+inline Layout make_layout(const moe_dims& d, int mode) {
+  Layout L{};
+  L.elem = d.dtype == MOE_BF16 ? 2 : 4;
+  L.P = d.tokens * (int64_t)d.top_k;
+  L.PPcap = padded_rows(d);
+  L.MTcap = L.PPcap / kRowPad;
+  L.NWc = (L.P + kPermChunk - 1) / kPermChunk;
+  const int64_t E = d.experts, T = d.tokens, h = d.d_hidden, dm = d.d_model,
+                hs = d.shared_hidden;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + (bytes ? bytes : 1), 256);
+    return at;
+  };
+  L.status = take(64);
+  L.warp_counts = take(sizeof(int) * L.NWc * E);
+  L.warp_base = take(sizeof(int) * L.NWc * E);
+  L.counts = take(sizeof(int) * E);
+  L.poff = take(sizeof(int) * (E + 1));
+  L.rowpair = take(sizeof(int) * L.PPcap);
+  L.pad_inv = take(sizeof(int) * L.P);
+  L.tiles = take(sizeof(int4) * L.MTcap);
+  L.ntiles = take(sizeof(int) * 4);
+  L.loss_part = take(sizeof(float) * kLossBlocks);
+  L.logits = take(sizeof(float) * T * E);
+  if (mode == MOE_SAVE_FOR_BWD) {
+    L.dg_part = take(sizeof(float) * L.PPcap * (h / 64));
+    L.dA = take((size_t)L.elem * L.PPcap * 2 * h);
+    L.gH = take((size_t)L.elem * L.PPcap * h);
+    L.dx_acc = take(sizeof(float) * T * dm);
+    L.dAs = take((size_t)L.elem * T * 2 * hs);
+    L.gHs = take((size_t)L.elem * T * hs);
+    L.dsel = take(sizeof(float) * T * d.top_k);
+    L.dwr_part = take(sizeof(float) * kRouterBwdRanges * dm * E);
+  }
+  L.total = o;
+  return L;
+}
+
+template <typename T>
+__host__ __device__ __forceinline__ T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(base) + off);
+}
+
+// One 128-row tile of the expert-sorted (padded) rows.
+// x = expert, y = first padded row, z = number of real rows (1..128), w = unused.
+using TileEntry = int4;
+
+}  // namespace moe

@@ -1,0 +1,624 @@
+// Grouped expert GEMMs on the CUDA cores (FFMA, float32 accumulation).
+//
+// This is the strict-float32 path of the layer (no TF32 rounding of the
+// operands), and it serves every contraction of the forward and the train
+// step:
+//   LOGITS  logits = x W_r
+//   GU      a_g = x_t W_gate[e], a_u = x_t W_up[e], H = silu(a_g) * a_u
+//           (gather of the token rows fused into the operand load)
+//   DOWN    y_acc[t] += gate * (H W_down[e])   (combine fused in the epilogue)
+//   DZ      Z = dy_t W_down[e]^T; dgate = <Z, H>; dA_g, dA_u by the SwiGLU
+//           chain rule; gH = gate * H kept for the W_down gradient
+//   DX      dx_acc[t] += dA_g W_gate[e]^T + dA_u W_up[e]^T
+//   DWD     dW_down[e] = sum_r gH_r^T dy_t           (ragged K = expert rows)
+//   DWGU    dW_gate[e] | dW_up[e] = sum_r x_t^T [dA_g | dA_u]
+// Each kind also runs densely (one expert, identity row map) for the shared
+// expert.  The method these follow: the experts_grouped_swiglu and
+// unpermute_combine pieces of kernel_gmm_gpu.json and the value_and_grad
+// train step of gpu_moe_h100.json.
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+enum Kind { LOGITS, GU, DOWN, DZ, DX, DWD, DWGU };
+
+constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
+
+struct SimtArgs {
+  // operands
+  const void* A = nullptr;
+  const void* B = nullptr;
+  const void* B2 = nullptr;  // GU: W_up; DX: W_up (second half of K)
+  int lda = 0, ldb = 0;
+  int64_t b_estride = 0;     // elements between consecutive experts' B matrices
+  int N = 0, K = 0;          // output columns; reduction length of the row GEMMs
+  int64_t rows = 0;          // dense kinds: number of rows
+  int h = 0;                 // DX: K split point; DWGU: N split point; DZ: hidden width
+  // dispatch tables
+  const int4* tiles = nullptr;
+  const int* ntiles = nullptr;
+  const int32_t* rowpair = nullptr;
+  int top_k = 1;
+  const int* counts = nullptr;
+  const int* poff = nullptr;
+  const float* gates = nullptr;
+  // epilogue operands / outputs
+  void* h_out = nullptr;         // GU
+  void* ag_out = nullptr;        // GU (train)
+  void* au_out = nullptr;        // GU (train)
+  const void* ag_in = nullptr;   // DZ
+  const void* au_in = nullptr;   // DZ
+  void* dA_out = nullptr;        // DZ  [rows, 2h]
+  void* gH_out = nullptr;        // DZ  [rows, h]
+  float* dg_part = nullptr;      // DZ  [rows, dg_ld]
+  int dg_ld = 0;
+  float* acc_out = nullptr;      // LOGITS / DOWN / DX / DWD / DWGU (gate half)
+  float* acc_out2 = nullptr;     // DWGU (up half)
+  int ldo = 0;
+  int n_ntiles = 1, n_mtiles = 1;
+};
+
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p, bool ok) {
+  if (!ok) return make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (sizeof(T) == 4) {
+    return *reinterpret_cast<const float4*>(p);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+    const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float load1(const T* p, bool ok) {
+  return ok ? to_f32(*p) : 0.f;
+}
+
+__device__ __forceinline__ float comp(const float4& v, int q) {
+  return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
+}
+
+template <Kind KIND, typename T, bool ROUTED>
+__global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
+  constexpr bool A_KCONTIG = (KIND == LOGITS || KIND == GU || KIND == DOWN || KIND == DZ ||
+                              KIND == DX);
+  constexpr bool B_KCONTIG = (KIND == DZ || KIND == DX);
+  constexpr bool DUAL = (KIND == GU);
+  constexpr bool DW = (KIND == DWD || KIND == DWGU);
+
+  __shared__ __align__(16) float As[BK][BM + 4];
+  __shared__ __align__(16) float Bs[BK][BN + 4];
+  __shared__ __align__(16) float Bs2[DUAL ? BK : 1][BN + 4];
+  __shared__ int s_tok[BM];  // source rows of the tile (row kinds)
+
+  const int tid = threadIdx.x;
+  const int ntile = blockIdx.x % a.n_ntiles;
+  const int rest = blockIdx.x / a.n_ntiles;
+  const int n0 = ntile * BN;
+
+  int e = 0;
+  int64_t row0 = 0;     // first output row (row kinds) / first K row (DW kinds)
+  int nvalid = 0;       // row kinds: valid rows in this tile
+  int m0 = 0;           // DW kinds: first output row
+  int64_t kbeg = 0, kend = 0;
+
+  if constexpr (!DW) {
+    if constexpr (ROUTED) {
+      const int mt = rest >> 1, half = rest & 1;
+      if (mt >= a.ntiles[0]) return;
+      const int4 tile = a.tiles[mt];
+      e = tile.x;
+      row0 = tile.y + half * BM;
+      nvalid = min(BM, tile.z - half * BM);
+      if (nvalid <= 0) return;
+    } else {
+      row0 = (int64_t)rest * BM;
+      if (row0 >= a.rows) return;
+      nvalid = a.rows - row0 < BM ? (int)(a.rows - row0) : BM;
+    }
+    for (int i = tid; i < BM; i += NT) {
+      int64_t src = row0 + i;
+      if constexpr (ROUTED) {
+        if (KIND == GU || KIND == DZ) {
+          const int32_t p = i < nvalid ? a.rowpair[row0 + i] : -1;
+          src = p >= 0 ? p / a.top_k : 0;
+        }
+      }
+      s_tok[i] = (int)src;  // token (gathered kinds) or sorted row
+    }
+    kbeg = 0;
+    kend = a.K;
+  } else {
+    const int mt = rest % a.n_mtiles;
+    e = rest / a.n_mtiles;
+    m0 = mt * BM;
+    if constexpr (ROUTED) {
+      kbeg = a.poff[e];
+      kend = kbeg + a.counts[e];
+    } else {
+      kbeg = 0;
+      kend = a.rows;
+    }
+  }
+  __syncthreads();
+
+  const T* A = reinterpret_cast<const T*>(a.A);
+  const T* B = reinterpret_cast<const T*>(a.B) + (ROUTED ? a.b_estride * e : 0);
+  const T* B2 = a.B2 ? reinterpret_cast<const T*>(a.B2) + (ROUTED ? a.b_estride * e : 0) : nullptr;
+
+  float acc[4][4] = {};
+  float acc2[DUAL ? 4 : 1][DUAL ? 4 : 1] = {};
+  const int ty = tid / 16, tx = tid % 16;
+
+  float4 ra, rb, rb2;
+  auto gload = [&](int64_t kt) {
+    // ---- A ----
+    if constexpr (A_KCONTIG) {
+      const int m = tid / 4, k4 = (tid % 4) * 4;
+      const bool ok = m < nvalid || (KIND == DOWN || KIND == DX);
+      const int64_t src = (KIND == LOGITS || !ROUTED) ? row0 + m : (int64_t)s_tok[m];
+      const bool in = ok && (ROUTED || row0 + m < a.rows);
+      if constexpr (KIND == LOGITS) {
+        ra = load4(A + src * a.lda + kt + k4, in);
+      } else {
+        ra = load4(A + src * a.lda + kt + k4, in);
+      }
+    } else {
+      const int kl = tid / 16, m4 = (tid % 16) * 4;
+      const int64_t r = kbeg + kt + kl;
+      const bool ok = r < kend;
+      int64_t src = r;
+      if (KIND == DWGU && ROUTED && ok) src = a.rowpair[r] / a.top_k;
+      ra = load4(A + src * a.lda + m0 + m4, ok);
+    }
+    // ---- B ----
+    if constexpr (!B_KCONTIG) {
+      const int kl = tid / 16, n4 = (tid % 16) * 4;
+      if constexpr (KIND == LOGITS) {
+        const int64_t kk = kt + kl;
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = load1(B + kk * a.ldb + n0 + n4 + q, n0 + n4 + q < a.N);
+        rb = make_float4(v[0], v[1], v[2], v[3]);
+      } else if constexpr (DW) {
+        const int64_t r = kbeg + kt + kl;
+        const bool ok = r < kend;
+        int64_t src = r;
+        if (KIND == DWD && ROUTED && ok) src = a.rowpair[r] / a.top_k;
+        rb = load4(B + src * a.ldb + n0 + n4, ok);
+      } else {
+        const int64_t kk = kt + kl;
+        rb = load4(B + kk * a.ldb + n0 + n4, true);
+        if constexpr (DUAL) rb2 = load4(B2 + kk * a.ldb + n0 + n4, true);
+      }
+    } else {
+      const int n = tid / 4, k4 = (tid % 4) * 4;
+      const int64_t kk = kt + k4;
+      if constexpr (KIND == DX) {
+        const T* src = kk < a.h ? B + (int64_t)(n0 + n) * a.ldb + kk
+                                : B2 + (int64_t)(n0 + n) * a.ldb + (kk - a.h);
+        rb = load4(src, true);
+      } else {
+        rb = load4(B + (int64_t)(n0 + n) * a.ldb + kk, true);
+      }
+    }
+  };
+  auto sstore = [&]() {
+    if constexpr (A_KCONTIG) {
+      const int m = tid / 4, k4 = (tid % 4) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) As[k4 + q][m] = comp(ra, q);
+    } else {
+      const int kl = tid / 16, m4 = (tid % 16) * 4;
+      *reinterpret_cast<float4*>(&As[kl][m4]) = ra;
+    }
+    if constexpr (!B_KCONTIG) {
+      const int kl = tid / 16, n4 = (tid % 16) * 4;
+      *reinterpret_cast<float4*>(&Bs[kl][n4]) = rb;
+      if constexpr (DUAL) *reinterpret_cast<float4*>(&Bs2[kl][n4]) = rb2;
+    } else {
+      const int n = tid / 4, k4 = (tid % 4) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) Bs[k4 + q][n] = comp(rb, q);
+    }
+  };
+
+  const int64_t klen = kend - kbeg;
+  if (klen > 0) gload(0);
+  for (int64_t kt = 0; kt < klen; kt += BK) {
+    __syncthreads();
+    sstore();
+    __syncthreads();
+    if (kt + BK < klen) gload(kt + BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float am[4] = {av.x, av.y, av.z, av.w};
+      const float bn[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(am[i], bn[j], acc[i][j]);
+      if constexpr (DUAL) {
+        const float4 b2 = *reinterpret_cast<const float4*>(&Bs2[kk][tx * 4]);
+        const float bn2[4] = {b2.x, b2.y, b2.z, b2.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(am[i], bn2[j], acc2[i][j]);
+      }
+    }
+  }
+
+  // ---------------- epilogues ----------------
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = ty * 4 + i;
+    const int64_t r = row0 + m;
+    if constexpr (KIND == LOGITS) {
+      if (r < a.rows)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + tx * 4 + j;
+          if (n < a.N) a.acc_out[r * a.ldo + n] = acc[i][j];
+        }
+    } else if constexpr (KIND == GU) {
+      if (!ROUTED && r >= a.rows) continue;
+      T* H = reinterpret_cast<T*>(a.h_out);
+      T* AG = reinterpret_cast<T*>(a.ag_out);
+      T* AU = reinterpret_cast<T*>(a.au_out);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int n = n0 + tx * 4 + j;
+        // round to the storage type first, so H is computed from exactly the
+        // values a backward pass reads back
+        const float g = to_f32(from_f32<T>(acc[i][j]));
+        const float u = to_f32(from_f32<T>(acc2[i][j]));
+        H[r * a.ldo + n] = from_f32<T>(g * sigmoidf_(g) * u);
+        if (AG) {
+          AG[r * a.ldo + n] = from_f32<T>(g);
+          AU[r * a.ldo + n] = from_f32<T>(u);
+        }
+      }
+    } else if constexpr (KIND == DOWN) {
+      if (m >= nvalid) continue;
+      if constexpr (ROUTED) {
+        const int32_t p = a.rowpair[r];
+        const int64_t t = p / a.top_k;
+        const float gt = a.gates[p];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          atomicAdd(&a.acc_out[t * a.ldo + n0 + tx * 4 + j], gt * acc[i][j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a.acc_out[r * a.ldo + n0 + tx * 4 + j] += acc[i][j];
+      }
+    } else if constexpr (KIND == DZ) {
+      const bool exists = ROUTED || r < a.rows;
+      const bool valid = m < nvalid;
+      float gt = 1.f;
+      if constexpr (ROUTED) gt = valid ? a.gates[a.rowpair[r]] : 0.f;
+      const T* AG = reinterpret_cast<const T*>(a.ag_in);
+      const T* AU = reinterpret_cast<const T*>(a.au_in);
+      T* dA = reinterpret_cast<T*>(a.dA_out);
+      T* gH = reinterpret_cast<T*>(a.gH_out);
+      const int64_t h = a.h;
+      float dgp = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int n = n0 + tx * 4 + j;
+        const float z = acc[i][j];
+        const float ag = valid ? to_f32(AG[r * h + n]) : 0.f;
+        const float au = valid ? to_f32(AU[r * h + n]) : 0.f;
+        const float s = sigmoidf_(ag);
+        const float sl = ag * s;
+        const float hv = to_f32(from_f32<T>(sl * au));  // H as the forward stored it
+        dgp += z * hv;
+        const float dh = gt * z;
+        const float dau = dh * sl;
+        const float dag = dh * au * s * (1.f + ag * (1.f - s));
+        if (exists) {
+          dA[r * 2 * h + n] = from_f32<T>(valid ? dag : 0.f);
+          dA[r * 2 * h + h + n] = from_f32<T>(valid ? dau : 0.f);
+          gH[r * h + n] = from_f32<T>(valid ? gt * hv : 0.f);
+        }
+      }
+      // the 16 threads of one row are 16 consecutive lanes of a warp
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, o);
+      if (ROUTED && tx == 0 && a.dg_part) a.dg_part[r * a.dg_ld + ntile] = valid ? dgp : 0.f;
+    } else if constexpr (KIND == DX) {
+      if (m >= nvalid) continue;
+      if constexpr (ROUTED) {
+        const int64_t t = a.rowpair[r] / a.top_k;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) atomicAdd(&a.acc_out[t * a.ldo + n0 + tx * 4 + j], acc[i][j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a.acc_out[r * a.ldo + n0 + tx * 4 + j] = acc[i][j];
+      }
+    } else {  // DWD / DWGU: plain stores of the expert's gradient tile
+      const int64_t om = m0 + m;
+      const int64_t eoff = (int64_t)e * a.n_mtiles * BM;  // expert offset in rows
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int n = n0 + tx * 4 + j;
+        if constexpr (KIND == DWGU) {
+          if (n < a.h)
+            a.acc_out[(eoff + om) * a.h + n] = acc[i][j];
+          else
+            a.acc_out2[(eoff + om) * a.h + (n - a.h)] = acc[i][j];
+        } else {
+          a.acc_out[(eoff + om) * a.ldo + n] = acc[i][j];
+        }
+      }
+    }
+  }
+}
+
+template <Kind KIND, typename T, bool ROUTED>
+void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
+  if (blocks <= 0) return;
+  static const char* names[] = {"simt_logits", "simt_gateup", "simt_down", "simt_dz", "simt_dx",
+                                "simt_dw_down", "simt_dw_gateup"};
+  MOE_LAUNCH(names[KIND], s, simt_gemm_kernel<KIND, T, ROUTED><<<(unsigned)blocks, NT, 0, s>>>(a));
+}
+
+template <typename T>
+void router_logits_t(const moe_dims& d, const LayerPtrs& p, float* logits, cudaStream_t s) {
+  SimtArgs a;
+  a.A = p.x;
+  a.lda = d.d_model;
+  a.B = p.w_router;
+  a.ldb = d.experts;
+  a.N = d.experts;
+  a.K = d.d_model;
+  a.rows = d.tokens;
+  a.acc_out = logits;
+  a.ldo = d.experts;
+  a.n_ntiles = (d.experts + BN - 1) / BN;
+  launch<LOGITS, T, false>(a, a.n_ntiles * ((d.tokens + BM - 1) / BM), s);
+}
+
+template <typename T>
+void grouped_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                   cudaStream_t s) {
+  const int h = d.d_hidden, dm = d.d_model;
+  zero_fill_f32(p.y_acc, d.tokens * (int64_t)dm, s);
+  SimtArgs a;
+  a.tiles = at<int4>(ws, L.tiles);
+  a.ntiles = at<int>(ws, L.ntiles);
+  a.rowpair = at<int32_t>(ws, L.rowpair);
+  a.top_k = d.top_k;
+  a.gates = p.gates;
+  // gate/up projection with the SwiGLU epilogue
+  a.A = p.x;
+  a.lda = dm;
+  a.B = p.w_gate;
+  a.B2 = p.w_up;
+  a.ldb = h;
+  a.b_estride = (int64_t)dm * h;
+  a.N = h;
+  a.K = dm;
+  a.h_out = p.h_buf;
+  a.ag_out = mode == MOE_SAVE_FOR_BWD ? p.a_gate : nullptr;
+  a.au_out = mode == MOE_SAVE_FOR_BWD ? p.a_up : nullptr;
+  a.ldo = h;
+  a.n_ntiles = h / BN;
+  launch<GU, T, true>(a, a.n_ntiles * 2 * L.MTcap, s);
+  // down projection with the gate-weighted combine
+  SimtArgs b = a;
+  b.A = p.h_buf;
+  b.lda = h;
+  b.B = p.w_down;
+  b.B2 = nullptr;
+  b.ldb = dm;
+  b.b_estride = (int64_t)h * dm;
+  b.N = dm;
+  b.K = h;
+  b.acc_out = p.y_acc;
+  b.ldo = dm;
+  b.n_ntiles = dm / BN;
+  launch<DOWN, T, true>(b, b.n_ntiles * 2 * L.MTcap, s);
+}
+
+template <typename T>
+void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                  cudaStream_t s) {
+  const int hs = d.shared_hidden, dm = d.d_model;
+  const int64_t mt = (d.tokens + BM - 1) / BM;
+  SimtArgs a;
+  a.rows = d.tokens;
+  a.A = p.x;
+  a.lda = dm;
+  a.B = p.ws_gate;
+  a.B2 = p.ws_up;
+  a.ldb = hs;
+  a.N = hs;
+  a.K = dm;
+  a.h_out = p.hs_buf;
+  a.ag_out = mode == MOE_SAVE_FOR_BWD ? p.as_gate : nullptr;
+  a.au_out = mode == MOE_SAVE_FOR_BWD ? p.as_up : nullptr;
+  a.ldo = hs;
+  a.n_ntiles = hs / BN;
+  launch<GU, T, false>(a, a.n_ntiles * mt, s);
+  SimtArgs b = a;
+  b.A = p.hs_buf;
+  b.lda = hs;
+  b.B = p.ws_down;
+  b.B2 = nullptr;
+  b.ldb = dm;
+  b.N = dm;
+  b.K = hs;
+  b.acc_out = p.y_acc;
+  b.ldo = dm;
+  b.n_ntiles = dm / BN;
+  launch<DOWN, T, false>(b, b.n_ntiles * mt, s);
+  (void)L;
+  (void)ws;
+}
+
+template <typename T>
+void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, cudaStream_t s) {
+  const int h = d.d_hidden, dm = d.d_model, E = d.experts, hs = d.shared_hidden;
+  float* dx_acc = at<float>(ws, L.dx_acc);
+  void* dA = at<void>(ws, L.dA);
+  void* gH = at<void>(ws, L.gH);
+  const int64_t mt_dense = (d.tokens + BM - 1) / BM;
+
+  if (hs > 0) {
+    void* dAs = at<void>(ws, L.dAs);
+    void* gHs = at<void>(ws, L.gHs);
+    // Z_s = dy Ws_down^T with the SwiGLU chain rule (gate = 1)
+    SimtArgs z;
+    z.rows = d.tokens;
+    z.A = p.dy;
+    z.lda = dm;
+    z.B = p.ws_down;
+    z.ldb = dm;
+    z.N = hs;
+    z.K = dm;
+    z.h = hs;
+    z.ag_in = p.as_gate;
+    z.au_in = p.as_up;
+    z.dA_out = dAs;
+    z.gH_out = gHs;
+    z.n_ntiles = hs / BN;
+    launch<DZ, T, false>(z, z.n_ntiles * mt_dense, s);
+    // dx_acc = dAs [Ws_gate | Ws_up]^T   (plain store: first writer)
+    SimtArgs x;
+    x.rows = d.tokens;
+    x.A = dAs;
+    x.lda = 2 * hs;
+    x.B = p.ws_gate;
+    x.B2 = p.ws_up;
+    x.ldb = hs;
+    x.N = dm;
+    x.K = 2 * hs;
+    x.h = hs;
+    x.acc_out = dx_acc;
+    x.ldo = dm;
+    x.n_ntiles = dm / BN;
+    launch<DX, T, false>(x, x.n_ntiles * mt_dense, s);
+    // dWs_down = Hs^T dy ; dWs_gate | dWs_up = x^T dAs
+    SimtArgs w;
+    w.rows = d.tokens;
+    w.A = gHs;
+    w.lda = hs;
+    w.B = p.dy;
+    w.ldb = dm;
+    w.acc_out = p.dws_down;
+    w.ldo = dm;
+    w.n_mtiles = hs / BM;
+    w.n_ntiles = dm / BN;
+    launch<DWD, T, false>(w, (int64_t)w.n_ntiles * w.n_mtiles, s);
+    SimtArgs g;
+    g.rows = d.tokens;
+    g.A = p.x;
+    g.lda = dm;
+    g.B = dAs;
+    g.ldb = 2 * hs;
+    g.h = hs;
+    g.acc_out = p.dws_gate;
+    g.acc_out2 = p.dws_up;
+    g.n_mtiles = dm / BM;
+    g.n_ntiles = 2 * hs / BN;
+    launch<DWGU, T, false>(g, (int64_t)g.n_ntiles * g.n_mtiles, s);
+  } else {
+    zero_fill_f32(dx_acc, d.tokens * (int64_t)dm, s);
+  }
+
+  // routed experts
+  SimtArgs z;
+  z.tiles = at<int4>(ws, L.tiles);
+  z.ntiles = at<int>(ws, L.ntiles);
+  z.rowpair = at<int32_t>(ws, L.rowpair);
+  z.top_k = d.top_k;
+  z.gates = p.gates;
+  z.counts = at<int>(ws, L.counts);
+  z.poff = at<int>(ws, L.poff);
+  SimtArgs base = z;
+  z.A = p.dy;
+  z.lda = dm;
+  z.B = p.w_down;
+  z.ldb = dm;
+  z.b_estride = (int64_t)h * dm;
+  z.N = h;
+  z.K = dm;
+  z.h = h;
+  z.ag_in = p.a_gate;
+  z.au_in = p.a_up;
+  z.dA_out = dA;
+  z.gH_out = gH;
+  z.dg_part = at<float>(ws, L.dg_part);
+  z.dg_ld = h / BN;
+  z.n_ntiles = h / BN;
+  launch<DZ, T, true>(z, z.n_ntiles * 2 * L.MTcap, s);
+
+  SimtArgs x = base;
+  x.A = dA;
+  x.lda = 2 * h;
+  x.B = p.w_gate;
+  x.B2 = p.w_up;
+  x.ldb = h;
+  x.b_estride = (int64_t)dm * h;
+  x.N = dm;
+  x.K = 2 * h;
+  x.h = h;
+  x.acc_out = dx_acc;
+  x.ldo = dm;
+  x.n_ntiles = dm / BN;
+  launch<DX, T, true>(x, x.n_ntiles * 2 * L.MTcap, s);
+
+  SimtArgs w = base;
+  w.A = gH;
+  w.lda = h;
+  w.B = p.dy;
+  w.ldb = dm;
+  w.acc_out = p.dw_down;
+  w.ldo = dm;
+  w.n_mtiles = h / BM;
+  w.n_ntiles = dm / BN;
+  launch<DWD, T, true>(w, (int64_t)w.n_ntiles * w.n_mtiles * E, s);
+
+  SimtArgs g = base;
+  g.A = p.x;
+  g.lda = dm;
+  g.B = dA;
+  g.ldb = 2 * h;
+  g.h = h;
+  g.acc_out = p.dw_gate;
+  g.acc_out2 = p.dw_up;
+  g.n_mtiles = dm / BM;
+  g.n_ntiles = 2 * h / BN;
+  launch<DWGU, T, true>(g, (int64_t)g.n_ntiles * g.n_mtiles * E, s);
+}
+
+}  // namespace
+
+void simt_router_logits(const moe_dims& d, const LayerPtrs& p, float* logits, cudaStream_t s) {
+  if (d.dtype == MOE_BF16) router_logits_t<__nv_bfloat16>(d, p, logits, s);
+  else router_logits_t<float>(d, p, logits, s);
+}
+void simt_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                      cudaStream_t s) {
+  if (d.dtype == MOE_BF16) grouped_fwd_t<__nv_bfloat16>(d, L, mode, p, ws, s);
+  else grouped_fwd_t<float>(d, L, mode, p, ws, s);
+}
+void simt_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                     cudaStream_t s) {
+  if (d.dtype == MOE_BF16) shared_fwd_t<__nv_bfloat16>(d, L, mode, p, ws, s);
+  else shared_fwd_t<float>(d, L, mode, p, ws, s);
+}
+void simt_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                         cudaStream_t s) {
+  if (d.dtype == MOE_BF16) backward_t<__nv_bfloat16>(d, L, p, ws, s);
+  else backward_t<float>(d, L, p, ws, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,79 @@
+// Launchers of the layer's kernels (host side), shared by the C ABI.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// kernel timing records (profile.cu); MOE_LAUNCH brackets one launch
+void prof_begin(const char* name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+#define MOE_LAUNCH(name, stream, ...)   \
+  do {                                  \
+    ::moe::prof_begin(name, stream);    \
+    __VA_ARGS__;                        \
+    ::moe::prof_end(stream);            \
+  } while (0)
+
+// utility kernels (misc.cu)
+void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s);
+void zero_fill_f32(float* p, int64_t n, cudaStream_t s);
+void clear_status(int* status, cudaStream_t s);
+
+// routing and permutation (route_permute.cu)
+void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
+                         float* gates, cudaStream_t s);
+void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
+                    cudaStream_t s);
+
+// Operands and outputs of one layer invocation, as the grouped kernels see
+// them.  Pointers are device pointers; storage type per dims.dtype.
+struct LayerPtrs {
+  const void* x = nullptr;
+  const void* dy = nullptr;
+  const void* w_router = nullptr;
+  const void* w_gate = nullptr;
+  const void* w_up = nullptr;
+  const void* w_down = nullptr;
+  const void* ws_gate = nullptr;
+  const void* ws_up = nullptr;
+  const void* ws_down = nullptr;
+  const float* gates = nullptr;
+  const int32_t* topk_idx = nullptr;
+  // forward outputs / saved activations
+  void* h_buf = nullptr;
+  void* a_gate = nullptr;
+  void* a_up = nullptr;
+  void* hs_buf = nullptr;
+  void* as_gate = nullptr;
+  void* as_up = nullptr;
+  float* y_acc = nullptr;
+  float* logits = nullptr;
+  // backward outputs
+  void* dx = nullptr;
+  float* dw_router = nullptr;
+  float* dw_gate = nullptr;
+  float* dw_up = nullptr;
+  float* dw_down = nullptr;
+  float* dws_gate = nullptr;
+  float* dws_up = nullptr;
+  float* dws_down = nullptr;
+};
+
+// grouped expert GEMMs (gemm_simt.cu: float32 storage)
+void simt_router_logits(const moe_dims& d, const LayerPtrs& p, float* logits, cudaStream_t s);
+void simt_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                      cudaStream_t s);
+void simt_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                     cudaStream_t s);
+void simt_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                         cudaStream_t s);
+
+// combine / loss / router backward (combine.cu)
+void launch_finalize_y(const moe_dims& d, const Layout& L, const float* y_acc, void* y,
+                       const void* upstream, float* loss, void* ws, cudaStream_t s);
+void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dz_ntiles,
+                            int dg_ld, void* ws, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,284 @@
+// Routing (top-k selection + softmax over the selected logits) and the
+// counting-sort permutation of token-expert pairs.
+//
+// Routing: benchmark page gpu_moe_h100.json (top_k field) and the layer
+// structure fixed by gpu_nn.json's parameter count: per token the k largest
+// router logits, ties to the lower expert index, slots in descending order,
+// gates = softmax of the selected logits.
+//
+// Permutation: the `sort_permute` piece of kernel_gmm_gpu.json (dispatch
+// `sorted`): pairs p = t*k + j ordered by expert, stable in p, plus an
+// expert-padded copy of the order in which every expert's rows start on a
+// multiple of 128 (the row tiles of the grouped GEMMs never straddle two
+// experts).
+#include "kernels.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Top-k over one row of logits held by a warp: lane l owns logits
+// l, l+32, ..., and k rounds of a butterfly arg-max pick the experts.
+// `better` is the total order (larger logit first, lower index on equality).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+constexpr int kMaxPerLane = kMaxExperts / 32;
+
+__global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits,
+                                                           int64_t T, int E, int k,
+                                                           int32_t* __restrict__ idx_out,
+                                                           float* __restrict__ gates_out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int per_lane = (E + 31) >> 5;
+  for (int64_t t = warp; t < T; t += nwarps) {
+    float v[kMaxPerLane];
+    unsigned live = 0u;  // bit j: entry lane + 32*j not yet taken
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+      const int e = lane + 32 * j;
+      const bool ok = (j < per_lane) && (e < E);
+      if (ok) live |= 1u << j;
+      v[j] = ok ? logits[t * E + e] : -INFINITY;
+    }
+    float my_sel = 0.f;
+    int my_idx = 0;
+    float top = 0.f;
+    for (int r = 0; r < k; ++r) {
+      // best live entry of this lane
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < kMaxPerLane; ++j) {
+        const int e = lane + 32 * j;
+        if (((live >> j) & 1u) && (bi == 0x7fffffff || better(v[j], e, bv, bi))) {
+          bv = v[j];
+          bi = e;
+        }
+      }
+      // butterfly arg-max over the warp (the order is total, so every lane
+      // ends with the same winner)
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, s);
+        if (oi != 0x7fffffff && (bi == 0x7fffffff || better(ov, oi, bv, bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) live &= ~(1u << (bi >> 5));
+      if (r == 0) top = bv;
+      if (lane == r) {
+        my_sel = bv;
+        my_idx = bi;
+      }
+    }
+    const float z = lane < k ? expf(my_sel - top) : 0.f;
+    float sum = z;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s);
+    if (lane < k) {
+      idx_out[t * k + lane] = my_idx;
+      gates_out[t * k + lane] = z / sum;
+    }
+  }
+}
+
+void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
+                         float* gates, cudaStream_t s) {
+  if (T == 0) return;
+  int64_t warps = T;
+  int64_t blocks = (warps + 7) / 8;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  MOE_LAUNCH("topk_softmax", s, topk_softmax_kernel<<<(unsigned)blocks, 256, 0, s>>>(logits, T, E, k, idx, gates));
+}
+
+// ---------------------------------------------------------------------------
+// Counting sort.  Warp w owns pairs [w*kPermChunk, (w+1)*kPermChunk) and
+// walks them in rounds of 32; within a round, lanes holding the same expert
+// find each other with __match_any_sync, so a pair's rank inside its warp
+// chunk is (earlier rounds' count for its expert) + (lower lanes with the
+// same expert).  Both passes run the same walk, so the ranks agree.
+// ---------------------------------------------------------------------------
+template <bool SCATTER>
+__device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int64_t P, int E,
+                                           int64_t chunk, int* hist, const int* base_e,
+                                           const int* off_e, const int* poff_e, int32_t* perm,
+                                           int32_t* inv_perm, int32_t* rowpair,
+                                           int32_t* pad_inv, int* status) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r = 0; r < kPermRounds; ++r) {
+    const int64_t p = chunk * kPermChunk + (int64_t)r * 32 + lane;
+    int e = -1;
+    if (p < P) {
+      e = idx[p];
+      if (e < 0 || e >= E) {
+        report_error(status, MOE_ERR_DEVICE_CHECK, 1);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int before = __popc(peers & lt);
+    int rank = 0;
+    if (e >= 0) rank = hist[e] + before;
+    __syncwarp();
+    if (e >= 0 && before == 0) hist[e] += __popc(peers);
+    __syncwarp();
+    if (SCATTER && e >= 0) {
+      const int within = base_e[e] + rank;  // rank of the pair inside its expert
+      const int pos = off_e[e] + within;
+      const int ppos = poff_e[e] + within;
+      perm[pos] = (int32_t)p;
+      inv_perm[p] = pos;
+      rowpair[ppos] = (int32_t)p;
+      pad_inv[p] = ppos;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t P,
+                                                        int E, int64_t NW, int* warp_counts,
+                                                        int* status) {
+  __shared__ int hist[8][kMaxExperts];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
+  for (int e = lane; e < E; e += 32) hist[w][e] = 0;
+  __syncwarp();
+  if (chunk >= NW) return;
+  walk_chunk<false>(idx, P, E, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, nullptr,
+                    nullptr, nullptr, status);
+  for (int e = lane; e < E; e += 32) warp_counts[chunk * E + e] = hist[w][e];
+}
+
+// Exclusive scan of column e of warp_counts (one block per expert).
+__global__ void __launch_bounds__(1024) perm_colscan_kernel(const int* __restrict__ warp_counts,
+                                                            int64_t NW, int E, int* warp_base,
+                                                            int* counts_ws) {
+  __shared__ int part[1024];
+  const int e = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int64_t per = (NW + 1023) / 1024;
+  const int64_t lo = tid * per;
+  const int64_t hi = lo + per < NW ? lo + per : NW;
+  int s = 0;
+  for (int64_t w = lo; w < hi; ++w) s += warp_counts[w * E + e];
+  part[tid] = s;
+  __syncthreads();
+  // Hillis-Steele inclusive scan over 1024 partials
+  for (int o = 1; o < 1024; o <<= 1) {
+    int v = tid >= o ? part[tid - o] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int run = tid ? part[tid - 1] : 0;
+  for (int64_t w = lo; w < hi; ++w) {
+    const int c = warp_counts[w * E + e];
+    warp_base[w * E + e] = run;
+    run += c;
+  }
+  if (tid == 1023) counts_ws[e] = part[1023];
+}
+
+// Offsets, padded offsets, the tile list and the padding rows (one block).
+__global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restrict__ counts_ws,
+                                                             int E, int64_t MTcap,
+                                                             int32_t* counts_out,
+                                                             int32_t* offsets_out, int* poff,
+                                                             int4* tiles, int* ntiles,
+                                                             int32_t* rowpair) {
+  __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1], s_toff[kMaxExperts + 1];
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    int o = 0, po = 0, to = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = o;
+      s_poff[e] = po;
+      s_toff[e] = to;
+      const int c = counts_ws[e];
+      const int nt = (c + kRowPad - 1) / kRowPad;
+      o += c;
+      po += nt * kRowPad;
+      to += nt;
+    }
+    s_off[E] = o;
+    s_poff[E] = po;
+    s_toff[E] = to;
+    ntiles[0] = to;
+    ntiles[1] = po;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) {
+    offsets_out[e] = s_off[e];
+    poff[e] = s_poff[e];
+    if (e < E) counts_out[e] = counts_ws[e];
+  }
+  // tile list
+  for (int e = 0; e < E; ++e) {
+    const int c = counts_ws[e];
+    const int nt = s_toff[e + 1] - s_toff[e];
+    for (int j = tid; j < nt; j += blockDim.x) {
+      const int valid = min(kRowPad, c - j * kRowPad);
+      tiles[s_toff[e] + j] = make_int4(e, s_poff[e] + j * kRowPad, valid, 0);
+    }
+    // padding rows of this expert's last tile
+    const int pad_lo = s_poff[e] + c, pad_hi = s_poff[e + 1];
+    for (int r = pad_lo + tid; r < pad_hi; r += blockDim.x) rowpair[r] = -1;
+  }
+  (void)MTcap;
+}
+
+__global__ void __launch_bounds__(256) perm_scatter_kernel(
+    const int32_t* __restrict__ idx, int64_t P, int E, int64_t NW,
+    const int* __restrict__ warp_base, const int32_t* __restrict__ offsets,
+    const int* __restrict__ poff, int32_t* perm, int32_t* inv_perm, int32_t* rowpair,
+    int32_t* pad_inv, int* status) {
+  __shared__ int hist[8][kMaxExperts];
+  __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    s_off[e] = offsets[e];
+    s_poff[e] = poff[e];
+  }
+  for (int e = lane; e < E; e += 32) hist[w][e] = 0;
+  __syncthreads();
+  const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
+  if (chunk >= NW) return;
+  walk_chunk<true>(idx, P, E, chunk, hist[w], warp_base + chunk * E, s_off, s_poff, perm,
+                   inv_perm, rowpair, pad_inv, status);
+}
+
+void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
+                    cudaStream_t s) {
+  const int E = d.experts;
+  int* status = at<int>(ws, L.status);
+  int* warp_counts = at<int>(ws, L.warp_counts);
+  int* warp_base = at<int>(ws, L.warp_base);
+  int* counts_ws = at<int>(ws, L.counts);
+  int* poff = at<int>(ws, L.poff);
+  int32_t* rowpair = at<int32_t>(ws, L.rowpair);
+  int32_t* pad_inv = at<int32_t>(ws, L.pad_inv);
+  int4* tiles = at<int4>(ws, L.tiles);
+  int* ntiles = at<int>(ws, L.ntiles);
+  const int64_t NW = L.NWc;
+  const unsigned blocks = (unsigned)((NW + 7) / 8);
+  if (NW > 0) {
+    MOE_LAUNCH("perm_hist", s, perm_hist_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, NW, warp_counts, status));
+    MOE_LAUNCH("perm_colscan", s, perm_colscan_kernel<<<E, 1024, 0, s>>>(warp_counts, NW, E, warp_base, counts_ws));
+  } else {
+    zero_fill_i32(counts_ws, E, s);
+  }
+  MOE_LAUNCH("perm_finalize", s, perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, L.MTcap, counts, offsets, poff, tiles,
+                                          ntiles, rowpair));
+  if (NW > 0)
+    MOE_LAUNCH("perm_scatter", s, perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, NW, warp_base, offsets, poff, perm,
+                                               inv_perm, rowpair, pad_inv, status));
+}
+
+}  // namespace moe

@@ -1,0 +1,131 @@
+"""The layer's forward pass and train step, composed from the C-ABI calls.
+
+PyTorch only provides device memory and the current stream here; every step
+(routing, permutation, grouped experts, combine, backward) is a call into the
+CUDA library.  ``MoELayer`` owns the workspace and the intermediate buffers of
+one problem size and reuses them across calls.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import abi
+
+_DT = {"bf16": (torch.bfloat16, abi.MOE_BF16), "f32": (torch.float32, abi.MOE_F32)}
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+class MoELayer:
+    """Buffers and calls for one (tokens, d_model, d_hidden, experts, top_k,
+    shared_hidden, dtype) problem on one CUDA device."""
+
+    def __init__(self, tokens, d_model, d_hidden, experts, top_k, shared_hidden=0, dtype="bf16",
+                 device="cuda", train=True):
+        self.T, self.d, self.h, self.E, self.k, self.hs = (
+            int(tokens), int(d_model), int(d_hidden), int(experts), int(top_k), int(shared_hidden))
+        self.tdtype, cdt = _DT[dtype]
+        self.dtype = dtype
+        self.device = torch.device(device)
+        self.dims = abi.make_dims(self.T, self.d, self.h, self.E, self.k, self.hs, cdt)
+        self.mode = abi.MOE_SAVE_FOR_BWD if train else abi.MOE_FWD_ONLY
+        self.ws_bytes = abi.moe_workspace_bytes(self.dims, self.mode)
+        self.PP = abi.moe_padded_rows(self.dims)
+        dev, f32, i32, td = self.device, torch.float32, torch.int32, self.tdtype
+        T, d, h, E, k, hs, P = self.T, self.d, self.h, self.E, self.k, self.hs, self.T * self.k
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device=dev)
+        off = (-self.ws.data_ptr()) % 256
+        self.ws_ptr = self.ws.data_ptr() + off
+        self.logits = torch.empty(T, E, dtype=f32, device=dev)
+        self.idx = torch.empty(T, k, dtype=i32, device=dev)
+        self.gates = torch.empty(T, k, dtype=f32, device=dev)
+        self.counts = torch.empty(E, dtype=i32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=i32, device=dev)
+        self.perm = torch.empty(P, dtype=i32, device=dev)
+        self.inv_perm = torch.empty(P, dtype=i32, device=dev)
+        self.h_buf = torch.empty(self.PP, h, dtype=td, device=dev)
+        self.a_gate = torch.empty(self.PP, h, dtype=td, device=dev) if train else None
+        self.a_up = torch.empty(self.PP, h, dtype=td, device=dev) if train else None
+        self.y_acc = torch.empty(T, d, dtype=f32, device=dev)
+        self.y = torch.empty(T, d, dtype=td, device=dev)
+        self.hs_buf = torch.empty(T, hs, dtype=td, device=dev) if hs else None
+        self.as_gate = torch.empty(T, hs, dtype=td, device=dev) if (hs and train) else None
+        self.as_up = torch.empty(T, hs, dtype=td, device=dev) if (hs and train) else None
+        self.loss = torch.zeros(1, dtype=f32, device=dev)
+        if train:
+            self.dx = torch.empty(T, d, dtype=td, device=dev)
+            self.grads = {
+                "dw_router": torch.empty(d, E, dtype=f32, device=dev),
+                "dw_gate": torch.empty(E, d, h, dtype=f32, device=dev),
+                "dw_up": torch.empty(E, d, h, dtype=f32, device=dev),
+                "dw_down": torch.empty(E, h, d, dtype=f32, device=dev),
+                "dws_gate": torch.empty(d, hs, dtype=f32, device=dev) if hs else None,
+                "dws_up": torch.empty(d, hs, dtype=f32, device=dev) if hs else None,
+                "dws_down": torch.empty(hs, d, dtype=f32, device=dev) if hs else None,
+            }
+
+    # -- the five calls ---------------------------------------------------
+    def _stream(self):
+        return torch.cuda.current_stream(self.device).cuda_stream
+
+    def route(self, x, w_router, logits_in=None):
+        abi.moe_route(self.dims, _ptr(x), _ptr(w_router), _ptr(logits_in), _ptr(self.logits),
+                      _ptr(self.idx), _ptr(self.gates), self.ws_ptr, self.ws_bytes, self._stream())
+
+    def permute(self):
+        abi.moe_permute(self.dims, _ptr(self.idx), _ptr(self.counts), _ptr(self.offsets),
+                        _ptr(self.perm), _ptr(self.inv_perm), self.ws_ptr, self.ws_bytes,
+                        self._stream())
+
+    def grouped_ffn_fwd(self, x, p, mode):
+        abi.moe_grouped_ffn_fwd(self.dims, mode, _ptr(x), _ptr(self.gates), _ptr(p["w_gate"]),
+                                _ptr(p["w_up"]), _ptr(p["w_down"]), _ptr(self.h_buf),
+                                _ptr(self.a_gate), _ptr(self.a_up), _ptr(self.y_acc),
+                                self.ws_ptr, self.ws_bytes, self._stream())
+
+    def combine(self, x, p, mode, upstream=None):
+        abi.moe_combine(self.dims, mode, _ptr(x), _ptr(p.get("ws_gate")), _ptr(p.get("ws_up")),
+                        _ptr(p.get("ws_down")), _ptr(self.y_acc), _ptr(self.y),
+                        _ptr(self.hs_buf), _ptr(self.as_gate if mode else None),
+                        _ptr(self.as_up if mode else None), _ptr(upstream),
+                        _ptr(self.loss if upstream is not None else None),
+                        self.ws_ptr, self.ws_bytes, self._stream())
+
+    def backward(self, x, p, dy):
+        g = self.grads
+        abi.moe_backward(self.dims, _ptr(dy), _ptr(x), _ptr(p["w_router"]), _ptr(p["w_gate"]),
+                         _ptr(p["w_up"]), _ptr(p["w_down"]), _ptr(p.get("ws_gate")),
+                         _ptr(p.get("ws_up")), _ptr(p.get("ws_down")), _ptr(self.idx),
+                         _ptr(self.gates), _ptr(self.a_gate), _ptr(self.a_up),
+                         _ptr(self.as_gate), _ptr(self.as_up), _ptr(self.dx),
+                         _ptr(g["dw_router"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]),
+                         _ptr(g["dw_down"]), _ptr(g["dws_gate"]), _ptr(g["dws_up"]),
+                         _ptr(g["dws_down"]), self.ws_ptr, self.ws_bytes, self._stream())
+
+    # -- composed passes ---------------------------------------------------
+    def forward(self, x, p, logits_in=None):
+        """y = layer(x); returns the output buffer (valid until the next call)."""
+        self.route(x, p["w_router"], logits_in)
+        self.permute()
+        self.grouped_ffn_fwd(x, p, abi.MOE_FWD_ONLY)
+        self.combine(x, p, abi.MOE_FWD_ONLY)
+        return self.y
+
+    def train_step(self, x, p, dy, logits_in=None):
+        """value_and_grad of L = sum(y * dy): returns (loss [1] device tensor,
+        dx, grads dict); all are the layer's buffers."""
+        if self.mode != abi.MOE_SAVE_FOR_BWD:
+            raise RuntimeError("layer was built with train=False")
+        self.route(x, p["w_router"], logits_in)
+        self.permute()
+        self.grouped_ffn_fwd(x, p, abi.MOE_SAVE_FOR_BWD)
+        self.combine(x, p, abi.MOE_SAVE_FOR_BWD, upstream=dy)
+        self.backward(x, p, dy)
+        return self.loss, self.dx, self.grads
+
+    def device_status(self):
+        """(status, detail) recorded by the kernels; synchronises the stream."""
+        return abi.moe_read_device_status(self.ws_ptr, self.ws_bytes, self._stream())

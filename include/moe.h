@@ -1,0 +1,199 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) dropless, sorted-dispatch
+ * mixture-of-experts layer: forward pass and train step (value and gradients
+ * with respect to the input and every parameter).
+ *
+ * The layer (benchmark pages kernel_gmm_gpu.json / gpu_nn.json /
+ * gpu_moe_h100.json; the parameter count on gpu_nn.json, results[suite=moe]
+ * .params = 12,587,008 = E*3*d*h + d*E for E=8, d=512, h=1024, fixes the
+ * structure):
+ *
+ *   logits = x W_r                               (route piece)
+ *   idx[t, 0..k-1] = top-k experts of logits[t]  (ties -> lower expert index,
+ *                    slots in descending logit order)
+ *   gates[t, :]    = softmax(logits[t, idx[t, :]])
+ *   pairs p = t*k + j sorted by expert, stable  (sort_permute piece)
+ *   H_r = silu(x_t W_gate[e]) * (x_t W_up[e]),  O_r = H_r W_down[e]
+ *                                               (experts_grouped_swiglu piece)
+ *   y[t] = sum_j gates[t, j] O_{row(t, j)} + shared(x[t])
+ *                                               (unpermute_combine piece; the
+ *                    shared expert is the `shared` field of gpu_moe_h100.json)
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  Every
+ *   tensor is dense and row-major.  Weights: w_router [d, E]; w_gate, w_up
+ *   [E, d, h]; w_down [E, h, d]; ws_gate, ws_up [d, hs]; ws_down [hs, d].
+ * - dtype MOE_F32: every activation, weight and gradient is float32.
+ *   dtype MOE_BF16: x, y, dy, dx, weights and the saved activations are
+ *   bfloat16; logits, gates, y_acc and every weight gradient are float32.
+ *   Accumulation is float32 in both.
+ * - The library allocates nothing.  Scratch is the caller's workspace of
+ *   moe_workspace_bytes() bytes (256-byte aligned).  The SAME workspace must
+ *   be passed to every call of one layer invocation: moe_permute writes the
+ *   dispatch tables (expert-padded row map, tile list) into it and the later
+ *   calls read them; the forward leaves state there that moe_backward reads.
+ * - Everything is enqueued on `stream`; no call synchronises the host except
+ *   moe_read_device_status.
+ * - Arguments are validated before anything is launched.  On a non-OK status
+ *   nothing was launched and no output was written.
+ * - Kernel-side failures (a bounded wait that ran out, a device-side index
+ *   check) do not fault: they set a code in the workspace that
+ *   moe_read_device_status returns.
+ * - Expert-sorted activation buffers (h_buf, a_gate_saved, a_up_saved) hold
+ *   moe_padded_rows() rows: each expert's rows start on a multiple of 128 and
+ *   the rows between experts are padding.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad mode          */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but not implemented (shape, dtype)  */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed         */
+  MOE_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out            */
+  MOE_ERR_DEVICE_CHECK = 6   /* device: an index check failed             */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  MOE_FWD_ONLY = 0,      /* forward only: nothing saved for a backward     */
+  MOE_SAVE_FOR_BWD = 1   /* forward of a train step: pre-activations saved */
+} moe_mode;
+
+typedef struct {
+  int64_t tokens;        /* T >= 0                                      */
+  int32_t d_model;       /* d, multiple of 64                            */
+  int32_t d_hidden;      /* h, expert hidden width, multiple of 64       */
+  int32_t experts;       /* E, 1..256                                    */
+  int32_t top_k;         /* k, 1..min(E, 32)                             */
+  int32_t shared_hidden; /* hs, 0 = no shared expert, else multiple of 64 */
+  int32_t dtype;         /* moe_dtype                                    */
+} moe_dims;
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Workspace bytes needed by every call of one layer invocation in `mode`
+ * (MOE_SAVE_FOR_BWD also covers moe_backward).  *bytes is written on OK. */
+moe_status moe_workspace_bytes(const moe_dims* dims, int mode, size_t* bytes);
+
+/* Row capacity of the expert-sorted activation buffers:
+ * T*k + E*127 rounded up to 128. */
+moe_status moe_padded_rows(const moe_dims* dims, int64_t* rows);
+
+/* Router: logits = x W_r (float32 accumulate), then per token the top-k
+ * experts (ties to the lower index, descending slots) and the softmax of
+ * the selected logits.
+ *   x          [T, d]  (dtype)            w_router [d, E] (dtype)
+ *   logits_in  [T, E]  f32, nullable: when given, the GEMM is skipped and
+ *              the selection is made on these logits (fed-logits mode;
+ *              x and w_router may then be NULL)
+ *   logits_out [T, E]  f32, nullable: receives the logits used
+ *   topk_idx   [T, k]  int32 out          gates [T, k] f32 out
+ * Logits must be finite (a NaN makes the selection unspecified). */
+moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
+                     const float* logits_in, float* logits_out, int32_t* topk_idx,
+                     float* gates, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/* Counting sort of the T*k pairs p = t*k + j by expert topk_idx[p],
+ * stable in p.
+ *   counts   [E]     int32 out: pairs per expert
+ *   offsets  [E+1]   int32 out: exclusive prefix sum of counts
+ *   perm     [T*k]   int32 out: perm[r] = pair at sorted position r
+ *   inv_perm [T*k]   int32 out: inv_perm[perm[r]] = r
+ * Also writes the expert-padded row map and the tile list into the
+ * workspace for the grouped calls.  Entries of topk_idx must lie in
+ * [0, E) and be distinct per token. */
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Grouped SwiGLU experts over the expert-sorted rows, gather of the token
+ * rows fused into the first GEMM's operand load and the gate-weighted
+ * combine fused into the down projection:
+ *   h_buf[r]   = silu(x_t W_gate[e]) * (x_t W_up[e])   [padded_rows, h] (dtype)
+ *   y_acc[t]  += gates[t, j] * (h_buf[r] W_down[e])    [T, d] f32, ZEROED HERE
+ * In MOE_SAVE_FOR_BWD mode a_gate_saved / a_up_saved [padded_rows, h]
+ * (dtype) receive x_t W_gate[e] and x_t W_up[e]; in MOE_FWD_ONLY they may
+ * be NULL.  gates is moe_route's output. */
+moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x,
+                               const float* gates, const void* w_gate, const void* w_up,
+                               const void* w_down, void* h_buf, void* a_gate_saved,
+                               void* a_up_saved, float* y_acc, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/* Combine: y = y_acc + shared(x) cast to dtype, where shared(x) =
+ * (silu(x Ws_gate) * (x Ws_up)) Ws_down when hs > 0 (its weights are
+ * ignored and may be NULL when hs == 0).
+ *   hs_buf [T, hs] (dtype) scratch for the shared hidden activations
+ *                          (NULL when hs == 0)
+ *   as_gate_saved, as_up_saved [T, hs] (dtype): saved shared
+ *                          pre-activations in MOE_SAVE_FOR_BWD, else NULL
+ *   upstream [T, d] (dtype), nullable; when given, *loss (f32, device)
+ *   receives sum(y * upstream), the train step's value, reduced in a fixed
+ *   order.  y_acc is consumed (it may be overwritten). */
+moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
+                       const void* ws_up, const void* ws_down, float* y_acc, void* y,
+                       void* hs_buf, void* as_gate_saved, void* as_up_saved,
+                       const void* upstream, float* loss, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
+/* Backward of the train step for L = sum(y * dy):
+ *   inputs : dy [T, d], x, all weights, topk_idx, gates, and the saved
+ *            pre-activations of a MOE_SAVE_FOR_BWD forward that used the
+ *            same workspace (as_* NULL when hs == 0)
+ *   outputs: dx [T, d] (dtype); dw_router [d, E], dw_gate/dw_up [E, d, h],
+ *            dw_down [E, h, d], dws_gate/dws_up [d, hs], dws_down [hs, d]
+ *            (all f32; the dws_* NULL when hs == 0).  Outputs are
+ *            overwritten, not accumulated.
+ * The router gradient follows from the softmax over the selected logits;
+ * experts that were not selected get no logit gradient. */
+moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x,
+                        const void* w_router, const void* w_gate, const void* w_up,
+                        const void* w_down, const void* ws_gate, const void* ws_up,
+                        const void* ws_down, const int32_t* topk_idx, const float* gates,
+                        const void* a_gate_saved, const void* a_up_saved,
+                        const void* as_gate_saved, const void* as_up_saved, void* dx,
+                        float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
+                        float* dws_gate, float* dws_up, float* dws_down, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream);
+
+/* Synchronises `stream`, then returns the device-side status recorded in
+ * the workspace since the last moe_permute (MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE_CHECK) and clears it.  *detail (nullable) receives a
+ * kernel-specific detail word. */
+moe_status moe_read_device_status(void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream, int32_t* detail);
+
+/* Kernel timing records, a measurement aid outside the layer itself: while
+ * enabled, every kernel the library launches is bracketed by two CUDA events
+ * recorded on its stream.  Enabling or disabling discards earlier records.
+ * Not thread-safe with respect to concurrent launches from several threads. */
+moe_status moe_profile_enable(int enable);
+
+/* Aggregates the records per kernel name (synchronising on them): up to
+ * max_entries names of 64 bytes each (NUL-terminated) into `names`, launch
+ * counts into `launches` and summed device milliseconds into `total_ms`
+ * (each nullable); *n_entries receives the number of distinct kernels. */
+moe_status moe_profile_read(int max_entries, char* names, int64_t* launches, double* total_ms,
+                            int* n_entries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -296,7 +296,8 @@ def backward(x, params, top_k: int, upstream, fwd):
         dW_gate[e] = dWg
         dW_up[e] = dWu
         dW_down[e] = dWd
-        np.add.at(dx, toks, dX)
+        # a token selects distinct experts, so `toks` has no repeats here
+        dx[toks] += dX
 
     dgate = dgate_pair.reshape(T, top_k)
     dsel = gates * (dgate - np.sum(gates * dgate, axis=1, keepdims=True))

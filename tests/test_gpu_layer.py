@@ -1,0 +1,118 @@
+"""Parity of the CUDA path with the float64 oracle, through the C ABI.
+
+Routing and the permutation are bit-exact on the device's own logits; every
+floating-point output is within the stated tolerance of the oracle run on the
+same routing.  Sizes span several 128-row tiles with ragged tails."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dropless_mixture_experts_gb300.synthetic import MoEConfig, make_inputs, params_of
+from gpu_util import (TOL, check_routing_bit_exact, compare_layer, rel_err, run_layer, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    MoEConfig(1000, 128, 192, 4, 2, 0, "f32", "f32_e4k2"),
+    MoEConfig(1000, 128, 192, 4, 2, 0, "bf16", "bf16_e4k2"),
+    MoEConfig(777, 128, 128, 8, 3, 128, "bf16", "bf16_e8k3_shared"),
+    MoEConfig(300, 64, 64, 5, 5, 64, "f32", "f32_k_eq_E_shared"),
+    MoEConfig(1, 128, 64, 4, 1, 0, "f32", "f32_one_token"),
+    MoEConfig(4097, 128, 64, 16, 4, 0, "bf16", "bf16_e16k4"),
+    MoEConfig(2050, 256, 128, 64, 8, 256, "bf16", "bf16_decoder_small"),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=[c.name for c in SMALL])
+def test_train_step_matches_oracle(cfg):
+    inp, layer, dev, res = run_layer(cfg)
+    assert res["status"] == 0
+    check_routing_bit_exact(res, cfg)
+    errs = compare_layer(inp, res, cfg, train=True)
+    bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
+    assert not bad, (errs, cfg)
+
+
+@pytest.mark.parametrize("cfg", SMALL[:3], ids=[c.name for c in SMALL[:3]])
+def test_forward_only_matches_train_forward(cfg):
+    inp, _, _, r_train = run_layer(cfg, train=True)
+    _, _, _, r_fwd = run_layer(cfg, train=False, inputs=inp)
+    assert np.array_equal(r_train["idx"], r_fwd["idx"])
+    assert np.array_equal(r_train["y"], r_fwd["y"])
+
+
+def _fed(cfg, logits):
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, cfg.dtype)
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                     cfg.shared_hidden, cfg.dtype, train=True)
+    p = {k: dev[k] for k in params_of(inp)}
+    lg = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
+    loss, dx, grads = layer.train_step(dev["x"], p, dev["upstream"], logits_in=lg)
+    torch.cuda.synchronize()
+    return inp, layer
+
+
+@pytest.mark.parametrize("case", ["ties", "one_expert", "empty_experts", "signed_zero"])
+def test_fed_logits_routing_and_layer(case):
+    cfg = MoEConfig(1500, 128, 64, 8, 2, 0, "f32", case)
+    rng = np.random.default_rng(5)
+    if case == "ties":
+        logits = rng.integers(-2, 3, size=(cfg.tokens, cfg.experts)).astype(np.float32)
+    elif case == "one_expert":
+        logits = rng.standard_normal((cfg.tokens, cfg.experts)).astype(np.float32)
+        logits[:, 3] = 50.0   # every token's first choice is expert 3
+    elif case == "empty_experts":
+        logits = rng.standard_normal((cfg.tokens, cfg.experts)).astype(np.float32)
+        logits[:, 4:] = -50.0  # experts 4..7 never chosen
+    else:
+        logits = np.zeros((cfg.tokens, cfg.experts), np.float32)
+        logits[::2, ::3] = -0.0
+    inp, layer = _fed(cfg, logits)
+    idx = layer.idx.cpu().numpy()
+    ref_idx, ref_g = oracle.route_from_logits(logits.astype(np.float64), cfg.top_k)
+    assert np.array_equal(idx, ref_idx)
+    np.testing.assert_allclose(layer.gates.cpu().numpy(), ref_g, rtol=1e-6)
+    counts, offsets, perm, inv = oracle.counting_sort(ref_idx, cfg.experts)
+    assert np.array_equal(layer.counts.cpu().numpy(), counts)
+    assert np.array_equal(layer.perm.cpu().numpy(), perm)
+    assert np.array_equal(layer.inv_perm.cpu().numpy(), inv)
+    L, fwd, grads = oracle.train_step(inp["x"], params_of(inp), cfg.top_k, inp["upstream"],
+                                      idx=ref_idx, logits=logits)
+    assert rel_err(layer.y.float().cpu().numpy(), fwd["y"]) < TOL["f32"]
+    assert rel_err(layer.dx.float().cpu().numpy(), grads["dx"]) < TOL["f32"]
+    for k in ("dw_gate", "dw_up", "dw_down", "dw_router"):
+        assert rel_err(layer.grads[k].cpu().numpy(), grads[k]) < TOL["f32"], k
+    if case == "empty_experts":
+        assert np.all(layer.grads["dw_down"][4:].cpu().numpy() == 0)
+
+
+def test_zero_tokens():
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    cfg = MoEConfig(0, 128, 64, 4, 2, 64, "bf16", "empty")
+    layer = MoELayer(0, 128, 64, 4, 2, 64, "bf16", train=True)
+    inp = make_inputs(MoEConfig(1, 128, 64, 4, 2, 64, "bf16"))
+    dev = to_dev(inp, "bf16")
+    p = {k: dev[k] for k in params_of(inp)}
+    x = dev["x"][:0]
+    loss, dx, grads = layer.train_step(x, p, dev["upstream"][:0])
+    torch.cuda.synchronize()
+    assert float(loss.item()) == 0.0
+    for k, v in grads.items():
+        if v is not None:
+            assert torch.count_nonzero(v).item() == 0, k
+
+
+def test_out_of_range_expert_index_is_reported_not_faulted():
+    from dropless_mixture_experts_gb300 import abi
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    layer = MoELayer(64, 128, 64, 4, 2, 0, "f32", train=False)
+    layer.idx.copy_(torch.zeros(64, 2, dtype=torch.int32))
+    layer.idx[5, 1] = 9   # not an expert
+    layer.permute()
+    status, detail = layer.device_status()
+    assert status == abi.MOE_ERR_DEVICE_CHECK
+    assert layer.device_status()[0] == 0   # cleared by the read
