@@ -139,7 +139,11 @@ moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x, co
   p.a_gate = a_gate_saved;
   p.a_up = a_up_saved;
   p.y_acc = y_acc;
-  simt_grouped_fwd(*dims, L, mode, p, workspace, stream);
+  if (dims->dtype == MOE_BF16) {
+    if (!tc_grouped_fwd(*dims, L, mode, p, workspace, stream)) return MOE_ERR_CUDA;
+  } else {
+    simt_grouped_fwd(*dims, L, mode, p, workspace, stream);
+  }
   return cuda_status();
 }
 
@@ -170,7 +174,11 @@ moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void
     p.as_gate = as_gate_saved;
     p.as_up = as_up_saved;
     p.y_acc = y_acc;
-    simt_shared_fwd(*dims, L, mode, p, workspace, stream);
+    if (dims->dtype == MOE_BF16) {
+      if (!tc_shared_fwd(*dims, L, mode, p, workspace, stream)) return MOE_ERR_CUDA;
+    } else {
+      simt_shared_fwd(*dims, L, mode, p, workspace, stream);
+    }
   }
   launch_finalize_y(*dims, L, y_acc, y, upstream, loss, workspace, stream);
   return cuda_status();
@@ -239,9 +247,16 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
   p.dws_gate = dws_gate;
   p.dws_up = dws_up;
   p.dws_down = dws_down;
-  simt_backward_gemms(*dims, L, p, workspace, stream);
-  const int nt = (int)(h / 64);
-  launch_router_backward(*dims, L, p, nt, nt, workspace, stream);
+  // gate-gradient partials: one per DZ column tile, rows h/64 apart
+  const int dg_ld = (int)(h / 64);
+  int dg_n = dg_ld;
+  if (dims->dtype == MOE_BF16) {
+    if (!tc_backward_gemms(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
+    dg_n = (int)(h / tc_dz_bn((int)h));
+  } else {
+    simt_backward_gemms(*dims, L, p, workspace, stream);
+  }
+  launch_router_backward(*dims, L, p, dg_n, dg_ld, workspace, stream);
   return cuda_status();
 }
 

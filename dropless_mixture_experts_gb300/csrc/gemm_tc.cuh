@@ -1,0 +1,623 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, bf16
+// operands, f32 accumulators in tensor memory) for sm_103a.
+//
+// One persistent, warp-specialised kernel body serves every contraction of
+// the forward pass and the train step (the experts_grouped_swiglu piece of
+// kernel_gmm_gpu.json and the value_and_grad train step of gpu_moe_h100.json):
+//
+//   warp 0     producer: TMA tile loads, or TMA gather4 loads that fetch the
+//              token rows of the expert-sorted order straight from x / dy
+//              (the gather is fused into the operand load)
+//   warp 1     tensor-memory allocation and the MMA issuer (one thread)
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU,
+//              gate-weighted combine, SwiGLU backward or gradient stores
+//
+// Tiles are 128 rows x BN columns with K blocks of 64 (one 128-byte swizzle
+// row of bf16); shared memory holds a ring of STAGES operand stages and the
+// accumulator is double-buffered in tensor memory so the epilogue of one
+// tile overlaps the main loop of the next.  Every wait is bounded: a wait
+// that runs out records MOE_ERR_TIMEOUT, makes the other roles leave, lets
+// in-flight copies land and frees the tensor memory before returning.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include "kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace tcg {
+
+enum AKind { A_K_TMA = 0, A_K_GATHER = 1, A_MN_TMA = 2, A_MN_GATHER = 3 };
+enum BKind { B_MN_TMA = 0, B_K_TMA = 1, B_MN_GATHER = 2 };
+enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4 };
+
+struct Params {
+  // scheduling
+  const int4* tiles = nullptr;      // routed row kinds: expert-padded tile list
+  const int* ntiles_dev = nullptr;  // routed row kinds: number of tiles
+  const int* counts = nullptr;      // routed DW kinds: rows per expert
+  const int* poff = nullptr;        // routed DW kinds: first padded row per expert
+  const int32_t* rowpair = nullptr; // padded row -> pair id (-1 = padding)
+  int top_k = 1;
+  int64_t rows = 0;                 // dense kinds: number of tokens
+  int n_nt = 1;                     // column tiles
+  int n_mt = 1;                     // DW kinds: output row tiles; dense row kinds: row tiles
+  int splits = 1;                   // DW kinds: K splits (atomic adds when > 1)
+  int experts = 1;
+  int kb_total = 0;                 // row kinds: K / 64
+  int kb_split = 0;                 // dual-K B (dx): K blocks taken from the first map
+  int brow_stride = 0;              // rows of a B weight matrix per expert (0: activations)
+  int M = 0, N = 0;                 // DW output dims / row-kind output columns
+  // epilogue
+  const float* gates = nullptr;
+  void* out0 = nullptr;
+  void* out1 = nullptr;
+  void* out2 = nullptr;
+  const void* in0 = nullptr;
+  const void* in1 = nullptr;
+  float* facc = nullptr;
+  float* facc2 = nullptr;
+  float* dg_part = nullptr;
+  int dg_ld = 0;
+  int ld_out = 0;
+  int hsplit = 0;
+  int* status = nullptr;
+};
+
+template <int AK_, int BKIND_, int EK_, int BN_, bool ROUTED_>
+struct Cfg {
+  static constexpr int AK = AK_, BKIND = BKIND_, EK = EK_, BN = BN_;
+  static constexpr bool ROUTED = ROUTED_;
+  static constexpr bool DW = EK == E_DW;
+  static constexpr bool DUALN = EK == E_GU;
+  static constexpr bool DUALK = EK == E_DX;
+  static constexpr int BM = 128, BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196 * 1024 / STAGE_BYTES) > 8 ? 8 : (196 * 1024 / STAGE_BYTES);
+  static constexpr bool A_MN = AK == A_MN_TMA || AK == A_MN_GATHER;
+  static constexpr bool B_MN = BKIND != B_K_TMA;
+  static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+};
+
+struct Tile {
+  int e, row0, nvalid, m0, n0, kb0, kb1, nt;
+};
+
+template <class C>
+__device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles, Tile& tl) {
+  if constexpr (!C::DW) {
+    const int mt = t / p.n_nt;
+    tl.nt = t % p.n_nt;
+    if (mt >= nrow_tiles) return false;
+    if constexpr (C::ROUTED) {
+      const int4 v = p.tiles[mt];
+      tl.e = v.x;
+      tl.row0 = v.y;
+      tl.nvalid = v.z;
+    } else {
+      tl.e = 0;
+      tl.row0 = mt * C::BM;
+      const int64_t left = p.rows - tl.row0;
+      tl.nvalid = left < C::BM ? (int)left : C::BM;
+    }
+    tl.m0 = 0;
+    tl.n0 = tl.nt * (C::DUALN ? C::BN / 2 : C::BN);
+    tl.kb0 = 0;
+    tl.kb1 = p.kb_total;
+  } else {
+    tl.nt = t % p.n_nt;
+    int r = t / p.n_nt;
+    const int mt = r % p.n_mt;
+    r /= p.n_mt;
+    const int s = r % p.splits;
+    tl.e = r / p.splits;
+    if (tl.e >= p.experts) return false;
+    int64_t ne;
+    if constexpr (C::ROUTED) {
+      ne = p.counts[tl.e];
+      tl.row0 = p.poff[tl.e];
+    } else {
+      ne = p.rows;
+      tl.row0 = 0;
+    }
+    const int nkb = (int)((ne + C::BK - 1) / C::BK);
+    tl.kb0 = (int)((int64_t)s * nkb / p.splits);
+    tl.kb1 = (int)((int64_t)(s + 1) * nkb / p.splits);
+    tl.nvalid = 0;
+    tl.m0 = mt * C::BM;
+    tl.n0 = tl.nt * C::BN;
+  }
+  return true;
+}
+
+struct Shared {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Shared* sh,
+                                              int* status, int where) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::globaltimer();
+  while (true) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (sh->abort) return false;
+    if (tc::globaltimer() - t0 > 2000000000ull) {
+      sh->abort = 1;
+      report_error(status, MOE_ERR_TIMEOUT, where);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 u = s[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+      const float2 f = __bfloat1622float2(b);
+      v[8 * i + 2 * j] = f.x;
+      v[8 * i + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+}
+
+template <class C>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
+                   const __grid_constant__ CUtensorMap mB1, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Shared* sh = reinterpret_cast<Shared*>(smem + C::STAGES * C::STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      tc::mbar_init(&sh->full[s], 1);
+      tc::mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&sh->tfull[a], 1);
+      tc::mbar_init(&sh->tempty[a], 4);
+    }
+    sh->abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::tma_prefetch_desc(&mA);
+    tc::tma_prefetch_desc(&mB0);
+    tc::tma_prefetch_desc(&mB1);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+
+  int nrow_tiles = p.n_mt;
+  if constexpr (C::ROUTED && !C::DW) nrow_tiles = p.ntiles_dev[0];
+
+  bool aborted = false;
+  if (warp == 0) {
+    // ------------------------------ producer ------------------------------
+    int stage = 0;
+    uint32_t phase = 0;
+    Tile tl;
+    for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+      int tok[4] = {0, 0, 0, 0};
+      if constexpr (C::AK == A_K_GATHER) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = 4 * lane + q;
+          const int32_t pr = i < tl.nvalid ? p.rowpair[tl.row0 + i] : -1;
+          tok[q] = pr >= 0 ? pr / p.top_k : 0;
+        }
+      }
+      int brow0 = 0;
+      if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
+      if constexpr (C::DW && C::BKIND != B_MN_GATHER) brow0 = tl.row0;
+      for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+        if (!wait_or_abort(&sh->empty[stage], phase ^ 1, sh, p.status, 100)) {
+          aborted = true;
+          break;
+        }
+        uint8_t* sA = smem + stage * C::STAGE_BYTES;
+        uint8_t* sB = sA + C::A_BYTES;
+        uint64_t* fb = &sh->full[stage];
+        if (lane == 0) tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        __syncwarp();
+        // ---- A ----
+        if constexpr (C::AK == A_K_TMA) {
+          if (lane == 0) tc::tma_load_2d(sA, &mA, fb, kb * C::BK, tl.row0);
+        } else if constexpr (C::AK == A_K_GATHER) {
+          tc::tma_gather4(sA + lane * 512, &mA, fb, kb * C::BK, tok[0], tok[1], tok[2], tok[3]);
+        } else if constexpr (C::AK == A_MN_TMA) {
+          if (lane == 0) {
+            const int krow = (C::DW ? tl.row0 : 0) + kb * C::BK;
+            tc::tma_load_2d(sA, &mA, fb, tl.m0, krow);
+            tc::tma_load_2d(sA + 8192, &mA, fb, tl.m0 + 64, krow);
+          }
+        } else {  // A_MN_GATHER: rows are K indices of the expert's sorted rows
+          const int j = lane >> 4, i = lane & 15;
+          const int krow = tl.row0 + kb * C::BK + 4 * i;
+          int tk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int32_t pr = p.rowpair[krow + q];
+            tk[q] = pr >= 0 ? pr / p.top_k : 0;
+          }
+          tc::tma_gather4(sA + j * 8192 + i * 512, &mA, fb, tl.m0 + 64 * j, tk[0], tk[1], tk[2],
+                          tk[3]);
+        }
+        // ---- B ----
+        if constexpr (C::BKIND == B_MN_TMA) {
+          if (lane == 0) {
+#pragma unroll
+            for (int j = 0; j < C::BN / 64; ++j) {
+              const bool second = C::DUALN && j >= C::BN / 128;
+              const int x = C::DUALN ? tl.n0 + 64 * (second ? j - C::BN / 128 : j) : tl.n0 + 64 * j;
+              tc::tma_load_2d(sB + j * 8192, second ? &mB1 : &mB0, fb, x, brow0 + kb * C::BK);
+            }
+          }
+        } else if constexpr (C::BKIND == B_K_TMA) {
+          if (lane == 0) {
+            const bool second = C::DUALK && kb >= p.kb_split;
+            const int x = (second ? kb - p.kb_split : kb) * C::BK;
+            tc::tma_load_2d(sB, second ? &mB1 : &mB0, fb, x, brow0 + tl.n0);
+          }
+        } else {  // B_MN_GATHER
+#pragma unroll
+          for (int it = 0; it < C::BN / 64 / 2; ++it) {
+            const int g = lane + 32 * it;
+            const int j = g >> 4, i = g & 15;
+            const int krow = tl.row0 + kb * C::BK + 4 * i;
+            int tk[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int32_t pr = p.rowpair[krow + q];
+              tk[q] = pr >= 0 ? pr / p.top_k : 0;
+            }
+            tc::tma_gather4(sB + j * 8192 + i * 512, &mB0, fb, tl.n0 + 64 * j, tk[0], tk[1],
+                            tk[2], tk[3]);
+          }
+          if constexpr (C::BN == 64) {
+            // 16 gather4 for one 64-column block: lanes 0..15
+            const int i = lane & 15;
+            if (lane < 16) {
+              const int krow = tl.row0 + kb * C::BK + 4 * i;
+              int tk[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int32_t pr = p.rowpair[krow + q];
+                tk[q] = pr >= 0 ? pr / p.top_k : 0;
+              }
+              tc::tma_gather4(sB + i * 512, &mB0, fb, tl.n0, tk[0], tk[1], tk[2], tk[3]);
+            }
+          }
+        }
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, aphase = 0;
+    Tile tl;
+    for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+      if (!wait_or_abort(&sh->tempty[acc], aphase ^ 1, sh, p.status, 200)) {
+        aborted = true;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * C::BN;
+      for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+        if (!wait_or_abort(&sh->full[stage], phase, sh, p.status, 300)) {
+          aborted = true;
+          break;
+        }
+        tc::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = tc::smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+          for (int s = 0; s < C::BK / 16; ++s) {
+            const uint64_t ad = C::A_MN ? tc::sw128_desc(a0 + s * 2048, 8192, 1024)
+                                        : tc::sw128_desc(a0 + s * 32, 0, 1024);
+            const uint64_t bd = C::B_MN ? tc::sw128_desc(b0 + s * 2048, 8192, 1024)
+                                        : tc::sw128_desc(b0 + s * 32, 0, 1024);
+            tc::mma_bf16(d_tmem, ad, bd, C::IDESC, (kb > tl.kb0 || s > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(&sh->empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (aborted) break;
+      if (lane == 0) tc::mma_commit(&sh->tfull[acc]);
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1;
+      }
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    int acc = 0;
+    uint32_t aphase = 0;
+    Tile tl;
+    for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+      if (!wait_or_abort(&sh->tfull[acc], aphase, sh, p.status, 400)) {
+        aborted = true;
+        break;
+      }
+      tc::tc_fence_after();
+      const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * C::BN;
+      const bool has_k = tl.kb1 > tl.kb0;
+
+      if constexpr (C::EK == E_GU) {
+        // H = silu(a_g) * a_u with a_g, a_u rounded to bf16 first (the values
+        // a backward pass reads back)
+        const int64_t r = (int64_t)tl.row0 + row;
+        const bool exists = C::ROUTED || row < tl.nvalid;
+        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(p.out0);
+        __nv_bfloat16* AG = reinterpret_cast<__nv_bfloat16*>(p.out1);
+        __nv_bfloat16* AU = reinterpret_cast<__nv_bfloat16*>(p.out2);
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 64; ++c) {
+          uint32_t g[32], u[32];
+          tc::tmem_ld32(tacc + 32 * c, g);
+          tc::tmem_ld32(tacc + C::BN / 2 + 32 * c, u);
+          tc::tmem_ld_wait();
+          float gv[32], uv[32], hv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            gv[i] = bf16r(__uint_as_float(g[i]));
+            uv[i] = bf16r(__uint_as_float(u[i]));
+            hv[i] = gv[i] / (1.f + __expf(-gv[i])) * uv[i];
+          }
+          if (exists) {
+            const int64_t off = r * p.ld_out + tl.n0 + 32 * c;
+            store_bf16x32(H + off, hv);
+            if (AG) {
+              store_bf16x32(AG + off, gv);
+              store_bf16x32(AU + off, uv);
+            }
+          }
+        }
+      } else if constexpr (C::EK == E_DOWN) {
+        // gate-weighted combine: y_acc[token] += gate * (H W_down) (routed,
+        // atomic float4 adds) or y_acc[token] += H_s Ws_down (shared expert)
+        const bool valid = row < tl.nvalid;
+        const int64_t r = (int64_t)tl.row0 + row;
+        int64_t t_out = r;
+        float gt = 1.f;
+        if (C::ROUTED && valid) {
+          const int32_t pr = p.rowpair[r];
+          t_out = pr / p.top_k;
+          gt = p.gates[pr];
+        }
+        float* dst = p.facc + t_out * p.ld_out + tl.n0;
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(tacc + 32 * c, v);
+          tc::tmem_ld_wait();
+          if (!valid) continue;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = make_float4(gt * __uint_as_float(v[4 * i]), gt * __uint_as_float(v[4 * i + 1]),
+                                         gt * __uint_as_float(v[4 * i + 2]), gt * __uint_as_float(v[4 * i + 3]));
+            float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * i);
+            if constexpr (C::ROUTED) {
+              atomicAdd(a, f);
+            } else {
+              float4 o = *a;
+              o.x += f.x;
+              o.y += f.y;
+              o.z += f.z;
+              o.w += f.w;
+              *a = o;
+            }
+          }
+        }
+      } else if constexpr (C::EK == E_DZ) {
+        // Z = dy W_down^T for this row; SwiGLU backward from the saved
+        // pre-activations; gate-gradient partial <Z, H> over these columns
+        const int64_t r = (int64_t)tl.row0 + row;
+        const bool exists = C::ROUTED || row < tl.nvalid;
+        const bool valid = row < tl.nvalid;
+        float gt = 1.f;
+        if constexpr (C::ROUTED) gt = valid ? p.gates[p.rowpair[r]] : 0.f;
+        const int64_t h = p.ld_out;
+        const __nv_bfloat16* AG = reinterpret_cast<const __nv_bfloat16*>(p.in0);
+        const __nv_bfloat16* AU = reinterpret_cast<const __nv_bfloat16*>(p.in1);
+        __nv_bfloat16* dA = reinterpret_cast<__nv_bfloat16*>(p.out0);
+        __nv_bfloat16* gH = reinterpret_cast<__nv_bfloat16*>(p.out1);
+        float dgp = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          uint32_t zv[32];
+          tc::tmem_ld32(tacc + 32 * c, zv);
+          tc::tmem_ld_wait();
+          if (!exists) continue;
+          const int64_t col = tl.n0 + 32 * c;
+          float ag[32], au[32], dag[32], dau[32], gh[32];
+          if (valid) {
+            load_bf16x32(AG + r * h + col, ag);
+            load_bf16x32(AU + r * h + col, au);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ag[i] = au[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float z = __uint_as_float(zv[i]);
+            const float s = 1.f / (1.f + __expf(-ag[i]));
+            const float sl = ag[i] * s;
+            const float hv = bf16r(sl * au[i]);
+            dgp = fmaf(z, hv, dgp);
+            const float dh = gt * z;
+            dau[i] = dh * sl;
+            dag[i] = dh * au[i] * s * (1.f + ag[i] * (1.f - s));
+            gh[i] = gt * hv;
+          }
+          store_bf16x32(dA + r * 2 * h + col, dag);
+          store_bf16x32(dA + r * 2 * h + h + col, dau);
+          store_bf16x32(gH + r * h + col, gh);
+        }
+        if (C::ROUTED && p.dg_part) p.dg_part[r * p.dg_ld + tl.nt] = valid ? dgp : 0.f;
+      } else if constexpr (C::EK == E_DX) {
+        // input gradient: dx_acc[token] += dA [W_gate | W_up]^T (routed, atomic
+        // float4 adds) or dx_acc = dA_s [Ws_gate | Ws_up]^T (shared, first writer)
+        const bool valid = row < tl.nvalid;
+        const int64_t r = (int64_t)tl.row0 + row;
+        int64_t t_out = r;
+        if (C::ROUTED && valid) t_out = p.rowpair[r] / p.top_k;
+        float* dst = p.facc + t_out * p.ld_out + tl.n0;
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(tacc + 32 * c, v);
+          tc::tmem_ld_wait();
+          if (!valid) continue;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                         __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * i);
+            if constexpr (C::ROUTED) atomicAdd(a, f);
+            else *a = f;
+          }
+        }
+      } else {  // E_DW
+        const int om = tl.m0 + row;
+        float* base;
+        int ncol = tl.n0, ld = p.N;
+        if (p.hsplit > 0) {
+          ld = p.hsplit;
+          if (tl.n0 < p.hsplit) {
+            base = p.facc;
+          } else {
+            base = p.facc2;
+            ncol = tl.n0 - p.hsplit;
+          }
+        } else {
+          base = p.facc;
+        }
+        float* dst = base + ((int64_t)tl.e * p.M + om) * ld + ncol;
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          uint32_t v[32];
+          if (has_k) {
+            tc::tmem_ld32(tacc + 32 * c, v);
+            tc::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+          if (om < p.M) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * i);
+              if (p.splits > 1) {
+                if (has_k) atomicAdd(a, f);
+              } else {
+                *a = f;
+              }
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sh->tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        aphase ^= 1;
+      }
+    }
+  }
+
+  if (aborted || sh->abort) {
+    // let copies and MMAs already in flight land before the memory goes away
+    const uint64_t t0 = tc::globaltimer();
+    while (tc::globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
+int sm_count();
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+              uint32_t box_rows);
+
+template <class C>
+void launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
+               int64_t max_tiles, const char* name, cudaStream_t s) {
+  if (max_tiles <= 0) return;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(tc_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         C::SMEM_BYTES);
+    attr = true;
+  }
+  const int sms = sm_count();
+  const int grid = (int)(max_tiles < sms ? max_tiles : sms);
+  MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, 192, C::SMEM_BYTES, s>>>(a, b0, b1, p));
+}
+
+}  // namespace tcg
+}  // namespace moe

@@ -70,6 +70,16 @@ void simt_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPt
 void simt_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                          cudaStream_t s);
 
+// grouped expert GEMMs on the tensor cores (tc_fwd.cu, tc_bwd.cu: bfloat16
+// storage); false when a tensor map could not be encoded
+bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                    cudaStream_t s);
+bool tc_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                   cudaStream_t s);
+bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                       cudaStream_t s);
+int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials per row)
+
 // combine / loss / router backward (combine.cu)
 void launch_finalize_y(const moe_dims& d, const Layout& L, const float* y_acc, void* y,
                        const void* upstream, float* loss, void* ws, cudaStream_t s);

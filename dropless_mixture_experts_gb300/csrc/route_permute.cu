@@ -77,13 +77,16 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
         my_idx = bi;
       }
     }
-    const float z = lane < k ? expf(my_sel - top) : 0.f;
-    float sum = z;
+    // softmax of the selected logits in double: the difference of two
+    // float32 logits is exact there, so each gate is correctly rounded to
+    // float32 up to the exp's own error (k exps per token, negligible cost)
+    const double z = lane < k ? exp((double)my_sel - (double)top) : 0.0;
+    double sum = z;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s);
     if (lane < k) {
       idx_out[t * k + lane] = my_idx;
-      gates_out[t * k + lane] = z / sum;
+      gates_out[t * k + lane] = (float)(z / sum);
     }
   }
 }

@@ -1,0 +1,116 @@
+// Forward launches of the tensor-core GEMMs (bf16 storage):
+//   gate/up projection of the expert-sorted rows with the token gather in the
+//   operand load and SwiGLU in the epilogue, then the down projection with
+//   the gate-weighted combine in the epilogue; and the dense shared expert.
+#include "gemm_tc.cuh"
+
+namespace moe {
+using namespace tcg;
+
+namespace {
+
+template <int BN>
+bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+            bool routed, cudaStream_t s) {
+  const int dm = d.d_model;
+  const int h = routed ? d.d_hidden : d.shared_hidden;
+  CUtensorMap a, b0, b1;
+  Params q;
+  q.status = at<int>(ws, L.status);
+  q.n_nt = h / (BN / 2);
+  q.kb_total = dm / 64;
+  q.ld_out = h;
+  if (routed) {
+    if (!make_map(&a, p.x, d.tokens, dm, 64, 1)) return false;
+    if (!make_map(&b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, 64)) return false;
+    if (!make_map(&b1, p.w_up, (uint64_t)d.experts * dm, h, 64, 64)) return false;
+    q.tiles = at<int4>(ws, L.tiles);
+    q.ntiles_dev = at<int>(ws, L.ntiles);
+    q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.top_k = d.top_k;
+    q.brow_stride = dm;
+    q.out0 = p.h_buf;
+    q.out1 = mode == MOE_SAVE_FOR_BWD ? p.a_gate : nullptr;
+    q.out2 = mode == MOE_SAVE_FOR_BWD ? p.a_up : nullptr;
+    launch_tc<Cfg<A_K_GATHER, B_MN_TMA, E_GU, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt,
+                                                          "tc_gateup", s);
+  } else {
+    if (!make_map(&a, p.x, d.tokens, dm, 64, 128)) return false;
+    if (!make_map(&b0, p.ws_gate, dm, h, 64, 64)) return false;
+    if (!make_map(&b1, p.ws_up, dm, h, 64, 64)) return false;
+    q.rows = d.tokens;
+    q.n_mt = (int)((d.tokens + 127) / 128);
+    q.out0 = p.hs_buf;
+    q.out1 = mode == MOE_SAVE_FOR_BWD ? p.as_gate : nullptr;
+    q.out2 = mode == MOE_SAVE_FOR_BWD ? p.as_up : nullptr;
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, false>>(a, b0, b1, q, (int64_t)q.n_mt * q.n_nt,
+                                                        "tc_gateup", s);
+  }
+  return true;
+}
+
+template <int BN>
+bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
+          cudaStream_t s) {
+  const int dm = d.d_model;
+  const int h = routed ? d.d_hidden : d.shared_hidden;
+  CUtensorMap a, b0;
+  Params q;
+  q.status = at<int>(ws, L.status);
+  q.n_nt = dm / BN;
+  q.kb_total = h / 64;
+  q.ld_out = dm;
+  q.facc = p.y_acc;
+  if (routed) {
+    if (!make_map(&a, p.h_buf, L.PPcap, h, 64, 128)) return false;
+    if (!make_map(&b0, p.w_down, (uint64_t)d.experts * h, dm, 64, 64)) return false;
+    q.tiles = at<int4>(ws, L.tiles);
+    q.ntiles_dev = at<int>(ws, L.ntiles);
+    q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.top_k = d.top_k;
+    q.brow_stride = h;
+    q.gates = p.gates;
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, true>>(a, b0, b0, q, L.MTcap * q.n_nt,
+                                                         "tc_down", s);
+  } else {
+    if (!make_map(&a, p.hs_buf, d.tokens, h, 64, 128)) return false;
+    if (!make_map(&b0, p.ws_down, h, dm, 64, 64)) return false;
+    q.rows = d.tokens;
+    q.n_mt = (int)((d.tokens + 127) / 128);
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, false>>(a, b0, b0, q, (int64_t)q.n_mt * q.n_nt,
+                                                          "tc_down", s);
+  }
+  return true;
+}
+
+bool gateup_any(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                bool routed, cudaStream_t s) {
+  const int h = routed ? d.d_hidden : d.shared_hidden;
+  return h % 128 == 0 ? gateup<256>(d, L, mode, p, ws, routed, s)
+                      : gateup<128>(d, L, mode, p, ws, routed, s);
+}
+
+bool down_any(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
+              cudaStream_t s) {
+  const int n = d.d_model;
+  if (n % 256 == 0) return down<256>(d, L, p, ws, routed, s);
+  if (n % 128 == 0) return down<128>(d, L, p, ws, routed, s);
+  return down<64>(d, L, p, ws, routed, s);
+}
+
+}  // namespace
+
+bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                    cudaStream_t s) {
+  zero_fill_f32(p.y_acc, d.tokens * (int64_t)d.d_model, s);
+  if (!gateup_any(d, L, mode, p, ws, true, s)) return false;
+  return down_any(d, L, p, ws, true, s);
+}
+
+bool tc_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
+                   cudaStream_t s) {
+  if (!gateup_any(d, L, mode, p, ws, false, s)) return false;
+  return down_any(d, L, p, ws, false, s);
+}
+
+}  // namespace moe
