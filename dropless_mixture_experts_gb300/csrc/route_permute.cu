@@ -77,16 +77,23 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
         my_idx = bi;
       }
     }
-    // softmax of the selected logits in double: the difference of two
-    // float32 logits is exact there, so each gate is correctly rounded to
-    // float32 up to the exp's own error (k exps per token, negligible cost)
-    const double z = lane < k ? exp((double)my_sel - (double)top) : 0.0;
-    double sum = z;
+    // softmax of the selected logits.  The difference of two float32 logits
+    // is exact in double; splitting it into a float head and tail gives
+    // exp(head + tail) = expf(head) * (1 + tail) to float accuracy even for
+    // large gaps, where a float32 difference alone would lose the tail
+    float z = 0.f;
+    if (lane < k) {
+      const double diff = (double)my_sel - (double)top;
+      const float head = (float)diff;
+      const float tail = (float)(diff - (double)head);
+      z = expf(head) * (1.f + tail);
+    }
+    float sum = z;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s);
     if (lane < k) {
       idx_out[t * k + lane] = my_idx;
-      gates_out[t * k + lane] = (float)(z / sum);
+      gates_out[t * k + lane] = z / sum;
     }
   }
 }

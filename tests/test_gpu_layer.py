@@ -40,7 +40,12 @@ def test_forward_only_matches_train_forward(cfg):
     inp, _, _, r_train = run_layer(cfg, train=True)
     _, _, _, r_fwd = run_layer(cfg, train=False, inputs=inp)
     assert np.array_equal(r_train["idx"], r_fwd["idx"])
-    assert np.array_equal(r_train["y"], r_fwd["y"])
+    if cfg.top_k <= 2:
+        # two float adds onto zero commute exactly, so the combine is
+        # deterministic whatever order the atomic adds land in
+        assert np.array_equal(r_train["y"], r_fwd["y"])
+    else:
+        assert rel_err(r_fwd["y"], r_train["y"]) < 1e-5
 
 
 def _fed(cfg, logits):
