@@ -45,7 +45,9 @@ def test_forward_only_matches_train_forward(cfg):
         # deterministic whatever order the atomic adds land in
         assert np.array_equal(r_train["y"], r_fwd["y"])
     else:
-        assert rel_err(r_fwd["y"], r_train["y"]) < 1e-5
+        # a different order of the float atomic adds may flip the output's
+        # last rounding step
+        assert rel_err(r_fwd["y"], r_train["y"]) < TOL[cfg.dtype]
 
 
 def _fed(cfg, logits):
