@@ -86,6 +86,11 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
   if (T == 0) return MOE_OK;
   const float* logits = logits_in;
   if (!logits_in) {
+    if (router_fused_supported(*dims)) {
+      // router GEMM, selection and softmax in one pass over x
+      launch_router_fused(*dims, x, w_router, logits_out, topk_idx, gates, stream);
+      return cuda_status();
+    }
     float* dst = logits_out ? logits_out : at<float>(workspace, L.logits);
     LayerPtrs p;
     p.x = x;
@@ -205,8 +210,7 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
   }
   MOE_TRY(shape_supported(dims));
   // the router backward keeps W_r^T and one dW_r column block in shared memory
-  if ((int64_t)dims->d_model * dims->experts > 49152 || dims->experts > 192)
-    return MOE_ERR_UNSUPPORTED;
+  if (!router_backward_supported(*dims)) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(dims, MOE_SAVE_FOR_BWD, workspace, workspace_bytes));
   const Layout L = make_layout(*dims, MOE_SAVE_FOR_BWD);
   const int64_t E = dims->experts, dm = dims->d_model, h = dims->d_hidden,
@@ -247,12 +251,13 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
   p.dws_gate = dws_gate;
   p.dws_up = dws_up;
   p.dws_down = dws_down;
-  // gate-gradient partials: one per DZ column tile, rows h/64 apart
-  const int dg_ld = (int)(h / 64);
-  int dg_n = dg_ld;
+  // gate-gradient partials per pair: one per DZ column tile (and column
+  // half of the tensor-core epilogue), pairs 2*h/64 apart
+  const int dg_ld = (int)(2 * h / 64);
+  int dg_n = (int)(h / 64);
   if (dims->dtype == MOE_BF16) {
     if (!tc_backward_gemms(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
-    dg_n = (int)(h / tc_dz_bn((int)h));
+    dg_n = (int)(2 * h / tc_dz_bn((int)h));
   } else {
     simt_backward_gemms(*dims, L, p, workspace, stream);
   }

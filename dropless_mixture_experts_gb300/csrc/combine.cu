@@ -8,7 +8,7 @@
 // the logit gradient of slot j is g_j (dg_j - sum_i g_i dg_i), with dg_j the
 // gradient of the gate (the row-dot <dy_t W_down[e]^T, H_r> produced by the
 // grouped backward), and zero on the experts that were not selected.  Then
-// dW_r = x^T dlogits and dx += dlogits W_r^T.
+// dW_r = x^T dlogits and dx = dx_acc + dlogits W_r^T.
 #include "kernels.cuh"
 
 namespace moe {
@@ -49,75 +49,75 @@ __global__ void __launch_bounds__(32) loss_reduce_kernel(const float* __restrict
   if (threadIdx.x == 0) *loss = s;
 }
 
-// One warp per token: dsel_j = g_j (dg_j - sum_i g_i dg_i), and
-// dx[t] = dx_acc[t] + sum_j dsel_j W_r[:, e_j]  (W_r^T staged in shared memory).
+// Router backward of a block's token range, in chunks of 256/k tokens:
+//   phase A: thread i of the chunk takes pair i: its gate gradient (the sum
+//            of the DZ partials), then dsel = g (dg - sum_j g_j dg_j)
+//   phase B: thread i takes input dimensions i, i+256, ...: for every token
+//            of the chunk dx = dx_acc + sum_j dsel_j W_r[i, e_j] and the
+//            block's dW_r partial gains x[t, i] dsel_j in column e_j.  Each
+//            thread owns its dimensions' accumulators, so the order of the
+//            adds is fixed and the result deterministic.
 template <typename T>
-__global__ void __launch_bounds__(256) router_dl_dx_kernel(
+__global__ void __launch_bounds__(256) router_bwd_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ gates,
-    const float* __restrict__ dg_part, int dg_ld, int dg_n, const int32_t* __restrict__ pad_inv,
-    const T* __restrict__ w_router, const float* __restrict__ dx_acc, T* dx, float* dsel,
-    int64_t Tn, int d, int E, int k) {
-  extern __shared__ float s_wt[];  // [E][d]
-  for (int i = threadIdx.x; i < d * E; i += blockDim.x) {
+    const float* __restrict__ dg_part, int dg_ld, int dg_n, const T* __restrict__ w_router,
+    const T* __restrict__ x, const float* __restrict__ dx_acc, T* __restrict__ dx,
+    float* __restrict__ part, int64_t Tn, int d, int E, int k, int64_t per_block) {
+  extern __shared__ __align__(16) float s_acc[];  // [E][d] f32, then W_r^T [E][d] (T)
+  T* s_wt = reinterpret_cast<T*>(s_acc + (size_t)E * d);
+  __shared__ int s_e[256];
+  __shared__ float s_g[256], s_dg[256], s_ds[256];
+  const int tid = threadIdx.x;
+  for (int i = tid; i < E * d; i += blockDim.x) {
+    s_acc[i] = 0.f;
     const int r = i / E, e = i % E;  // coalesced read of W_r[r][e]
-    s_wt[e * d + r] = to_f32(w_router[i]);
+    s_wt[e * d + r] = w_router[i];
+  }
+  const int64_t t0 = blockIdx.x * per_block;
+  const int64_t t1 = t0 + per_block < Tn ? t0 + per_block : Tn;
+  const int CH = 256 / k;
+  for (int64_t tc = t0; tc < t1; tc += CH) {
+    const int nt = (int)(t1 - tc < CH ? t1 - tc : CH);
+    const int npair = nt * k;
+    __syncthreads();
+    if (tid < npair) {
+      const int64_t p = tc * k + tid;
+      s_e[tid] = idx[p];
+      s_g[tid] = gates[p];
+      float dg = 0.f;
+      const float* row = dg_part + p * dg_ld;
+      for (int q = 0; q < dg_n; ++q) dg += row[q];
+      s_dg[tid] = dg;
+    }
+    __syncthreads();
+    if (tid < npair) {
+      const int base = (tid / k) * k;
+      float sgd = 0.f;
+      for (int j = 0; j < k; ++j) sgd = fmaf(s_g[base + j], s_dg[base + j], sgd);
+      s_ds[tid] = s_g[tid] * (s_dg[tid] - sgd);
+    }
+    __syncthreads();
+    for (int i = tid; i < d; i += blockDim.x) {
+#pragma unroll 4
+      for (int u = 0; u < nt; ++u) {
+        const int64_t t = tc + u;
+        float v = dx_acc[t * d + i];
+        const float xv = to_f32(x[t * d + i]);
+        for (int j = 0; j < k; ++j) {
+          const int e = s_e[u * k + j];
+          const float ds = s_ds[u * k + j];
+          v = fmaf(ds, to_f32(s_wt[e * d + i]), v);
+          s_acc[e * d + i] = fmaf(xv, ds, s_acc[e * d + i]);
+        }
+        dx[t * d + i] = from_f32<T>(v);
+      }
+    }
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t t = warp; t < Tn; t += nwarps) {
-    int e = 0;
-    float g = 0.f, dg = 0.f;
-    if (lane < k) {
-      const int64_t p = t * k + lane;
-      e = idx[p];
-      g = gates[p];
-      const float* row = dg_part + (int64_t)pad_inv[p] * dg_ld;
-      for (int q = 0; q < dg_n; ++q) dg += row[q];
-    }
-    float sgd = g * dg;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sgd += __shfl_xor_sync(0xffffffffu, sgd, o);
-    const float ds = g * (dg - sgd);
-    if (lane < k) dsel[t * k + lane] = ds;
-    for (int i = lane; i < d; i += 32) {
-      float v = dx_acc[t * d + i];
-      for (int j = 0; j < k; ++j) {
-        const int ej = __shfl_sync(0xffffffffu, e, j);
-        const float dj = __shfl_sync(0xffffffffu, ds, j);
-        v = fmaf(dj, s_wt[ej * d + i], v);
-      }
-      dx[t * d + i] = from_f32<T>(v);
-    }
-  }
-}
-
-// dW_r partials: block (range, dim-slice) accumulates sum_t x[t, i] dsel[t, j]
-// into column e_j, each thread owning one input dimension i (its column of
-// the shared accumulator is private, so the order of the adds is fixed).
-template <typename T>
-__global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
-                                                        const int32_t* __restrict__ idx,
-                                                        const float* __restrict__ dsel,
-                                                        int64_t Tn, int d, int E, int k,
-                                                        float* part) {
-  extern __shared__ float s_acc[];  // [E][256]
-  const int range = blockIdx.x;
-  const int i = blockIdx.y * 256 + threadIdx.x;
-  for (int e = 0; e < E; ++e) s_acc[e * 256 + threadIdx.x] = 0.f;
-  const int64_t per = (Tn + gridDim.x - 1) / gridDim.x;
-  const int64_t t0 = range * per;
-  const int64_t t1 = t0 + per < Tn ? t0 + per : Tn;
-  if (i < d) {
-    for (int64_t t = t0; t < t1; ++t) {
-      const float xv = to_f32(x[t * d + i]);
-      for (int j = 0; j < k; ++j) {
-        const int e = idx[t * k + j];
-        s_acc[e * 256 + threadIdx.x] = fmaf(xv, dsel[t * k + j], s_acc[e * 256 + threadIdx.x]);
-      }
-    }
-    for (int e = 0; e < E; ++e) part[((int64_t)range * d + i) * E + e] = s_acc[e * 256 + threadIdx.x];
+  float* out = part + (int64_t)blockIdx.x * d * E;
+  for (int i = tid; i < E * d; i += blockDim.x) {
+    const int r = i / E, e = i % E;
+    out[i] = s_acc[e * d + r];
   }
 }
 
@@ -135,42 +135,47 @@ void finalize_y_t(const moe_dims& d, const Layout& L, const float* y_acc, void* 
                   const void* G, float* loss, void* ws, cudaStream_t s) {
   const int64_t n = d.tokens * (int64_t)d.d_model;
   float* part = at<float>(ws, L.loss_part);
-  MOE_LAUNCH("finalize_y", s, finalize_y_kernel<T><<<kLossBlocks, 256, 0, s>>>(y_acc, reinterpret_cast<T*>(y),
-                                                   reinterpret_cast<const T*>(G), n, part));
-  if (G && loss) MOE_LAUNCH("loss_reduce", s, loss_reduce_kernel<<<1, 32, 0, s>>>(part, kLossBlocks, loss));
+  MOE_LAUNCH("finalize_y", s,
+             finalize_y_kernel<T><<<kLossBlocks, 256, 0, s>>>(
+                 y_acc, reinterpret_cast<T*>(y), reinterpret_cast<const T*>(G), n, part));
+  if (G && loss)
+    MOE_LAUNCH("loss_reduce", s, loss_reduce_kernel<<<1, 32, 0, s>>>(part, kLossBlocks, loss));
 }
 
 template <typename T>
-void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dz_ntiles,
+void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                        int dg_ld, void* ws, cudaStream_t s) {
   const int dm = d.d_model, E = d.experts, k = d.top_k;
-  float* dsel = at<float>(ws, L.dsel);
   float* part = at<float>(ws, L.dwr_part);
-  if (d.tokens > 0) {
-    const size_t smem = sizeof(float) * dm * E;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(router_dl_dx_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           200 * 1024);
-      cudaFuncSetAttribute(router_dw_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           200 * 1024);
-      attr_set = true;
-    }
-    int64_t blocks = (d.tokens + 7) / 8;
-    if (blocks > 152 * 2) blocks = 152 * 2;
-    MOE_LAUNCH("router_dl_dx", s, router_dl_dx_kernel<T><<<(unsigned)blocks, 256, smem, s>>>(
-        p.topk_idx, p.gates, at<float>(ws, L.dg_part), dg_ld, dz_ntiles, at<int32_t>(ws, L.pad_inv),
-        reinterpret_cast<const T*>(p.w_router), at<float>(ws, L.dx_acc), reinterpret_cast<T*>(p.dx),
-        dsel, d.tokens, dm, E, k));
-    dim3 g(kRouterBwdRanges, (dm + 255) / 256);
-    MOE_LAUNCH("router_dw", s, router_dw_kernel<T><<<g, 256, sizeof(float) * E * 256, s>>>(
-        reinterpret_cast<const T*>(p.x), p.topk_idx, dsel, d.tokens, dm, E, k, part));
-    const int64_t n = (int64_t)dm * E;
-    MOE_LAUNCH("router_dw_reduce", s, router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(part, kRouterBwdRanges, n,
-                                                                       p.dw_router));
-  } else {
+  if (d.tokens == 0) {
     zero_fill_f32(p.dw_router, (int64_t)dm * E, s);
+    return;
   }
+  const size_t smem = (size_t)E * dm * (sizeof(float) + sizeof(T));
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(router_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kRouterBwdSmem);
+    attr_set = true;
+  }
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int CH = 256 / k;
+  int64_t blocks = (d.tokens + CH - 1) / CH;
+  const int64_t cap = sms < kRouterBwdRanges ? sms : kRouterBwdRanges;
+  if (blocks > cap) blocks = cap;
+  const int64_t per_block = (d.tokens + blocks - 1) / blocks;
+  MOE_LAUNCH("router_bwd", s,
+             router_bwd_kernel<T><<<(unsigned)blocks, 256, smem, s>>>(
+                 p.topk_idx, p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n,
+                 reinterpret_cast<const T*>(p.w_router), reinterpret_cast<const T*>(p.x),
+                 at<float>(ws, L.dx_acc), reinterpret_cast<T*>(p.dx), part, d.tokens, dm, E, k,
+                 per_block));
+  const int64_t n = (int64_t)dm * E;
+  MOE_LAUNCH("router_dw_reduce", s,
+             router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+                 part, (int)blocks, n, p.dw_router));
 }
 
 }  // namespace
@@ -185,10 +190,15 @@ void launch_finalize_y(const moe_dims& d, const Layout& L, const float* y_acc, v
   else finalize_y_t<float>(d, L, y_acc, y, upstream, loss, ws, s);
 }
 
-void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dz_ntiles,
+void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                             int dg_ld, void* ws, cudaStream_t s) {
-  if (d.dtype == MOE_BF16) router_backward_t<__nv_bfloat16>(d, L, p, dz_ntiles, dg_ld, ws, s);
-  else router_backward_t<float>(d, L, p, dz_ntiles, dg_ld, ws, s);
+  if (d.dtype == MOE_BF16) router_backward_t<__nv_bfloat16>(d, L, p, dg_n, dg_ld, ws, s);
+  else router_backward_t<float>(d, L, p, dg_n, dg_ld, ws, s);
+}
+
+bool router_backward_supported(const moe_dims& d) {
+  const size_t elem = d.dtype == MOE_BF16 ? 2 : 4;
+  return (size_t)d.experts * d.d_model * (4 + elem) <= (size_t)kRouterBwdSmem;
 }
 
 }  // namespace moe

@@ -16,7 +16,8 @@ constexpr int kPermChunk = 32 * kPermRounds;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 constexpr int kLossBlocks = 512;  // fixed partial count of the loss reduction
-constexpr int kRouterBwdRanges = 128;  // token ranges of the router-weight gradient partials
+constexpr int kRouterBwdRanges = 256;  // max token ranges of the router-weight gradient partials
+constexpr int kRouterBwdSmem = 200 * 1024;  // router backward: W_r^T + dW_r partial in shared memory
 
 // ---- element access ---------------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -37,9 +38,9 @@ __device__ __forceinline__ void report_error(int* status, int code, int detail) 
 
 // ---- workspace layout -------------------------------------------------------
 struct Layout {
-  size_t status, warp_counts, warp_base, counts, poff, rowpair, pad_inv, tiles, ntiles,
+  size_t status, warp_counts, warp_base, counts, poff, rowpair, tokrow, tiles, ntiles,
       loss_part, logits;
-  size_t dg_part, dA, gH, dx_acc, dAs, gHs, dsel, dwr_part;
+  size_t dg_part, dA, gH, dx_acc, dAs, gHs, dwr_part;
   size_t total;
   int64_t P, PPcap, MTcap, NWc;
   int elem;  // bytes per storage element
@@ -74,19 +75,18 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.counts = take(sizeof(int) * E);
   L.poff = take(sizeof(int) * (E + 1));
   L.rowpair = take(sizeof(int) * L.PPcap);
-  L.pad_inv = take(sizeof(int) * L.P);
+  L.tokrow = take(sizeof(int) * L.PPcap);
   L.tiles = take(sizeof(int4) * L.MTcap);
   L.ntiles = take(sizeof(int) * 4);
   L.loss_part = take(sizeof(float) * kLossBlocks);
   L.logits = take(sizeof(float) * T * E);
   if (mode == MOE_SAVE_FOR_BWD) {
-    L.dg_part = take(sizeof(float) * L.PPcap * (h / 64));
+    L.dg_part = take(sizeof(float) * L.P * 2 * (h / 64));
     L.dA = take((size_t)L.elem * L.PPcap * 2 * h);
     L.gH = take((size_t)L.elem * L.PPcap * h);
     L.dx_acc = take(sizeof(float) * T * dm);
     L.dAs = take((size_t)L.elem * T * 2 * hs);
     L.gHs = take((size_t)L.elem * T * hs);
-    L.dsel = take(sizeof(float) * T * d.top_k);
     L.dwr_part = take(sizeof(float) * kRouterBwdRanges * dm * E);
   }
   L.total = o;

@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       // the 16 threads of one row are 16 consecutive lanes of a warp
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, o);
-      if (ROUTED && tx == 0 && a.dg_part) a.dg_part[r * a.dg_ld + ntile] = valid ? dgp : 0.f;
+      if (ROUTED && tx == 0 && valid) a.dg_part[(int64_t)a.rowpair[r] * a.dg_ld + ntile] = dgp;
     } else if constexpr (KIND == DX) {
       if (m >= nvalid) continue;
       if constexpr (ROUTED) {
@@ -556,7 +556,7 @@ void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws
   z.dA_out = dA;
   z.gH_out = gH;
   z.dg_part = at<float>(ws, L.dg_part);
-  z.dg_ld = h / BN;
+  z.dg_ld = 2 * h / 64;  // per-pair stride of the gate-gradient partials
   z.n_ntiles = h / BN;
   launch<DZ, T, true>(z, z.n_ntiles * 2 * L.MTcap, s);
 

@@ -7,9 +7,11 @@
 //
 //   warp 0     producer: TMA tile loads, or TMA gather4 loads that fetch the
 //              token rows of the expert-sorted order straight from x / dy
-//              (the gather is fused into the operand load)
+//              (the gather is fused into the operand load); the token index
+//              of every sorted row is prefetched ahead of its k-block
 //   warp 1     tensor-memory allocation and the MMA issuer (one thread)
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU,
+//   warps 2-9  epilogue, two warps per 32-lane quarter of the accumulator
+//              splitting its columns: tcgen05.ld, then the fused SwiGLU,
 //              gate-weighted combine, SwiGLU backward or gradient stores
 //
 // Tiles are 128 rows x BN columns with K blocks of 64 (one 128-byte swizzle
@@ -32,6 +34,9 @@ enum AKind { A_K_TMA = 0, A_K_GATHER = 1, A_MN_TMA = 2, A_MN_GATHER = 3 };
 enum BKind { B_MN_TMA = 0, B_K_TMA = 1, B_MN_GATHER = 2 };
 enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4 };
 
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
 struct Params {
   // scheduling
   const int4* tiles = nullptr;      // routed row kinds: expert-padded tile list
@@ -39,6 +44,7 @@ struct Params {
   const int* counts = nullptr;      // routed DW kinds: rows per expert
   const int* poff = nullptr;        // routed DW kinds: first padded row per expert
   const int32_t* rowpair = nullptr; // padded row -> pair id (-1 = padding)
+  const int32_t* tokrow = nullptr;  // padded row -> token (0 on padding rows)
   int top_k = 1;
   int64_t rows = 0;                 // dense kinds: number of tokens
   int n_nt = 1;                     // column tiles
@@ -58,7 +64,7 @@ struct Params {
   const void* in1 = nullptr;
   float* facc = nullptr;
   float* facc2 = nullptr;
-  float* dg_part = nullptr;
+  float* dg_part = nullptr;         // DZ: [pairs, dg_ld], entry 2*column-tile + half
   int dg_ld = 0;
   int ld_out = 0;
   int hsplit = 0;
@@ -72,6 +78,7 @@ struct Cfg {
   static constexpr bool DW = EK == E_DW;
   static constexpr bool DUALN = EK == E_GU;
   static constexpr bool DUALK = EK == E_DX;
+  static constexpr bool KGATHER = AK == A_MN_GATHER || BKIND == B_MN_GATHER;
   static constexpr int BM = 128, BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
@@ -83,6 +90,7 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
+  static_assert(!DUALN || BN >= 128, "the gate/up tile holds 64-column halves");
 };
 
 struct Tile {
@@ -191,8 +199,12 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
                       pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
 }
 
+__device__ __forceinline__ int4 ld_tok4(const int32_t* p) {
+  return __ldg(reinterpret_cast<const int4*>(p));
+}
+
 template <class C>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
                    const __grid_constant__ CUtensorMap mB1, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -208,7 +220,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sh->tfull[a], 1);
-      tc::mbar_init(&sh->tempty[a], 4);
+      tc::mbar_init(&sh->tempty[a], kEpiWarps);
     }
     sh->abort = 0;
     tc::fence_barrier_init();
@@ -235,21 +247,42 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------ producer ------------------------------
     int stage = 0;
     uint32_t phase = 0;
-    Tile tl;
-    for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
-      int tok[4] = {0, 0, 0, 0};
+    Tile tl, tn;
+    int t = blockIdx.x;
+    bool have = get_tile<C>(p, t, nrow_tiles, tl);
+    // A_K_GATHER: lane l owns the token rows 4l..4l+3 of a row tile, loaded
+    // one tile ahead
+    int4 tok_cur = make_int4(0, 0, 0, 0), tok_next = make_int4(0, 0, 0, 0);
+    if constexpr (C::AK == A_K_GATHER) {
+      if (have) tok_cur = ld_tok4(p.tokrow + tl.row0 + 4 * lane);
+    }
+    while (have && !aborted) {
+      const int tnext = t + gridDim.x;
+      const bool have_next = get_tile<C>(p, tnext, nrow_tiles, tn);
       if constexpr (C::AK == A_K_GATHER) {
+        if (have_next) tok_next = ld_tok4(p.tokrow + tn.row0 + 4 * lane);
+      }
+      // K-row gathers: lanes (i = lane & 15) own K rows 4i..4i+3 of every
+      // k-block; a ring prefetches them four k-blocks ahead
+      int4 ring[4];
+      const int32_t* kt = p.tokrow + tl.row0 + 4 * (lane & 15);
+      if constexpr (C::KGATHER) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = 4 * lane + q;
-          const int32_t pr = i < tl.nvalid ? p.rowpair[tl.row0 + i] : -1;
-          tok[q] = pr >= 0 ? pr / p.top_k : 0;
-        }
+        for (int i = 0; i < 4; ++i)
+          ring[i] = tl.kb0 + i < tl.kb1 ? ld_tok4(kt + (tl.kb0 + i) * C::BK) : make_int4(0, 0, 0, 0);
       }
       int brow0 = 0;
       if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
       if constexpr (C::DW && C::BKIND != B_MN_GATHER) brow0 = tl.row0;
       for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+        int4 tk = make_int4(0, 0, 0, 0);
+        if constexpr (C::KGATHER) {
+          tk = ring[0];
+          ring[0] = ring[1];
+          ring[1] = ring[2];
+          ring[2] = ring[3];
+          ring[3] = kb + 4 < tl.kb1 ? ld_tok4(kt + (kb + 4) * C::BK) : make_int4(0, 0, 0, 0);
+        }
         if (!wait_or_abort(&sh->empty[stage], phase ^ 1, sh, p.status, 100)) {
           aborted = true;
           break;
@@ -263,24 +296,17 @@ __global__ void __launch_bounds__(192, 1)
         if constexpr (C::AK == A_K_TMA) {
           if (lane == 0) tc::tma_load_2d(sA, &mA, fb, kb * C::BK, tl.row0);
         } else if constexpr (C::AK == A_K_GATHER) {
-          tc::tma_gather4(sA + lane * 512, &mA, fb, kb * C::BK, tok[0], tok[1], tok[2], tok[3]);
+          tc::tma_gather4(sA + lane * 512, &mA, fb, kb * C::BK, tok_cur.x, tok_cur.y, tok_cur.z,
+                          tok_cur.w);
         } else if constexpr (C::AK == A_MN_TMA) {
           if (lane == 0) {
             const int krow = (C::DW ? tl.row0 : 0) + kb * C::BK;
             tc::tma_load_2d(sA, &mA, fb, tl.m0, krow);
             tc::tma_load_2d(sA + 8192, &mA, fb, tl.m0 + 64, krow);
           }
-        } else {  // A_MN_GATHER: rows are K indices of the expert's sorted rows
+        } else {  // A_MN_GATHER: two 64-column blocks, 16 gather4 each
           const int j = lane >> 4, i = lane & 15;
-          const int krow = tl.row0 + kb * C::BK + 4 * i;
-          int tk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int32_t pr = p.rowpair[krow + q];
-            tk[q] = pr >= 0 ? pr / p.top_k : 0;
-          }
-          tc::tma_gather4(sA + j * 8192 + i * 512, &mA, fb, tl.m0 + 64 * j, tk[0], tk[1], tk[2],
-                          tk[3]);
+          tc::tma_gather4(sA + j * 8192 + i * 512, &mA, fb, tl.m0 + 64 * j, tk.x, tk.y, tk.z, tk.w);
         }
         // ---- B ----
         if constexpr (C::BKIND == B_MN_TMA) {
@@ -298,34 +324,18 @@ __global__ void __launch_bounds__(192, 1)
             const int x = (second ? kb - p.kb_split : kb) * C::BK;
             tc::tma_load_2d(sB, second ? &mB1 : &mB0, fb, x, brow0 + tl.n0);
           }
-        } else {  // B_MN_GATHER
+        } else {  // B_MN_GATHER: BN/64 column blocks, 16 gather4 each
+          if constexpr (C::BN >= 128) {
 #pragma unroll
-          for (int it = 0; it < C::BN / 64 / 2; ++it) {
-            const int g = lane + 32 * it;
-            const int j = g >> 4, i = g & 15;
-            const int krow = tl.row0 + kb * C::BK + 4 * i;
-            int tk[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int32_t pr = p.rowpair[krow + q];
-              tk[q] = pr >= 0 ? pr / p.top_k : 0;
+            for (int it = 0; it < C::BN / 128; ++it) {
+              const int g = lane + 32 * it;
+              const int j = g >> 4, i = g & 15;
+              tc::tma_gather4(sB + j * 8192 + i * 512, &mB0, fb, tl.n0 + 64 * j, tk.x, tk.y, tk.z,
+                              tk.w);
             }
-            tc::tma_gather4(sB + j * 8192 + i * 512, &mB0, fb, tl.n0 + 64 * j, tk[0], tk[1],
-                            tk[2], tk[3]);
-          }
-          if constexpr (C::BN == 64) {
-            // 16 gather4 for one 64-column block: lanes 0..15
-            const int i = lane & 15;
-            if (lane < 16) {
-              const int krow = tl.row0 + kb * C::BK + 4 * i;
-              int tk[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int32_t pr = p.rowpair[krow + q];
-                tk[q] = pr >= 0 ? pr / p.top_k : 0;
-              }
-              tc::tma_gather4(sB + i * 512, &mB0, fb, tl.n0, tk[0], tk[1], tk[2], tk[3]);
-            }
+          } else {
+            if (lane < 16)
+              tc::tma_gather4(sB + lane * 512, &mB0, fb, tl.n0, tk.x, tk.y, tk.z, tk.w);
           }
         }
         if (++stage == C::STAGES) {
@@ -333,6 +343,10 @@ __global__ void __launch_bounds__(192, 1)
           phase ^= 1;
         }
       }
+      t = tnext;
+      tl = tn;
+      have = have_next;
+      tok_cur = tok_next;
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
@@ -381,7 +395,11 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------ epilogue ------------------------------
+    // warp w >= 2: lane quarter q = w % 4 (the tcgen05.ld lane window of the
+    // warp), column half = (w - 2) / 4: the two warps of a quarter take
+    // alternate column chunks
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = 32 * q + lane;
     int acc = 0;
     uint32_t aphase = 0;
@@ -404,7 +422,7 @@ __global__ void __launch_bounds__(192, 1)
         __nv_bfloat16* AG = reinterpret_cast<__nv_bfloat16*>(p.out1);
         __nv_bfloat16* AU = reinterpret_cast<__nv_bfloat16*>(p.out2);
 #pragma unroll 1
-        for (int c = 0; c < C::BN / 64; ++c) {
+        for (int c = half; c < C::BN / 64; c += 2) {
           uint32_t g[32], u[32];
           tc::tmem_ld32(tacc + 32 * c, g);
           tc::tmem_ld32(tacc + C::BN / 2 + 32 * c, u);
@@ -414,7 +432,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int i = 0; i < 32; ++i) {
             gv[i] = bf16r(__uint_as_float(g[i]));
             uv[i] = bf16r(__uint_as_float(u[i]));
-            hv[i] = gv[i] / (1.f + __expf(-gv[i])) * uv[i];
+            hv[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
           }
           if (exists) {
             const int64_t off = r * p.ld_out + tl.n0 + 32 * c;
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         float* dst = p.facc + t_out * p.ld_out + tl.n0;
 #pragma unroll 1
-        for (int c = 0; c < C::BN / 32; ++c) {
+        for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t v[32];
           tc::tmem_ld32(tacc + 32 * c, v);
           tc::tmem_ld_wait();
@@ -467,8 +485,16 @@ __global__ void __launch_bounds__(192, 1)
         const int64_t r = (int64_t)tl.row0 + row;
         const bool exists = C::ROUTED || row < tl.nvalid;
         const bool valid = row < tl.nvalid;
+        int32_t pr = -1;
         float gt = 1.f;
-        if constexpr (C::ROUTED) gt = valid ? p.gates[p.rowpair[r]] : 0.f;
+        if constexpr (C::ROUTED) {
+          if (valid) {
+            pr = p.rowpair[r];
+            gt = p.gates[pr];
+          } else {
+            gt = 0.f;
+          }
+        }
         const int64_t h = p.ld_out;
         const __nv_bfloat16* AG = reinterpret_cast<const __nv_bfloat16*>(p.in0);
         const __nv_bfloat16* AU = reinterpret_cast<const __nv_bfloat16*>(p.in1);
@@ -476,7 +502,7 @@ __global__ void __launch_bounds__(192, 1)
         __nv_bfloat16* gH = reinterpret_cast<__nv_bfloat16*>(p.out1);
         float dgp = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < C::BN / 32; ++c) {
+        for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t zv[32];
           tc::tmem_ld32(tacc + 32 * c, zv);
           tc::tmem_ld_wait();
@@ -493,7 +519,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float z = __uint_as_float(zv[i]);
-            const float s = 1.f / (1.f + __expf(-ag[i]));
+            const float s = __fdividef(1.f, 1.f + __expf(-ag[i]));
             const float sl = ag[i] * s;
             const float hv = bf16r(sl * au[i]);
             dgp = fmaf(z, hv, dgp);
@@ -506,7 +532,7 @@ __global__ void __launch_bounds__(192, 1)
           store_bf16x32(dA + r * 2 * h + h + col, dau);
           store_bf16x32(gH + r * h + col, gh);
         }
-        if (C::ROUTED && p.dg_part) p.dg_part[r * p.dg_ld + tl.nt] = valid ? dgp : 0.f;
+        if (C::ROUTED && pr >= 0) p.dg_part[(int64_t)pr * p.dg_ld + 2 * tl.nt + half] = dgp;
       } else if constexpr (C::EK == E_DX) {
         // input gradient: dx_acc[token] += dA [W_gate | W_up]^T (routed, atomic
         // float4 adds) or dx_acc = dA_s [Ws_gate | Ws_up]^T (shared, first writer)
@@ -516,7 +542,7 @@ __global__ void __launch_bounds__(192, 1)
         if (C::ROUTED && valid) t_out = p.rowpair[r] / p.top_k;
         float* dst = p.facc + t_out * p.ld_out + tl.n0;
 #pragma unroll 1
-        for (int c = 0; c < C::BN / 32; ++c) {
+        for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t v[32];
           tc::tmem_ld32(tacc + 32 * c, v);
           tc::tmem_ld_wait();
@@ -530,24 +556,20 @@ __global__ void __launch_bounds__(192, 1)
             else *a = f;
           }
         }
-      } else {  // E_DW
+      } else {  // E_DW: one expert's gradient tile (rows m0.., columns n0..)
         const int om = tl.m0 + row;
-        float* base;
+        float* base = p.facc;
         int ncol = tl.n0, ld = p.N;
         if (p.hsplit > 0) {
           ld = p.hsplit;
-          if (tl.n0 < p.hsplit) {
-            base = p.facc;
-          } else {
+          if (tl.n0 >= p.hsplit) {
             base = p.facc2;
             ncol = tl.n0 - p.hsplit;
           }
-        } else {
-          base = p.facc;
         }
         float* dst = base + ((int64_t)tl.e * p.M + om) * ld + ncol;
 #pragma unroll 1
-        for (int c = 0; c < C::BN / 32; ++c) {
+        for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t v[32];
           if (has_k) {
             tc::tmem_ld32(tacc + 32 * c, v);
@@ -616,7 +638,7 @@ void launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b
   }
   const int sms = sm_count();
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-  MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, 192, C::SMEM_BYTES, s>>>(a, b0, b1, p));
+  MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, s>>>(a, b0, b1, p));
 }
 
 }  // namespace tcg

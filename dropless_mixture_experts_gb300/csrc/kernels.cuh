@@ -23,6 +23,9 @@ void clear_status(int* status, cudaStream_t s);
 // routing and permutation (route_permute.cu)
 void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
                          float* gates, cudaStream_t s);
+bool router_fused_supported(const moe_dims& d);
+void launch_router_fused(const moe_dims& d, const void* x, const void* w, float* logits_out,
+                         int32_t* idx, float* gates, cudaStream_t s);
 void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
                     cudaStream_t s);
@@ -83,7 +86,8 @@ int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials 
 // combine / loss / router backward (combine.cu)
 void launch_finalize_y(const moe_dims& d, const Layout& L, const float* y_acc, void* y,
                        const void* upstream, float* loss, void* ws, cudaStream_t s);
-void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dz_ntiles,
+bool router_backward_supported(const moe_dims& d);
+void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                             int dg_ld, void* ws, cudaStream_t s);
 
 }  // namespace moe

@@ -1,5 +1,5 @@
-// Routing (top-k selection + softmax over the selected logits) and the
-// counting-sort permutation of token-expert pairs.
+// Routing (router GEMM, top-k selection, softmax over the selected logits)
+// and the counting-sort permutation of token-expert pairs.
 //
 // Routing: benchmark page gpu_moe_h100.json (top_k field) and the layer
 // structure fixed by gpu_nn.json's parameter count: per token the k largest
@@ -10,22 +10,33 @@
 // `sorted`): pairs p = t*k + j ordered by expert, stable in p, plus an
 // expert-padded copy of the order in which every expert's rows start on a
 // multiple of 128 (the row tiles of the grouped GEMMs never straddle two
-// experts).
+// experts) and the token of every padded row.
 #include "kernels.cuh"
 
 namespace moe {
 
-// ---------------------------------------------------------------------------
-// Top-k over one row of logits held by a warp: lane l owns logits
-// l, l+32, ..., and k rounds of a butterfly arg-max pick the experts.
-// `better` is the total order (larger logit first, lower index on equality).
-// ---------------------------------------------------------------------------
+// The total order of the selection: larger logit first, the lower expert
+// index on equal logits (+0.0 == -0.0).
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// exp(sel - top) for float32 logits: the gap is exact in double; its float
+// head and tail give expf(head) * (1 + tail) to float accuracy even for
+// large gaps, where a float32 difference alone would lose the tail.
+__device__ __forceinline__ float gate_exp(float sel, float top) {
+  const double diff = (double)sel - (double)top;
+  const float head = (float)diff;
+  const float tail = (float)(diff - (double)head);
+  return expf(head) * (1.f + tail);
+}
+
 constexpr int kMaxPerLane = kMaxExperts / 32;
 
+// ---------------------------------------------------------------------------
+// Top-k from a logits matrix (fed logits, or any expert count): one warp per
+// token, lane l owns logits l, l+32, ...; k rounds of a butterfly arg-max.
+// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restrict__ logits,
                                                            int64_t T, int E, int k,
                                                            int32_t* __restrict__ idx_out,
@@ -48,7 +59,6 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
     int my_idx = 0;
     float top = 0.f;
     for (int r = 0; r < k; ++r) {
-      // best live entry of this lane
       float bv = -INFINITY;
       int bi = 0x7fffffff;
 #pragma unroll
@@ -59,8 +69,7 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
           bi = e;
         }
       }
-      // butterfly arg-max over the warp (the order is total, so every lane
-      // ends with the same winner)
+      // the order is total, so every lane ends with the same winner
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, s);
@@ -77,17 +86,7 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
         my_idx = bi;
       }
     }
-    // softmax of the selected logits.  The difference of two float32 logits
-    // is exact in double; splitting it into a float head and tail gives
-    // exp(head + tail) = expf(head) * (1 + tail) to float accuracy even for
-    // large gaps, where a float32 difference alone would lose the tail
-    float z = 0.f;
-    if (lane < k) {
-      const double diff = (double)my_sel - (double)top;
-      const float head = (float)diff;
-      const float tail = (float)(diff - (double)head);
-      z = expf(head) * (1.f + tail);
-    }
+    const float z = lane < k ? gate_exp(my_sel, top) : 0.f;
     float sum = z;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s);
@@ -101,10 +100,143 @@ __global__ void __launch_bounds__(256) topk_softmax_kernel(const float* __restri
 void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
                          float* gates, cudaStream_t s) {
   if (T == 0) return;
-  int64_t warps = T;
-  int64_t blocks = (warps + 7) / 8;
+  int64_t blocks = (T + 7) / 8;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  MOE_LAUNCH("topk_softmax", s, topk_softmax_kernel<<<(unsigned)blocks, 256, 0, s>>>(logits, T, E, k, idx, gates));
+  MOE_LAUNCH("topk_softmax", s,
+             topk_softmax_kernel<<<(unsigned)blocks, 256, 0, s>>>(logits, T, E, k, idx, gates));
+}
+
+// ---------------------------------------------------------------------------
+// Fused router: one thread per token computes its EN logits (float32
+// accumulate, W_r staged in shared memory and read by broadcast), selects
+// the top k among them in registers and writes idx / gates (and the logits
+// when asked).  Persistent blocks loop over 128-token groups.
+// ---------------------------------------------------------------------------
+template <typename T, int EN>
+__global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__ x,
+                                                           const T* __restrict__ w_router,
+                                                           int64_t Tn, int d, int k,
+                                                           float* __restrict__ logits_out,
+                                                           int32_t* __restrict__ idx_out,
+                                                           float* __restrict__ gates_out) {
+  extern __shared__ __align__(16) float s_w[];  // [d][EN]
+  for (int i = threadIdx.x; i < d * EN; i += blockDim.x) s_w[i] = to_f32(w_router[i]);
+  __syncthreads();
+  constexpr int VE = 16 / sizeof(T);  // elements per 16-byte load
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < Tn + 0;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    float acc[EN];
+#pragma unroll
+    for (int e = 0; e < EN; ++e) acc[e] = 0.f;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + t * d);
+#pragma unroll 1
+    for (int c = 0; c < d / VE; ++c) {
+      const uint4 u = __ldg(xr + c);
+      float xv[VE];
+      if constexpr (sizeof(T) == 2) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+          xv[2 * j] = f.x;
+          xv[2 * j + 1] = f.y;
+        }
+      } else {
+        xv[0] = __uint_as_float(u.x);
+        xv[1] = __uint_as_float(u.y);
+        xv[2] = __uint_as_float(u.z);
+        xv[3] = __uint_as_float(u.w);
+      }
+#pragma unroll
+      for (int j = 0; j < VE; ++j) {
+        const float4* wr = reinterpret_cast<const float4*>(s_w + (c * VE + j) * EN);
+#pragma unroll
+        for (int e4 = 0; e4 < EN / 4; ++e4) {
+          const float4 w4 = wr[e4];
+          acc[4 * e4 + 0] = fmaf(xv[j], w4.x, acc[4 * e4 + 0]);
+          acc[4 * e4 + 1] = fmaf(xv[j], w4.y, acc[4 * e4 + 1]);
+          acc[4 * e4 + 2] = fmaf(xv[j], w4.z, acc[4 * e4 + 2]);
+          acc[4 * e4 + 3] = fmaf(xv[j], w4.w, acc[4 * e4 + 3]);
+        }
+      }
+    }
+    if (logits_out) {
+      float4* lo = reinterpret_cast<float4*>(logits_out + t * EN);
+#pragma unroll
+      for (int e4 = 0; e4 < EN / 4; ++e4)
+        lo[e4] = make_float4(acc[4 * e4], acc[4 * e4 + 1], acc[4 * e4 + 2], acc[4 * e4 + 3]);
+    }
+    // selection: k passes over the EN logits in registers
+    unsigned long long taken = 0ull;
+    float top = 0.f, sum = 0.f;
+    for (int r = 0; r < k; ++r) {
+      float bv = 0.f;
+      int bi = -1;
+#pragma unroll
+      for (int e = 0; e < EN; ++e) {
+        if (!((taken >> e) & 1ull) && (bi < 0 || better(acc[e], e, bv, bi))) {
+          bv = acc[e];
+          bi = e;
+        }
+      }
+      taken |= 1ull << bi;
+      if (r == 0) top = bv;
+      const float z = gate_exp(bv, top);
+      sum += z;
+      idx_out[t * k + r] = bi;
+      gates_out[t * k + r] = z;
+    }
+    for (int r = 0; r < k; ++r) gates_out[t * k + r] = gates_out[t * k + r] / sum;
+  }
+}
+
+template <typename T, int EN>
+static void router_fused_t(const moe_dims& dm, const void* x, const void* w, float* logits_out,
+                           int32_t* idx, float* gates, cudaStream_t s) {
+  const size_t smem = sizeof(float) * dm.d_model * EN;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(router_fused_kernel<T, EN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         160 * 1024);
+    attr = true;
+  }
+  int64_t blocks = (dm.tokens + 127) / 128;
+  const int64_t cap = EN >= 32 ? 152 : 152 * 8;  // amortise the W_r staging for wide routers
+  if (blocks > cap) blocks = cap;
+  MOE_LAUNCH("router_fused", s,
+             (router_fused_kernel<T, EN><<<(unsigned)blocks, 128, smem, s>>>(
+                 reinterpret_cast<const T*>(x), reinterpret_cast<const T*>(w), dm.tokens,
+                 dm.d_model, dm.top_k, logits_out, idx, gates)));
+}
+
+bool router_fused_supported(const moe_dims& d) {
+  const int E = d.experts;
+  return (E == 8 || E == 16 || E == 32 || E == 64) &&
+         (size_t)d.d_model * E * sizeof(float) <= 160 * 1024;
+}
+
+void launch_router_fused(const moe_dims& d, const void* x, const void* w, float* logits_out,
+                         int32_t* idx, float* gates, cudaStream_t s) {
+  if (d.tokens == 0) return;
+  const bool bf = d.dtype == MOE_BF16;
+  switch (d.experts) {
+    case 8:
+      bf ? router_fused_t<__nv_bfloat16, 8>(d, x, w, logits_out, idx, gates, s)
+         : router_fused_t<float, 8>(d, x, w, logits_out, idx, gates, s);
+      break;
+    case 16:
+      bf ? router_fused_t<__nv_bfloat16, 16>(d, x, w, logits_out, idx, gates, s)
+         : router_fused_t<float, 16>(d, x, w, logits_out, idx, gates, s);
+      break;
+    case 32:
+      bf ? router_fused_t<__nv_bfloat16, 32>(d, x, w, logits_out, idx, gates, s)
+         : router_fused_t<float, 32>(d, x, w, logits_out, idx, gates, s);
+      break;
+    default:
+      bf ? router_fused_t<__nv_bfloat16, 64>(d, x, w, logits_out, idx, gates, s)
+         : router_fused_t<float, 64>(d, x, w, logits_out, idx, gates, s);
+      break;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -116,10 +248,10 @@ void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* 
 // ---------------------------------------------------------------------------
 template <bool SCATTER>
 __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int64_t P, int E,
-                                           int64_t chunk, int* hist, const int* base_e,
+                                           int k, int64_t chunk, int* hist, const int* base_e,
                                            const int* off_e, const int* poff_e, int32_t* perm,
-                                           int32_t* inv_perm, int32_t* rowpair,
-                                           int32_t* pad_inv, int* status) {
+                                           int32_t* inv_perm, int32_t* rowpair, int32_t* tokrow,
+                                           int* status) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   for (int r = 0; r < kPermRounds; ++r) {
@@ -146,21 +278,21 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
       perm[pos] = (int32_t)p;
       inv_perm[p] = pos;
       rowpair[ppos] = (int32_t)p;
-      pad_inv[p] = ppos;
+      tokrow[ppos] = (int32_t)(p / k);
     }
   }
 }
 
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t P,
-                                                        int E, int64_t NW, int* warp_counts,
-                                                        int* status) {
+                                                        int E, int k, int64_t NW,
+                                                        int* warp_counts, int* status) {
   __shared__ int hist[8][kMaxExperts];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
   for (int e = lane; e < E; e += 32) hist[w][e] = 0;
   __syncwarp();
   if (chunk >= NW) return;
-  walk_chunk<false>(idx, P, E, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, nullptr,
+  walk_chunk<false>(idx, P, E, k, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, nullptr,
                     nullptr, nullptr, status);
   for (int e = lane; e < E; e += 32) warp_counts[chunk * E + e] = hist[w][e];
 }
@@ -197,11 +329,10 @@ __global__ void __launch_bounds__(1024) perm_colscan_kernel(const int* __restric
 
 // Offsets, padded offsets, the tile list and the padding rows (one block).
 __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restrict__ counts_ws,
-                                                             int E, int64_t MTcap,
-                                                             int32_t* counts_out,
+                                                             int E, int32_t* counts_out,
                                                              int32_t* offsets_out, int* poff,
                                                              int4* tiles, int* ntiles,
-                                                             int32_t* rowpair) {
+                                                             int32_t* rowpair, int32_t* tokrow) {
   __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1], s_toff[kMaxExperts + 1];
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -228,7 +359,6 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restri
     poff[e] = s_poff[e];
     if (e < E) counts_out[e] = counts_ws[e];
   }
-  // tile list
   for (int e = 0; e < E; ++e) {
     const int c = counts_ws[e];
     const int nt = s_toff[e + 1] - s_toff[e];
@@ -236,18 +366,20 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restri
       const int valid = min(kRowPad, c - j * kRowPad);
       tiles[s_toff[e] + j] = make_int4(e, s_poff[e] + j * kRowPad, valid, 0);
     }
-    // padding rows of this expert's last tile
+    // padding rows of this expert's last tile: no pair, token 0
     const int pad_lo = s_poff[e] + c, pad_hi = s_poff[e + 1];
-    for (int r = pad_lo + tid; r < pad_hi; r += blockDim.x) rowpair[r] = -1;
+    for (int r = pad_lo + tid; r < pad_hi; r += blockDim.x) {
+      rowpair[r] = -1;
+      tokrow[r] = 0;
+    }
   }
-  (void)MTcap;
 }
 
 __global__ void __launch_bounds__(256) perm_scatter_kernel(
-    const int32_t* __restrict__ idx, int64_t P, int E, int64_t NW,
+    const int32_t* __restrict__ idx, int64_t P, int E, int k, int64_t NW,
     const int* __restrict__ warp_base, const int32_t* __restrict__ offsets,
     const int* __restrict__ poff, int32_t* perm, int32_t* inv_perm, int32_t* rowpair,
-    int32_t* pad_inv, int* status) {
+    int32_t* tokrow, int* status) {
   __shared__ int hist[8][kMaxExperts];
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -259,36 +391,41 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
   __syncthreads();
   const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
   if (chunk >= NW) return;
-  walk_chunk<true>(idx, P, E, chunk, hist[w], warp_base + chunk * E, s_off, s_poff, perm,
-                   inv_perm, rowpair, pad_inv, status);
+  walk_chunk<true>(idx, P, E, k, chunk, hist[w], warp_base + chunk * E, s_off, s_poff, perm,
+                   inv_perm, rowpair, tokrow, status);
 }
 
 void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
                     cudaStream_t s) {
-  const int E = d.experts;
+  const int E = d.experts, k = d.top_k;
   int* status = at<int>(ws, L.status);
   int* warp_counts = at<int>(ws, L.warp_counts);
   int* warp_base = at<int>(ws, L.warp_base);
   int* counts_ws = at<int>(ws, L.counts);
   int* poff = at<int>(ws, L.poff);
   int32_t* rowpair = at<int32_t>(ws, L.rowpair);
-  int32_t* pad_inv = at<int32_t>(ws, L.pad_inv);
+  int32_t* tokrow = at<int32_t>(ws, L.tokrow);
   int4* tiles = at<int4>(ws, L.tiles);
   int* ntiles = at<int>(ws, L.ntiles);
   const int64_t NW = L.NWc;
   const unsigned blocks = (unsigned)((NW + 7) / 8);
   if (NW > 0) {
-    MOE_LAUNCH("perm_hist", s, perm_hist_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, NW, warp_counts, status));
-    MOE_LAUNCH("perm_colscan", s, perm_colscan_kernel<<<E, 1024, 0, s>>>(warp_counts, NW, E, warp_base, counts_ws));
+    MOE_LAUNCH("perm_hist", s,
+               perm_hist_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, k, NW, warp_counts, status));
+    MOE_LAUNCH("perm_colscan", s,
+               perm_colscan_kernel<<<E, 1024, 0, s>>>(warp_counts, NW, E, warp_base, counts_ws));
   } else {
     zero_fill_i32(counts_ws, E, s);
   }
-  MOE_LAUNCH("perm_finalize", s, perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, L.MTcap, counts, offsets, poff, tiles,
-                                          ntiles, rowpair));
+  MOE_LAUNCH("perm_finalize", s,
+             perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, counts, offsets, poff, tiles,
+                                                     ntiles, rowpair, tokrow));
   if (NW > 0)
-    MOE_LAUNCH("perm_scatter", s, perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, NW, warp_base, offsets, poff, perm,
-                                               inv_perm, rowpair, pad_inv, status));
+    MOE_LAUNCH("perm_scatter", s,
+               perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, k, NW, warp_base, offsets,
+                                                          poff, perm, inv_perm, rowpair, tokrow,
+                                                          status));
 }
 
 }  // namespace moe

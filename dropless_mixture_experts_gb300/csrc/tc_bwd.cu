@@ -32,6 +32,7 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
@@ -40,7 +41,7 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.out0 = at<void>(ws, L.dA);
     q.out1 = at<void>(ws, L.gH);
     q.dg_part = at<float>(ws, L.dg_part);
-    q.dg_ld = h / 64;
+    q.dg_ld = 2 * h / 64;
     launch_tc<Cfg<A_K_GATHER, B_K_TMA, E_DZ, BN, true>>(a, b0, b0, q, L.MTcap * q.n_nt, "tc_dz",
                                                          s);
   } else {
@@ -78,6 +79,7 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = dm;
     launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt, "tc_dx", s);
@@ -125,6 +127,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
     q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     launch_tc<Cfg<A_MN_TMA, B_MN_GATHER, E_DW, BN, true>>(
         a, b0, b0, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
@@ -169,6 +172,7 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
     q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     launch_tc<Cfg<A_MN_GATHER, B_MN_TMA, E_DW, BN, true>>(
         a, b0, b0, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);

@@ -27,6 +27,7 @@ bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, vo
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = dm;
     q.out0 = p.h_buf;
@@ -67,6 +68,7 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
+    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
