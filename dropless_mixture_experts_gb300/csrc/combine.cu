@@ -49,75 +49,119 @@ __global__ void __launch_bounds__(32) loss_reduce_kernel(const float* __restrict
   if (threadIdx.x == 0) *loss = s;
 }
 
-// Router backward of a block's token range, in chunks of 256/k tokens:
-//   phase A: thread i of the chunk takes pair i: its gate gradient (the sum
-//            of the DZ partials), then dsel = g (dg - sum_j g_j dg_j)
-//   phase B: thread i takes input dimensions i, i+256, ...: for every token
-//            of the chunk dx = dx_acc + sum_j dsel_j W_r[i, e_j] and the
-//            block's dW_r partial gains x[t, i] dsel_j in column e_j.  Each
-//            thread owns its dimensions' accumulators, so the order of the
-//            adds is fixed and the result deterministic.
+// dsel[t, j] = g_j (dg_j - sum_i g_i dg_i), one thread per token; dg_j is
+// the sum of the grouped backward's per-column-tile partials of pair t*k+j.
+__global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restrict__ gates,
+                                                          const float* __restrict__ dg_part,
+                                                          int dg_ld, int dg_n, int64_t Tn, int k,
+                                                          float* __restrict__ dsel) {
+  const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (t >= Tn) return;
+  float sgd = 0.f;
+  for (int j = 0; j < k; ++j) {
+    const int64_t p = t * k + j;
+    float dg = 0.f;
+    for (int q = 0; q < dg_n; ++q) dg += dg_part[p * dg_ld + q];
+    dsel[p] = dg;
+    sgd = fmaf(gates[p], dg, sgd);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int64_t p = t * k + j;
+    dsel[p] = gates[p] * (dsel[p] - sgd);
+  }
+}
+
+// dx[t, :] = dx_acc[t, :] + sum_j dsel[t, j] W_r[:, e_j]: each thread takes
+// four consecutive input dimensions of one token (W_r^T staged in shared
+// memory), blocks loop over token groups.
 template <typename T>
-__global__ void __launch_bounds__(256) router_bwd_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ gates,
-    const float* __restrict__ dg_part, int dg_ld, int dg_n, const T* __restrict__ w_router,
-    const T* __restrict__ x, const float* __restrict__ dx_acc, T* __restrict__ dx,
-    float* __restrict__ part, int64_t Tn, int d, int E, int k, int64_t per_block) {
-  extern __shared__ __align__(16) float s_acc[];  // [E][d] f32, then W_r^T [E][d] (T)
-  T* s_wt = reinterpret_cast<T*>(s_acc + (size_t)E * d);
-  __shared__ int s_e[256];
-  __shared__ float s_g[256], s_dg[256], s_ds[256];
-  const int tid = threadIdx.x;
-  for (int i = tid; i < E * d; i += blockDim.x) {
-    s_acc[i] = 0.f;
+__global__ void __launch_bounds__(256) router_dx_kernel(const int32_t* __restrict__ idx,
+                                                        const float* __restrict__ dsel,
+                                                        const T* __restrict__ w_router,
+                                                        const float* __restrict__ dx_acc,
+                                                        T* __restrict__ dx, int64_t Tn, int d,
+                                                        int E, int k) {
+  extern __shared__ __align__(16) unsigned char s_raw[];
+  T* s_wt = reinterpret_cast<T*>(s_raw);  // [E][d]
+  for (int i = threadIdx.x; i < E * d; i += blockDim.x) {
     const int r = i / E, e = i % E;  // coalesced read of W_r[r][e]
     s_wt[e * d + r] = w_router[i];
   }
-  const int64_t t0 = blockIdx.x * per_block;
-  const int64_t t1 = t0 + per_block < Tn ? t0 + per_block : Tn;
+  __syncthreads();
+  const int cpt = d / 4;                  // float4 chunks per token
+  const int tpb = blockDim.x / cpt;       // tokens per block pass
+  const int c = threadIdx.x % cpt, u = threadIdx.x / cpt;
+  if (u >= tpb) return;
+  for (int64_t t = (int64_t)blockIdx.x * tpb + u; t < Tn; t += (int64_t)gridDim.x * tpb) {
+    float4 v = reinterpret_cast<const float4*>(dx_acc + t * d)[c];
+    for (int j = 0; j < k; ++j) {
+      const int e = __ldg(idx + t * k + j);
+      const float ds = __ldg(dsel + t * k + j);
+      const T* w = s_wt + e * d + 4 * c;
+      v.x = fmaf(ds, to_f32(w[0]), v.x);
+      v.y = fmaf(ds, to_f32(w[1]), v.y);
+      v.z = fmaf(ds, to_f32(w[2]), v.z);
+      v.w = fmaf(ds, to_f32(w[3]), v.w);
+    }
+    T* o = dx + t * d + 4 * c;
+    o[0] = from_f32<T>(v.x);
+    o[1] = from_f32<T>(v.y);
+    o[2] = from_f32<T>(v.z);
+    o[3] = from_f32<T>(v.w);
+  }
+}
+
+// dW_r partial of one token range: thread i owns input dimension i and its
+// column of the shared accumulator [E][256], so the order of the adds is
+// fixed; the range's (expert, dsel) pairs are staged in shared memory.
+template <typename T>
+__global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
+                                                        const int32_t* __restrict__ idx,
+                                                        const float* __restrict__ dsel,
+                                                        int64_t Tn, int d, int E, int k,
+                                                        int64_t per_range, float* part) {
+  extern __shared__ __align__(16) float s_acc[];  // [E][256]
+  __shared__ int s_e[256];
+  __shared__ float s_ds[256];
+  const int tid = threadIdx.x;
+  const int i = blockIdx.y * 256 + tid;
+  for (int e = 0; e < E; ++e) s_acc[e * 256 + tid] = 0.f;
+  const int64_t t0 = blockIdx.x * per_range;
+  const int64_t t1 = t0 + per_range < Tn ? t0 + per_range : Tn;
   const int CH = 256 / k;
   for (int64_t tc = t0; tc < t1; tc += CH) {
     const int nt = (int)(t1 - tc < CH ? t1 - tc : CH);
-    const int npair = nt * k;
     __syncthreads();
-    if (tid < npair) {
-      const int64_t p = tc * k + tid;
-      s_e[tid] = idx[p];
-      s_g[tid] = gates[p];
-      float dg = 0.f;
-      const float* row = dg_part + p * dg_ld;
-      for (int q = 0; q < dg_n; ++q) dg += row[q];
-      s_dg[tid] = dg;
+    if (tid < nt * k) {
+      s_e[tid] = idx[tc * k + tid];
+      s_ds[tid] = dsel[tc * k + tid];
     }
     __syncthreads();
-    if (tid < npair) {
-      const int base = (tid / k) * k;
-      float sgd = 0.f;
-      for (int j = 0; j < k; ++j) sgd = fmaf(s_g[base + j], s_dg[base + j], sgd);
-      s_ds[tid] = s_g[tid] * (s_dg[tid] - sgd);
-    }
-    __syncthreads();
-    for (int i = tid; i < d; i += blockDim.x) {
-#pragma unroll 4
-      for (int u = 0; u < nt; ++u) {
-        const int64_t t = tc + u;
-        float v = dx_acc[t * d + i];
-        const float xv = to_f32(x[t * d + i]);
+    if (i < d) {
+      int u = 0;
+      for (; u + 8 <= nt; u += 8) {
+        float xv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xv[q] = to_f32(x[(tc + u + q) * d + i]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          for (int j = 0; j < k; ++j) {
+            const int e = s_e[(u + q) * k + j];
+            s_acc[e * 256 + tid] = fmaf(xv[q], s_ds[(u + q) * k + j], s_acc[e * 256 + tid]);
+          }
+      }
+      for (; u < nt; ++u) {
+        const float xv = to_f32(x[(tc + u) * d + i]);
         for (int j = 0; j < k; ++j) {
           const int e = s_e[u * k + j];
-          const float ds = s_ds[u * k + j];
-          v = fmaf(ds, to_f32(s_wt[e * d + i]), v);
-          s_acc[e * d + i] = fmaf(xv, ds, s_acc[e * d + i]);
+          s_acc[e * 256 + tid] = fmaf(xv, s_ds[u * k + j], s_acc[e * 256 + tid]);
         }
-        dx[t * d + i] = from_f32<T>(v);
       }
     }
   }
-  __syncthreads();
-  float* out = part + (int64_t)blockIdx.x * d * E;
-  for (int i = tid; i < E * d; i += blockDim.x) {
-    const int r = i / E, e = i % E;
-    out[i] = s_acc[e * d + r];
+  if (i < d) {
+    float* out = part + ((int64_t)blockIdx.x * d + i) * E;
+    for (int e = 0; e < E; ++e) out[e] = s_acc[e * 256 + tid];
   }
 }
 
@@ -146,36 +190,51 @@ template <typename T>
 void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                        int dg_ld, void* ws, cudaStream_t s) {
   const int dm = d.d_model, E = d.experts, k = d.top_k;
-  float* part = at<float>(ws, L.dwr_part);
   if (d.tokens == 0) {
     zero_fill_f32(p.dw_router, (int64_t)dm * E, s);
     return;
   }
-  const size_t smem = (size_t)E * dm * (sizeof(float) + sizeof(T));
+  float* dsel = at<float>(ws, L.dsel);
+  float* part = at<float>(ws, L.dwr_part);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(router_bwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(router_dx_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kRouterBwdSmem);
+    cudaFuncSetAttribute(router_dw_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          kRouterBwdSmem);
     attr_set = true;
   }
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int CH = 256 / k;
-  int64_t blocks = (d.tokens + CH - 1) / CH;
-  const int64_t cap = sms < kRouterBwdRanges ? sms : kRouterBwdRanges;
-  if (blocks > cap) blocks = cap;
-  const int64_t per_block = (d.tokens + blocks - 1) / blocks;
-  MOE_LAUNCH("router_bwd", s,
-             router_bwd_kernel<T><<<(unsigned)blocks, 256, smem, s>>>(
-                 p.topk_idx, p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n,
-                 reinterpret_cast<const T*>(p.w_router), reinterpret_cast<const T*>(p.x),
-                 at<float>(ws, L.dx_acc), reinterpret_cast<T*>(p.dx), part, d.tokens, dm, E, k,
-                 per_block));
+
+  MOE_LAUNCH("router_dsel", s,
+             router_dsel_kernel<<<(unsigned)((d.tokens + 255) / 256), 256, 0, s>>>(
+                 p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, dsel));
+
+  const int tpb = 256 / (dm / 4) > 0 ? 256 / (dm / 4) : 1;
+  int64_t bx = (d.tokens + tpb - 1) / tpb;
+  if (bx > (int64_t)sms * 4) bx = (int64_t)sms * 4;
+  MOE_LAUNCH("router_dx", s,
+             router_dx_kernel<T><<<(unsigned)bx, 256, sizeof(T) * E * dm, s>>>(
+                 p.topk_idx, dsel, reinterpret_cast<const T*>(p.w_router), at<float>(ws, L.dx_acc),
+                 reinterpret_cast<T*>(p.dx), d.tokens, dm, E, k));
+
+  const int ny = (dm + 255) / 256;
+  int64_t ranges = (int64_t)sms * 4 / ny;
+  const int64_t by_tokens = (d.tokens + 63) / 64;
+  if (ranges > by_tokens) ranges = by_tokens;
+  if (ranges > kRouterBwdRanges) ranges = kRouterBwdRanges;
+  if (ranges < 1) ranges = 1;
+  const int64_t per_range = (d.tokens + ranges - 1) / ranges;
+  MOE_LAUNCH("router_dw", s,
+             router_dw_kernel<T><<<dim3((unsigned)ranges, ny), 256, sizeof(float) * E * 256, s>>>(
+                 reinterpret_cast<const T*>(p.x), p.topk_idx, dsel, d.tokens, dm, E, k, per_range,
+                 part));
   const int64_t n = (int64_t)dm * E;
   MOE_LAUNCH("router_dw_reduce", s,
              router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
-                 part, (int)blocks, n, p.dw_router));
+                 part, (int)ranges, n, p.dw_router));
 }
 
 }  // namespace
@@ -198,7 +257,9 @@ void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs&
 
 bool router_backward_supported(const moe_dims& d) {
   const size_t elem = d.dtype == MOE_BF16 ? 2 : 4;
-  return (size_t)d.experts * d.d_model * (4 + elem) <= (size_t)kRouterBwdSmem;
+  return (size_t)d.experts * d.d_model * elem <= (size_t)kRouterBwdSmem &&
+         (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem && d.d_model % 4 == 0 &&
+         d.d_model <= 1024;
 }
 
 }  // namespace moe

@@ -16,7 +16,7 @@ constexpr int kPermChunk = 32 * kPermRounds;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 constexpr int kLossBlocks = 512;  // fixed partial count of the loss reduction
-constexpr int kRouterBwdRanges = 256;  // max token ranges of the router-weight gradient partials
+constexpr int kRouterBwdRanges = 608;  // max token ranges of the router-weight gradient partials
 constexpr int kRouterBwdSmem = 200 * 1024;  // router backward: W_r^T + dW_r partial in shared memory
 
 // ---- element access ---------------------------------------------------------
@@ -40,7 +40,8 @@ __device__ __forceinline__ void report_error(int* status, int code, int detail) 
 struct Layout {
   size_t status, warp_counts, warp_base, counts, poff, rowpair, tokrow, tiles, ntiles,
       loss_part, logits;
-  size_t dg_part, dA, gH, dx_acc, dAs, gHs, dwr_part;
+  size_t xs;  // expert-sorted copy of the token rows [padded rows, d]
+  size_t dg_part, dA, gH, dx_acc, dAs, gHs, dys, dsel, dwr_part;
   size_t total;
   int64_t P, PPcap, MTcap, NWc;
   int elem;  // bytes per storage element
@@ -80,6 +81,7 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.ntiles = take(sizeof(int) * 4);
   L.loss_part = take(sizeof(float) * kLossBlocks);
   L.logits = take(sizeof(float) * T * E);
+  L.xs = take((size_t)L.elem * L.PPcap * dm);
   if (mode == MOE_SAVE_FOR_BWD) {
     L.dg_part = take(sizeof(float) * L.P * 2 * (h / 64));
     L.dA = take((size_t)L.elem * L.PPcap * 2 * h);
@@ -87,6 +89,8 @@ inline Layout make_layout(const moe_dims& d, int mode) {
     L.dx_acc = take(sizeof(float) * T * dm);
     L.dAs = take((size_t)L.elem * T * 2 * hs);
     L.gHs = take((size_t)L.elem * T * hs);
+    L.dys = take((size_t)L.elem * L.PPcap * dm);
+    L.dsel = take(sizeof(float) * T * d.top_k);
     L.dwr_part = take(sizeof(float) * kRouterBwdRanges * dm * E);
   }
   L.total = o;

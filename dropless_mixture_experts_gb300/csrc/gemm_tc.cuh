@@ -5,10 +5,8 @@
 // the forward pass and the train step (the experts_grouped_swiglu piece of
 // kernel_gmm_gpu.json and the value_and_grad train step of gpu_moe_h100.json):
 //
-//   warp 0     producer: TMA tile loads, or TMA gather4 loads that fetch the
-//              token rows of the expert-sorted order straight from x / dy
-//              (the gather is fused into the operand load); the token index
-//              of every sorted row is prefetched ahead of its k-block
+//   warp 0     producer: TMA tile loads of both operands over the expert's
+//              ragged row range of the expert-sorted activations
 //   warp 1     tensor-memory allocation and the MMA issuer (one thread)
 //   warps 2-9  epilogue, two warps per 32-lane quarter of the accumulator
 //              splitting its columns: tcgen05.ld, then the fused SwiGLU,
@@ -30,8 +28,8 @@
 namespace moe {
 namespace tcg {
 
-enum AKind { A_K_TMA = 0, A_K_GATHER = 1, A_MN_TMA = 2, A_MN_GATHER = 3 };
-enum BKind { B_MN_TMA = 0, B_K_TMA = 1, B_MN_GATHER = 2 };
+enum AKind { A_K_TMA = 0, A_MN_TMA = 2 };   // A tile K-major (rows x 64 K) or MN-major
+enum BKind { B_MN_TMA = 0, B_K_TMA = 1 };   // B tile MN-major (64 K rows x BN) or K-major
 enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4 };
 
 constexpr int kEpiWarps = 8;
@@ -44,7 +42,6 @@ struct Params {
   const int* counts = nullptr;      // routed DW kinds: rows per expert
   const int* poff = nullptr;        // routed DW kinds: first padded row per expert
   const int32_t* rowpair = nullptr; // padded row -> pair id (-1 = padding)
-  const int32_t* tokrow = nullptr;  // padded row -> token (0 on padding rows)
   int top_k = 1;
   int64_t rows = 0;                 // dense kinds: number of tokens
   int n_nt = 1;                     // column tiles
@@ -78,14 +75,13 @@ struct Cfg {
   static constexpr bool DW = EK == E_DW;
   static constexpr bool DUALN = EK == E_GU;
   static constexpr bool DUALK = EK == E_DX;
-  static constexpr bool KGATHER = AK == A_MN_GATHER || BKIND == B_MN_GATHER;
   static constexpr int BM = 128, BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (196 * 1024 / STAGE_BYTES) > 8 ? 8 : (196 * 1024 / STAGE_BYTES);
-  static constexpr bool A_MN = AK == A_MN_TMA || AK == A_MN_GATHER;
-  static constexpr bool B_MN = BKIND != B_K_TMA;
+  static constexpr bool A_MN = AK == A_MN_TMA;
+  static constexpr bool B_MN = BKIND == B_MN_TMA;
   static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
@@ -97,17 +93,24 @@ struct Tile {
   int e, row0, nvalid, m0, n0, kb0, kb1, nt;
 };
 
-template <class C>
+// Tile t of the persistent schedule.  META=false skips the per-tile
+// metadata loads of the routed row kinds (the MMA issuer only needs the K
+// range, which is the same for every tile of those kinds).
+template <class C, bool META = true>
 __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles, Tile& tl) {
   if constexpr (!C::DW) {
     const int mt = t / p.n_nt;
     tl.nt = t % p.n_nt;
     if (mt >= nrow_tiles) return false;
     if constexpr (C::ROUTED) {
-      const int4 v = p.tiles[mt];
-      tl.e = v.x;
-      tl.row0 = v.y;
-      tl.nvalid = v.z;
+      if constexpr (META) {
+        const int4 v = p.tiles[mt];
+        tl.e = v.x;
+        tl.row0 = v.y;
+        tl.nvalid = v.z;
+      } else {
+        tl.e = tl.row0 = tl.nvalid = 0;
+      }
     } else {
       tl.e = 0;
       tl.row0 = mt * C::BM;
@@ -199,10 +202,6 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
                       pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
 }
 
-__device__ __forceinline__ int4 ld_tok4(const int32_t* p) {
-  return __ldg(reinterpret_cast<const int4*>(p));
-}
-
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
@@ -245,115 +244,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool aborted = false;
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
-    int stage = 0;
-    uint32_t phase = 0;
-    Tile tl, tn;
-    int t = blockIdx.x;
-    bool have = get_tile<C>(p, t, nrow_tiles, tl);
-    // A_K_GATHER: lane l owns the token rows 4l..4l+3 of a row tile, loaded
-    // one tile ahead
-    int4 tok_cur = make_int4(0, 0, 0, 0), tok_next = make_int4(0, 0, 0, 0);
-    if constexpr (C::AK == A_K_GATHER) {
-      if (have) tok_cur = ld_tok4(p.tokrow + tl.row0 + 4 * lane);
-    }
-    while (have && !aborted) {
-      const int tnext = t + gridDim.x;
-      const bool have_next = get_tile<C>(p, tnext, nrow_tiles, tn);
-      if constexpr (C::AK == A_K_GATHER) {
-        if (have_next) tok_next = ld_tok4(p.tokrow + tn.row0 + 4 * lane);
-      }
-      // K-row gathers: lanes (i = lane & 15) own K rows 4i..4i+3 of every
-      // k-block; a ring prefetches them four k-blocks ahead
-      int4 ring[4];
-      const int32_t* kt = p.tokrow + tl.row0 + 4 * (lane & 15);
-      if constexpr (C::KGATHER) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          ring[i] = tl.kb0 + i < tl.kb1 ? ld_tok4(kt + (tl.kb0 + i) * C::BK) : make_int4(0, 0, 0, 0);
-      }
-      int brow0 = 0;
-      if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
-      if constexpr (C::DW && C::BKIND != B_MN_GATHER) brow0 = tl.row0;
-      for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-        int4 tk = make_int4(0, 0, 0, 0);
-        if constexpr (C::KGATHER) {
-          tk = ring[0];
-          ring[0] = ring[1];
-          ring[1] = ring[2];
-          ring[2] = ring[3];
-          ring[3] = kb + 4 < tl.kb1 ? ld_tok4(kt + (kb + 4) * C::BK) : make_int4(0, 0, 0, 0);
-        }
-        if (!wait_or_abort(&sh->empty[stage], phase ^ 1, sh, p.status, 100)) {
-          aborted = true;
-          break;
-        }
-        uint8_t* sA = smem + stage * C::STAGE_BYTES;
-        uint8_t* sB = sA + C::A_BYTES;
-        uint64_t* fb = &sh->full[stage];
-        if (lane == 0) tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-        __syncwarp();
-        // ---- A ----
-        if constexpr (C::AK == A_K_TMA) {
-          if (lane == 0) tc::tma_load_2d(sA, &mA, fb, kb * C::BK, tl.row0);
-        } else if constexpr (C::AK == A_K_GATHER) {
-          tc::tma_gather4(sA + lane * 512, &mA, fb, kb * C::BK, tok_cur.x, tok_cur.y, tok_cur.z,
-                          tok_cur.w);
-        } else if constexpr (C::AK == A_MN_TMA) {
-          if (lane == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      Tile tl;
+      for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+        int brow0 = 0;
+        if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
+        if constexpr (C::DW) brow0 = tl.row0;
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
+          if (!wait_or_abort(&sh->empty[stage], phase ^ 1, sh, p.status, 100)) {
+            aborted = true;
+            break;
+          }
+          uint8_t* sA = smem + stage * C::STAGE_BYTES;
+          uint8_t* sB = sA + C::A_BYTES;
+          uint64_t* fb = &sh->full[stage];
+          tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          // ---- A ----
+          if constexpr (C::AK == A_K_TMA) {
+            tc::tma_load_2d(sA, &mA, fb, kb * C::BK, tl.row0);
+          } else {  // MN-major: two 64-column blocks of 64 K rows
             const int krow = (C::DW ? tl.row0 : 0) + kb * C::BK;
             tc::tma_load_2d(sA, &mA, fb, tl.m0, krow);
             tc::tma_load_2d(sA + 8192, &mA, fb, tl.m0 + 64, krow);
           }
-        } else {  // A_MN_GATHER: two 64-column blocks, 16 gather4 each
-          const int j = lane >> 4, i = lane & 15;
-          tc::tma_gather4(sA + j * 8192 + i * 512, &mA, fb, tl.m0 + 64 * j, tk.x, tk.y, tk.z, tk.w);
-        }
-        // ---- B ----
-        if constexpr (C::BKIND == B_MN_TMA) {
-          if (lane == 0) {
+          // ---- B ----
+          if constexpr (C::BKIND == B_MN_TMA) {
 #pragma unroll
             for (int j = 0; j < C::BN / 64; ++j) {
               const bool second = C::DUALN && j >= C::BN / 128;
               const int x = C::DUALN ? tl.n0 + 64 * (second ? j - C::BN / 128 : j) : tl.n0 + 64 * j;
               tc::tma_load_2d(sB + j * 8192, second ? &mB1 : &mB0, fb, x, brow0 + kb * C::BK);
             }
-          }
-        } else if constexpr (C::BKIND == B_K_TMA) {
-          if (lane == 0) {
+          } else {
             const bool second = C::DUALK && kb >= p.kb_split;
             const int x = (second ? kb - p.kb_split : kb) * C::BK;
             tc::tma_load_2d(sB, second ? &mB1 : &mB0, fb, x, brow0 + tl.n0);
           }
-        } else {  // B_MN_GATHER: BN/64 column blocks, 16 gather4 each
-          if constexpr (C::BN >= 128) {
-#pragma unroll
-            for (int it = 0; it < C::BN / 128; ++it) {
-              const int g = lane + 32 * it;
-              const int j = g >> 4, i = g & 15;
-              tc::tma_gather4(sB + j * 8192 + i * 512, &mB0, fb, tl.n0 + 64 * j, tk.x, tk.y, tk.z,
-                              tk.w);
-            }
-          } else {
-            if (lane < 16)
-              tc::tma_gather4(sB + lane * 512, &mB0, fb, tl.n0, tk.x, tk.y, tk.z, tk.w);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
           }
         }
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
       }
-      t = tnext;
-      tl = tn;
-      have = have_next;
-      tok_cur = tok_next;
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     int stage = 0, acc = 0;
     uint32_t phase = 0, aphase = 0;
     Tile tl;
-    for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+    for (int t = blockIdx.x; !aborted && get_tile<C, false>(p, t, nrow_tiles, tl);
+         t += gridDim.x) {
       if (!wait_or_abort(&sh->tempty[acc], aphase ^ 1, sh, p.status, 200)) {
         aborted = true;
         break;
@@ -403,8 +346,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = 32 * q + lane;
     int acc = 0;
     uint32_t aphase = 0;
-    Tile tl;
-    for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+    Tile tl, tn;
+    int t = blockIdx.x;
+    bool have = get_tile<C>(p, t, nrow_tiles, tl);
+    while (have && !aborted) {
+      // the next tile's metadata is read while this one is processed
+      const bool have_next = get_tile<C>(p, t + gridDim.x, nrow_tiles, tn);
+      // per-row metadata of this tile (routed kinds): issued before the wait
+      int32_t pr = -1;
+      float gt = 1.f;
+      if constexpr (C::ROUTED && (C::EK == E_DOWN || C::EK == E_DZ || C::EK == E_DX)) {
+        if (row < tl.nvalid) {
+          pr = p.rowpair[(int64_t)tl.row0 + row];
+          if constexpr (C::EK != E_DX) gt = p.gates[pr];
+        } else {
+          gt = 0.f;
+        }
+      }
       if (!wait_or_abort(&sh->tfull[acc], aphase, sh, p.status, 400)) {
         aborted = true;
         break;
@@ -448,13 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // atomic float4 adds) or y_acc[token] += H_s Ws_down (shared expert)
         const bool valid = row < tl.nvalid;
         const int64_t r = (int64_t)tl.row0 + row;
-        int64_t t_out = r;
-        float gt = 1.f;
-        if (C::ROUTED && valid) {
-          const int32_t pr = p.rowpair[r];
-          t_out = pr / p.top_k;
-          gt = p.gates[pr];
-        }
+        const int64_t t_out = C::ROUTED ? (valid ? pr / p.top_k : 0) : r;
         float* dst = p.facc + t_out * p.ld_out + tl.n0;
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
@@ -485,16 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t r = (int64_t)tl.row0 + row;
         const bool exists = C::ROUTED || row < tl.nvalid;
         const bool valid = row < tl.nvalid;
-        int32_t pr = -1;
-        float gt = 1.f;
-        if constexpr (C::ROUTED) {
-          if (valid) {
-            pr = p.rowpair[r];
-            gt = p.gates[pr];
-          } else {
-            gt = 0.f;
-          }
-        }
         const int64_t h = p.ld_out;
         const __nv_bfloat16* AG = reinterpret_cast<const __nv_bfloat16*>(p.in0);
         const __nv_bfloat16* AU = reinterpret_cast<const __nv_bfloat16*>(p.in1);
@@ -538,8 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // float4 adds) or dx_acc = dA_s [Ws_gate | Ws_up]^T (shared, first writer)
         const bool valid = row < tl.nvalid;
         const int64_t r = (int64_t)tl.row0 + row;
-        int64_t t_out = r;
-        if (C::ROUTED && valid) t_out = p.rowpair[r] / p.top_k;
+        const int64_t t_out = C::ROUTED ? (valid ? pr / p.top_k : 0) : r;
         float* dst = p.facc + t_out * p.ld_out + tl.n0;
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
@@ -600,6 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         aphase ^= 1;
       }
+      t += gridDim.x;
+      tl = tn;
+      have = have_next;
     }
   }
 

@@ -19,6 +19,9 @@ void prof_end(cudaStream_t s);
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s);
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s);
 void clear_status(int* status, cudaStream_t s);
+// expert-sorted copy of token rows: out[r] = src[tokrow[r]] for r < *used
+void launch_gather_rows(const void* src, const int32_t* tokrow, const int* used, void* out,
+                        int64_t cap_rows, int64_t row_bytes, cudaStream_t s);
 
 // routing and permutation (route_permute.cu)
 void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,

@@ -17,6 +17,35 @@ static void zero_fill(T* p, int64_t n, cudaStream_t s) {
   MOE_LAUNCH("zero_fill", s, zero_kernel<T><<<(unsigned)blocks, 256, 0, s>>>(p, n));
 }
 
+// out[r, :] = src[tokrow[r], :] for the padded rows r < *used (a count the
+// permutation wrote on the device): one warp per row, 16-byte copies.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                          const int32_t* __restrict__ tokrow,
+                                                          const int* __restrict__ used,
+                                                          uint4* __restrict__ out, int vecs,
+                                                          int64_t cap) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n = *used < cap ? *used : cap;
+  const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5; r < n; r += warps) {
+    const int64_t t = tokrow[r];
+    const uint4* s = src + t * vecs;
+    uint4* o = out + r * vecs;
+    for (int v = lane; v < vecs; v += 32) o[v] = __ldg(s + v);
+  }
+}
+
+void launch_gather_rows(const void* src, const int32_t* tokrow, const int* used, void* out,
+                        int64_t cap_rows, int64_t row_bytes, cudaStream_t s) {
+  if (cap_rows <= 0) return;
+  int64_t blocks = (cap_rows + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  MOE_LAUNCH("gather_rows", s,
+             gather_rows_kernel<<<(unsigned)blocks, 256, 0, s>>>(
+                 reinterpret_cast<const uint4*>(src), tokrow, used, reinterpret_cast<uint4*>(out),
+                 (int)(row_bytes / 16), cap_rows));
+}
+
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s) { zero_fill<int32_t>(p, n, s); }
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s) { zero_fill<float>(p, n, s); }
 void clear_status(int* status, cudaStream_t s) { zero_fill<int>(status, 2, s); }

@@ -1,6 +1,8 @@
-// Backward launches of the tensor-core GEMMs (bf16 storage):
+// Backward launches of the tensor-core GEMMs (bf16 storage).  The upstream
+// gradient rows are first gathered into expert-sorted order (one HBM pass);
+// the forward's sorted copy of x is reused.  Then
 //   DZ  Z = dy_t W_down[e]^T with the SwiGLU backward and the gate-gradient
-//       partials in the epilogue (dy rows gathered in the operand load)
+//       partials in the epilogue
 //   DX  dx_acc[t] += [dA_g | dA_u] [W_gate[e] | W_up[e]]^T
 //   DW  dW_down[e] = gH^T dy_t and dW_gate[e] | dW_up[e] = x_t^T [dA_g | dA_u]
 //       with K the expert's own rows (ragged), split over CTAs when the
@@ -27,12 +29,11 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   q.kb_total = dm / 64;
   q.ld_out = h;
   if (routed) {
-    if (!make_map(&a, p.dy, d.tokens, dm, 64, 1)) return false;
+    if (!make_map(&a, at<void>(ws, L.dys), L.PPcap, dm, 64, 128)) return false;
     if (!make_map(&b0, p.w_down, (uint64_t)d.experts * h, dm, 64, BN)) return false;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
-    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
@@ -42,8 +43,7 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.out1 = at<void>(ws, L.gH);
     q.dg_part = at<float>(ws, L.dg_part);
     q.dg_ld = 2 * h / 64;
-    launch_tc<Cfg<A_K_GATHER, B_K_TMA, E_DZ, BN, true>>(a, b0, b0, q, L.MTcap * q.n_nt, "tc_dz",
-                                                         s);
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, true>>(a, b0, b0, q, L.MTcap * q.n_nt, "tc_dz", s);
   } else {
     if (!make_map(&a, p.dy, d.tokens, dm, 64, 128)) return false;
     if (!make_map(&b0, p.ws_down, h, dm, 64, BN)) return false;
@@ -79,7 +79,6 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
-    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = dm;
     launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt, "tc_dx", s);
@@ -102,6 +101,8 @@ int splits_for(int64_t tiles, int64_t kblocks_per_tile) {
   return s;
 }
 
+// dW_down[e] = sum over the expert's rows of gH_r^T dy_r: A = gH (MN-major:
+// rows are K), B = sorted dy (MN-major)
 template <int BN>
 bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
              cudaStream_t s) {
@@ -123,13 +124,10 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   q.facc = out;
   if (routed) {
     if (!make_map(&a, at<void>(ws, L.gH), L.PPcap, h, 64, 64)) return false;
-    if (!make_map(&b0, p.dy, d.tokens, dm, 64, 1)) return false;
+    if (!make_map(&b0, at<void>(ws, L.dys), L.PPcap, dm, 64, 64)) return false;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    q.rowpair = at<int32_t>(ws, L.rowpair);
-    q.tokrow = at<int32_t>(ws, L.tokrow);
-    q.top_k = d.top_k;
-    launch_tc<Cfg<A_MN_TMA, B_MN_GATHER, E_DW, BN, true>>(
+    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(
         a, b0, b0, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
   } else {
     if (!make_map(&a, at<void>(ws, L.gHs), d.tokens, h, 64, 64)) return false;
@@ -141,6 +139,8 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   return true;
 }
 
+// dW_gate[e] | dW_up[e] = sum over the expert's rows of x_r^T [dA_g | dA_u]:
+// A = sorted x (MN-major), B = dA (MN-major)
 template <int BN>
 bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
                cudaStream_t s) {
@@ -167,14 +167,11 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
   q.facc = g;
   q.facc2 = u;
   if (routed) {
-    if (!make_map(&a, p.x, d.tokens, dm, 64, 1)) return false;
+    if (!make_map(&a, at<void>(ws, L.xs), L.PPcap, dm, 64, 64)) return false;
     if (!make_map(&b0, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 64)) return false;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    q.rowpair = at<int32_t>(ws, L.rowpair);
-    q.tokrow = at<int32_t>(ws, L.tokrow);
-    q.top_k = d.top_k;
-    launch_tc<Cfg<A_MN_GATHER, B_MN_TMA, E_DW, BN, true>>(
+    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(
         a, b0, b0, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
   } else {
     if (!make_map(&a, p.x, d.tokens, dm, 64, 64)) return false;
@@ -206,6 +203,8 @@ int tc_dz_bn(int h) { return pick_bn(h); }
 
 bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                        cudaStream_t s) {
+  launch_gather_rows(p.dy, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1,
+                     at<void>(ws, L.dys), L.PPcap, (int64_t)d.d_model * 2, s);
   // the shared expert's DX is the first writer of dx_acc; without it, zero it
   if (d.shared_hidden > 0) {
     if (!backward_one(d, L, p, ws, false, s)) return false;

@@ -1,7 +1,8 @@
-// Forward launches of the tensor-core GEMMs (bf16 storage):
-//   gate/up projection of the expert-sorted rows with the token gather in the
-//   operand load and SwiGLU in the epilogue, then the down projection with
-//   the gate-weighted combine in the epilogue; and the dense shared expert.
+// Forward launches of the tensor-core GEMMs (bf16 storage): the token rows
+// are first gathered into expert-sorted order (one HBM pass), then
+//   gate/up projection of the sorted rows with SwiGLU in the epilogue, and
+//   the down projection with the gate-weighted combine in the epilogue;
+// plus the dense shared expert.
 #include "gemm_tc.cuh"
 
 namespace moe {
@@ -21,20 +22,19 @@ bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, vo
   q.kb_total = dm / 64;
   q.ld_out = h;
   if (routed) {
-    if (!make_map(&a, p.x, d.tokens, dm, 64, 1)) return false;
+    if (!make_map(&a, at<void>(ws, L.xs), L.PPcap, dm, 64, 128)) return false;
     if (!make_map(&b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, 64)) return false;
     if (!make_map(&b1, p.w_up, (uint64_t)d.experts * dm, h, 64, 64)) return false;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
-    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = dm;
     q.out0 = p.h_buf;
     q.out1 = mode == MOE_SAVE_FOR_BWD ? p.a_gate : nullptr;
     q.out2 = mode == MOE_SAVE_FOR_BWD ? p.a_up : nullptr;
-    launch_tc<Cfg<A_K_GATHER, B_MN_TMA, E_GU, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt,
-                                                          "tc_gateup", s);
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt,
+                                                       "tc_gateup", s);
   } else {
     if (!make_map(&a, p.x, d.tokens, dm, 64, 128)) return false;
     if (!make_map(&b0, p.ws_gate, dm, h, 64, 64)) return false;
@@ -68,7 +68,6 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
-    q.tokrow = at<int32_t>(ws, L.tokrow);
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
@@ -105,6 +104,8 @@ bool down_any(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, 
 bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                     cudaStream_t s) {
   zero_fill_f32(p.y_acc, d.tokens * (int64_t)d.d_model, s);
+  launch_gather_rows(p.x, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1, at<void>(ws, L.xs),
+                     L.PPcap, (int64_t)d.d_model * 2, s);
   if (!gateup_any(d, L, mode, p, ws, true, s)) return false;
   return down_any(d, L, p, ws, true, s);
 }
