@@ -10,7 +10,11 @@
 //   warp 1     tensor-memory allocation and the MMA issuer (one thread)
 //   warps 2-9  epilogue, two warps per 32-lane quarter of the accumulator
 //              splitting its columns: tcgen05.ld, then the fused SwiGLU,
-//              gate-weighted combine, SwiGLU backward or gradient stores
+//              gate-weighted combine, SwiGLU backward or gradient stores.
+//              bf16 tiles the epilogue reads or writes (the SwiGLU outputs,
+//              the saved pre-activations, the backward's dA and gate*H) go
+//              through a per-warp 32x32 staging tile in shared memory and
+//              move with TMA loads and stores.
 //
 // Tiles are 128 rows x BN columns with K blocks of 64 (one 128-byte swizzle
 // row of bf16); shared memory holds a ring of STAGES operand stages and the
@@ -34,6 +38,15 @@ enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4 };
 
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSmemLimit = 232448;  // dynamic shared memory per block (227 KB)
+
+// Tensor maps of one launch: the two operands (B may come from two maps,
+// split along N or K) and the epilogue's bf16 outputs / inputs.
+struct Maps {
+  CUtensorMap a, b0, b1;
+  CUtensorMap o0, o1, o2;  // GU: H, a_g, a_u;  DZ: dA, gate*H
+  CUtensorMap i0, i1;      // DZ: saved a_g, a_u
+};
 
 struct Params {
   // scheduling
@@ -54,11 +67,7 @@ struct Params {
   int M = 0, N = 0;                 // DW output dims / row-kind output columns
   // epilogue
   const float* gates = nullptr;
-  void* out0 = nullptr;
-  void* out1 = nullptr;
-  void* out2 = nullptr;
-  const void* in0 = nullptr;
-  const void* in1 = nullptr;
+  int save = 0;                     // GU: also store a_g, a_u
   float* facc = nullptr;
   float* facc2 = nullptr;
   float* dg_part = nullptr;         // DZ: [pairs, dg_ld], entry 2*column-tile + half
@@ -79,14 +88,20 @@ struct Cfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196 * 1024 / STAGE_BYTES) > 8 ? 8 : (196 * 1024 / STAGE_BYTES);
+  // per-warp staging: 2 KB per bf16 32x32 tile
+  static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048 : EK == E_DZ ? 5 * 2048 : 0;
+  static constexpr int FIXED = kEpiWarps * EPI_BYTES + 1024 + 256;
+  static constexpr int STAGES = (kSmemLimit - FIXED) / STAGE_BYTES > 8
+                                    ? 8
+                                    : (kSmemLimit - FIXED) / STAGE_BYTES;
   static constexpr bool A_MN = AK == A_MN_TMA;
   static constexpr bool B_MN = BKIND == B_MN_TMA;
   static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + FIXED;
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(!DUALN || BN >= 128, "the gate/up tile holds 64-column halves");
+  static_assert(STAGES >= 2, "shared memory");
 };
 
 struct Tile {
@@ -152,6 +167,7 @@ struct Shared {
   uint64_t empty[8];
   uint64_t tfull[2];
   uint64_t tempty[2];
+  uint64_t ebar[kEpiWarps];  // per epilogue warp: its staged input tiles
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -178,38 +194,37 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 
 __device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float (&v)[32]) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
+// One thread's row (32 bf16) of a 64-byte-swizzled 32x32 staging tile.
+__device__ __forceinline__ void stage_read_row(const uint8_t* tile, int r, float (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint4 u = s[i];
+  for (int k = 0; k < 4; ++k) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::sw64_off(r, k));
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
-      const float2 f = __bfloat1622float2(b);
-      v[8 * i + 2 * j] = f.x;
-      v[8 * i + 2 * j + 1] = f.y;
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      v[8 * k + 2 * j] = f.x;
+      v[8 * k + 2 * j + 1] = f.y;
     }
   }
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+__device__ __forceinline__ void stage_write_row(uint8_t* tile, int r, const float (&v)[32]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    d[i] = make_uint4(pack_bf16(v[8 * i], v[8 * i + 1]), pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                      pack_bf16(v[8 * i + 4], v[8 * i + 5]), pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4*>(tile + tc::sw64_off(r, k)) =
+        make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                   pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
 }
 
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB0,
-                   const __grid_constant__ CUtensorMap mB1, const Params p) {
+    tc_gemm_kernel(const __grid_constant__ Maps m, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Shared* sh = reinterpret_cast<Shared*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;
+  Shared* sh = reinterpret_cast<Shared*>(epi + kEpiWarps * C::EPI_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -221,13 +236,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&sh->tfull[a], 1);
       tc::mbar_init(&sh->tempty[a], kEpiWarps);
     }
+    for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&sh->ebar[w], 1);
     sh->abort = 0;
     tc::fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tc::tma_prefetch_desc(&mA);
-    tc::tma_prefetch_desc(&mB0);
-    tc::tma_prefetch_desc(&mB1);
+    tc::tma_prefetch_desc(&m.a);
+    tc::tma_prefetch_desc(&m.b0);
+    tc::tma_prefetch_desc(&m.b1);
   }
   if (warp == 1) {
     tc::tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
@@ -263,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           // ---- A ----
           if constexpr (C::AK == A_K_TMA) {
-            tc::tma_load_2d(sA, &mA, fb, kb * C::BK, tl.row0);
+            tc::tma_load_2d(sA, &m.a, fb, kb * C::BK, tl.row0);
           } else {  // MN-major: two 64-column blocks of 64 K rows
             const int krow = (C::DW ? tl.row0 : 0) + kb * C::BK;
-            tc::tma_load_2d(sA, &mA, fb, tl.m0, krow);
-            tc::tma_load_2d(sA + 8192, &mA, fb, tl.m0 + 64, krow);
+            tc::tma_load_2d(sA, &m.a, fb, tl.m0, krow);
+            tc::tma_load_2d(sA + 8192, &m.a, fb, tl.m0 + 64, krow);
           }
           // ---- B ----
           if constexpr (C::BKIND == B_MN_TMA) {
@@ -275,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < C::BN / 64; ++j) {
               const bool second = C::DUALN && j >= C::BN / 128;
               const int x = C::DUALN ? tl.n0 + 64 * (second ? j - C::BN / 128 : j) : tl.n0 + 64 * j;
-              tc::tma_load_2d(sB + j * 8192, second ? &mB1 : &mB0, fb, x, brow0 + kb * C::BK);
+              tc::tma_load_2d(sB + j * 8192, second ? &m.b1 : &m.b0, fb, x, brow0 + kb * C::BK);
             }
           } else {
             const bool second = C::DUALK && kb >= p.kb_split;
             const int x = (second ? kb - p.kb_split : kb) * C::BK;
-            tc::tma_load_2d(sB, second ? &mB1 : &mB0, fb, x, brow0 + tl.n0);
+            tc::tma_load_2d(sB, second ? &m.b1 : &m.b0, fb, x, brow0 + tl.n0);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -340,15 +356,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ epilogue ------------------------------
     // warp w >= 2: lane quarter q = w % 4 (the tcgen05.ld lane window of the
     // warp), column half = (w - 2) / 4: the two warps of a quarter take
-    // alternate column chunks
+    // alternate 32-column chunks
+    const int ew = warp - 2;
     const int q = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = ew >> 2;
     const int row = 32 * q + lane;
+    uint8_t* stg = epi + ew * C::EPI_BYTES;  // this warp's staging tiles
+    uint64_t* ebar = &sh->ebar[ew];
+    uint32_t ephase = 0;
     int acc = 0;
     uint32_t aphase = 0;
     Tile tl, tn;
     int t = blockIdx.x;
     bool have = get_tile<C>(p, t, nrow_tiles, tl);
+    // DZ: saved a_g / a_u of this warp's first chunk, loaded ahead of the MMA
+    if constexpr (C::EK == E_DZ) {
+      if (have && lane == 0) {
+        tc::mbar_arrive_expect_tx(ebar, 4096);
+        tc::tma_load_2d(stg, &m.i0, ebar, tl.n0 + 32 * half, tl.row0 + 32 * q);
+        tc::tma_load_2d(stg + 2048, &m.i1, ebar, tl.n0 + 32 * half, tl.row0 + 32 * q);
+      }
+    }
     while (have && !aborted) {
       // the next tile's metadata is read while this one is processed
       const bool have_next = get_tile<C>(p, t + gridDim.x, nrow_tiles, tn);
@@ -370,15 +398,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tc_fence_after();
       const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * C::BN;
       const bool has_k = tl.kb1 > tl.kb0;
+      const int yrow = tl.row0 + 32 * q;  // first row of this warp's tiles
 
       if constexpr (C::EK == E_GU) {
         // H = silu(a_g) * a_u with a_g, a_u rounded to bf16 first (the values
-        // a backward pass reads back)
-        const int64_t r = (int64_t)tl.row0 + row;
-        const bool exists = C::ROUTED || row < tl.nvalid;
-        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(p.out0);
-        __nv_bfloat16* AG = reinterpret_cast<__nv_bfloat16*>(p.out1);
-        __nv_bfloat16* AU = reinterpret_cast<__nv_bfloat16*>(p.out2);
+        // a backward pass reads back); 32x32 tiles stored by TMA
 #pragma unroll 1
         for (int c = half; c < C::BN / 64; c += 2) {
           uint32_t g[32], u[32];
@@ -392,13 +416,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             uv[i] = bf16r(__uint_as_float(u[i]));
             hv[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
           }
-          if (exists) {
-            const int64_t off = r * p.ld_out + tl.n0 + 32 * c;
-            store_bf16x32(H + off, hv);
-            if (AG) {
-              store_bf16x32(AG + off, gv);
-              store_bf16x32(AU + off, uv);
+          if (lane == 0) tc::bulk_wait_read0();  // staging free again
+          __syncwarp();
+          stage_write_row(stg, lane, hv);
+          if (p.save) {
+            stage_write_row(stg + 2048, lane, gv);
+            stage_write_row(stg + 4096, lane, uv);
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x = tl.n0 + 32 * c;
+            tc::tma_store_2d(&m.o0, stg, x, yrow);
+            if (p.save) {
+              tc::tma_store_2d(&m.o1, stg + 2048, x, yrow);
+              tc::tma_store_2d(&m.o2, stg + 4096, x, yrow);
             }
+            tc::bulk_commit();
           }
         }
       } else if constexpr (C::EK == E_DOWN) {
@@ -433,31 +467,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else if constexpr (C::EK == E_DZ) {
         // Z = dy W_down^T for this row; SwiGLU backward from the saved
-        // pre-activations; gate-gradient partial <Z, H> over these columns
-        const int64_t r = (int64_t)tl.row0 + row;
-        const bool exists = C::ROUTED || row < tl.nvalid;
-        const bool valid = row < tl.nvalid;
-        const int64_t h = p.ld_out;
-        const __nv_bfloat16* AG = reinterpret_cast<const __nv_bfloat16*>(p.in0);
-        const __nv_bfloat16* AU = reinterpret_cast<const __nv_bfloat16*>(p.in1);
-        __nv_bfloat16* dA = reinterpret_cast<__nv_bfloat16*>(p.out0);
-        __nv_bfloat16* gH = reinterpret_cast<__nv_bfloat16*>(p.out1);
+        // pre-activations (TMA-staged); gate-gradient partial <Z, H> over
+        // these columns; dA and gate*H tiles stored by TMA
+        const int h = p.ld_out;
         float dgp = 0.f;
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t zv[32];
           tc::tmem_ld32(tacc + 32 * c, zv);
           tc::tmem_ld_wait();
-          if (!exists) continue;
-          const int64_t col = tl.n0 + 32 * c;
-          float ag[32], au[32], dag[32], dau[32], gh[32];
-          if (valid) {
-            load_bf16x32(AG + r * h + col, ag);
-            load_bf16x32(AU + r * h + col, au);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) ag[i] = au[i] = 0.f;
+          if (!wait_or_abort(ebar, ephase, sh, p.status, 500)) {
+            aborted = true;
+            break;
           }
+          ephase ^= 1;
+          float ag[32], au[32];
+          stage_read_row(stg, lane, ag);
+          stage_read_row(stg + 2048, lane, au);
+          __syncwarp();
+          // the next input tiles of this warp: next chunk, or the first chunk
+          // of the next tile
+          if (lane == 0) {
+            const bool more = c + 2 < C::BN / 32;
+            if (more || have_next) {
+              const int nx = more ? tl.n0 + 32 * (c + 2) : tn.n0 + 32 * half;
+              const int ny = more ? yrow : tn.row0 + 32 * q;
+              tc::mbar_arrive_expect_tx(ebar, 4096);
+              tc::tma_load_2d(stg, &m.i0, ebar, nx, ny);
+              tc::tma_load_2d(stg + 2048, &m.i1, ebar, nx, ny);
+            }
+          }
+          float dag[32], dau[32], gh[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float z = __uint_as_float(zv[i]);
@@ -470,10 +510,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             dag[i] = dh * au[i] * s * (1.f + ag[i] * (1.f - s));
             gh[i] = gt * hv;
           }
-          store_bf16x32(dA + r * 2 * h + col, dag);
-          store_bf16x32(dA + r * 2 * h + h + col, dau);
-          store_bf16x32(gH + r * h + col, gh);
+          if (lane == 0) tc::bulk_wait_read0();
+          __syncwarp();
+          stage_write_row(stg + 4096, lane, dag);
+          stage_write_row(stg + 6144, lane, dau);
+          stage_write_row(stg + 8192, lane, gh);
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const int x = tl.n0 + 32 * c;
+            tc::tma_store_2d(&m.o0, stg + 4096, x, yrow);
+            tc::tma_store_2d(&m.o0, stg + 6144, h + x, yrow);
+            tc::tma_store_2d(&m.o1, stg + 8192, x, yrow);
+            tc::bulk_commit();
+          }
         }
+        if (aborted) break;
         if (C::ROUTED && pr >= 0) p.dg_part[(int64_t)pr * p.dg_ld + 2 * tl.nt + half] = dgp;
       } else if constexpr (C::EK == E_DX) {
         // input gradient: dx_acc[token] += dA [W_gate | W_up]^T (routed, atomic
@@ -545,6 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tl = tn;
       have = have_next;
     }
+    if constexpr (C::EK == E_GU || C::EK == E_DZ) {
+      if (lane == 0) tc::bulk_wait0();  // this warp's tile stores are complete
+      __syncwarp();
+    }
   }
 
   if (aborted || sh->abort) {
@@ -565,14 +621,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
 int sm_count();
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle,
-// out-of-bounds elements read as zero.
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, out-of-bounds
+// elements read as zero (stores outside are dropped).  Operand tiles use the
+// 128-byte swizzle (box_cols = 64); the epilogue's 32x32 staging tiles use
+// the 64-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
               uint32_t box_rows);
+bool make_map_sw64(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols);
 
 template <class C>
-void launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const Params& p,
-               int64_t max_tiles, const char* name, cudaStream_t s) {
+void launch_tc(const Maps& maps, const Params& p, int64_t max_tiles, const char* name,
+               cudaStream_t s) {
   if (max_tiles <= 0) return;
   static bool attr = false;
   if (!attr) {
@@ -582,7 +641,7 @@ void launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b
   }
   const int sms = sm_count();
   const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-  MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, s>>>(a, b0, b1, p));
+  MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, s>>>(maps, p));
 }
 
 }  // namespace tcg

@@ -22,39 +22,39 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
         cudaStream_t s) {
   const int dm = d.d_model;
   const int h = routed ? d.d_hidden : d.shared_hidden;
-  CUtensorMap a, b0;
+  const int64_t rows = routed ? L.PPcap : d.tokens;
+  Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
   q.n_nt = h / BN;
   q.kb_total = dm / 64;
   q.ld_out = h;
+  if (!make_map_sw64(&mp.o0, at<void>(ws, routed ? L.dA : L.dAs), rows, 2 * h)) return false;
+  if (!make_map_sw64(&mp.o1, at<void>(ws, routed ? L.gH : L.gHs), rows, h)) return false;
+  if (!make_map_sw64(&mp.i0, routed ? p.a_gate : p.as_gate, rows, h)) return false;
+  if (!make_map_sw64(&mp.i1, routed ? p.a_up : p.as_up, rows, h)) return false;
+  mp.o2 = mp.o1;
   if (routed) {
-    if (!make_map(&a, at<void>(ws, L.dys), L.PPcap, dm, 64, 128)) return false;
-    if (!make_map(&b0, p.w_down, (uint64_t)d.experts * h, dm, 64, BN)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.dys), L.PPcap, dm, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.w_down, (uint64_t)d.experts * h, dm, 64, BN)) return false;
+    mp.b1 = mp.b0;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
-    q.in0 = p.a_gate;
-    q.in1 = p.a_up;
-    q.out0 = at<void>(ws, L.dA);
-    q.out1 = at<void>(ws, L.gH);
     q.dg_part = at<float>(ws, L.dg_part);
     q.dg_ld = 2 * h / 64;
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, true>>(a, b0, b0, q, L.MTcap * q.n_nt, "tc_dz", s);
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_dz", s);
   } else {
-    if (!make_map(&a, p.dy, d.tokens, dm, 64, 128)) return false;
-    if (!make_map(&b0, p.ws_down, h, dm, 64, BN)) return false;
+    if (!make_map(&mp.a, p.dy, d.tokens, dm, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.ws_down, h, dm, 64, BN)) return false;
+    mp.b1 = mp.b0;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    q.in0 = p.as_gate;
-    q.in1 = p.as_up;
-    q.out0 = at<void>(ws, L.dAs);
-    q.out1 = at<void>(ws, L.gHs);
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, false>>(a, b0, b0, q, (int64_t)q.n_mt * q.n_nt,
-                                                       "tc_dz", s);
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dz",
+                                                       s);
   }
   return true;
 }
@@ -64,7 +64,7 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
         cudaStream_t s) {
   const int dm = d.d_model;
   const int h = routed ? d.d_hidden : d.shared_hidden;
-  CUtensorMap a, b0, b1;
+  Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
   q.n_nt = dm / BN;
@@ -73,23 +73,23 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   q.ld_out = dm;
   q.facc = at<float>(ws, L.dx_acc);
   if (routed) {
-    if (!make_map(&a, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 128)) return false;
-    if (!make_map(&b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, BN)) return false;
-    if (!make_map(&b1, p.w_up, (uint64_t)d.experts * dm, h, 64, BN)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, BN)) return false;
+    if (!make_map(&mp.b1, p.w_up, (uint64_t)d.experts * dm, h, 64, BN)) return false;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = dm;
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt, "tc_dx", s);
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_dx", s);
   } else {
-    if (!make_map(&a, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 128)) return false;
-    if (!make_map(&b0, p.ws_gate, dm, h, 64, BN)) return false;
-    if (!make_map(&b1, p.ws_up, dm, h, 64, BN)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.ws_gate, dm, h, 64, BN)) return false;
+    if (!make_map(&mp.b1, p.ws_up, dm, h, 64, BN)) return false;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false>>(a, b0, b1, q, (int64_t)q.n_mt * q.n_nt,
-                                                       "tc_dx", s);
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dx",
+                                                       s);
   }
   return true;
 }
@@ -109,7 +109,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   const int dm = d.d_model;
   const int h = routed ? d.d_hidden : d.shared_hidden;
   const int E = routed ? d.experts : 1;
-  CUtensorMap a, b0;
+  Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
   q.M = h;
@@ -123,18 +123,20 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   if (q.splits > 1) zero_fill_f32(out, (int64_t)E * h * dm, s);
   q.facc = out;
   if (routed) {
-    if (!make_map(&a, at<void>(ws, L.gH), L.PPcap, h, 64, 64)) return false;
-    if (!make_map(&b0, at<void>(ws, L.dys), L.PPcap, dm, 64, 64)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.gH), L.PPcap, h, 64, 64)) return false;
+    if (!make_map(&mp.b0, at<void>(ws, L.dys), L.PPcap, dm, 64, 64)) return false;
+    mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(
-        a, b0, b0, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
+        mp, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
   } else {
-    if (!make_map(&a, at<void>(ws, L.gHs), d.tokens, h, 64, 64)) return false;
-    if (!make_map(&b0, p.dy, d.tokens, dm, 64, 64)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.gHs), d.tokens, h, 64, 64)) return false;
+    if (!make_map(&mp.b0, p.dy, d.tokens, dm, 64, 64)) return false;
+    mp.b1 = mp.b0;
     q.rows = d.tokens;
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
-        a, b0, b0, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
+        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
   }
   return true;
 }
@@ -147,7 +149,7 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
   const int dm = d.d_model;
   const int h = routed ? d.d_hidden : d.shared_hidden;
   const int E = routed ? d.experts : 1;
-  CUtensorMap a, b0;
+  Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
   q.M = dm;
@@ -167,18 +169,20 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
   q.facc = g;
   q.facc2 = u;
   if (routed) {
-    if (!make_map(&a, at<void>(ws, L.xs), L.PPcap, dm, 64, 64)) return false;
-    if (!make_map(&b0, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 64)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.xs), L.PPcap, dm, 64, 64)) return false;
+    if (!make_map(&mp.b0, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 64)) return false;
+    mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(
-        a, b0, b0, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
+        mp, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
   } else {
-    if (!make_map(&a, p.x, d.tokens, dm, 64, 64)) return false;
-    if (!make_map(&b0, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 64)) return false;
+    if (!make_map(&mp.a, p.x, d.tokens, dm, 64, 64)) return false;
+    if (!make_map(&mp.b0, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 64)) return false;
+    mp.b1 = mp.b0;
     q.rows = d.tokens;
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
-        a, b0, b0, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
+        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
   }
   return true;
 }

@@ -15,36 +15,39 @@ bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, vo
             bool routed, cudaStream_t s) {
   const int dm = d.d_model;
   const int h = routed ? d.d_hidden : d.shared_hidden;
-  CUtensorMap a, b0, b1;
+  const int64_t rows = routed ? L.PPcap : d.tokens;
+  const bool save = mode == MOE_SAVE_FOR_BWD;
+  Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
   q.n_nt = h / (BN / 2);
   q.kb_total = dm / 64;
   q.ld_out = h;
+  q.save = save ? 1 : 0;
+  void* H = routed ? p.h_buf : p.hs_buf;
+  void* AG = routed ? p.a_gate : p.as_gate;
+  void* AU = routed ? p.a_up : p.as_up;
+  if (!make_map_sw64(&mp.o0, H, rows, h)) return false;
+  mp.o1 = mp.o2 = mp.o0;
+  if (save && (!make_map_sw64(&mp.o1, AG, rows, h) || !make_map_sw64(&mp.o2, AU, rows, h)))
+    return false;
   if (routed) {
-    if (!make_map(&a, at<void>(ws, L.xs), L.PPcap, dm, 64, 128)) return false;
-    if (!make_map(&b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, 64)) return false;
-    if (!make_map(&b1, p.w_up, (uint64_t)d.experts * dm, h, 64, 64)) return false;
+    if (!make_map(&mp.a, at<void>(ws, L.xs), L.PPcap, dm, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, 64)) return false;
+    if (!make_map(&mp.b1, p.w_up, (uint64_t)d.experts * dm, h, 64, 64)) return false;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = dm;
-    q.out0 = p.h_buf;
-    q.out1 = mode == MOE_SAVE_FOR_BWD ? p.a_gate : nullptr;
-    q.out2 = mode == MOE_SAVE_FOR_BWD ? p.a_up : nullptr;
-    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, true>>(a, b0, b1, q, L.MTcap * q.n_nt,
-                                                       "tc_gateup", s);
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_gateup", s);
   } else {
-    if (!make_map(&a, p.x, d.tokens, dm, 64, 128)) return false;
-    if (!make_map(&b0, p.ws_gate, dm, h, 64, 64)) return false;
-    if (!make_map(&b1, p.ws_up, dm, h, 64, 64)) return false;
+    if (!make_map(&mp.a, p.x, d.tokens, dm, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.ws_gate, dm, h, 64, 64)) return false;
+    if (!make_map(&mp.b1, p.ws_up, dm, h, 64, 64)) return false;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    q.out0 = p.hs_buf;
-    q.out1 = mode == MOE_SAVE_FOR_BWD ? p.as_gate : nullptr;
-    q.out2 = mode == MOE_SAVE_FOR_BWD ? p.as_up : nullptr;
-    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, false>>(a, b0, b1, q, (int64_t)q.n_mt * q.n_nt,
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt,
                                                         "tc_gateup", s);
   }
   return true;
@@ -55,7 +58,7 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
           cudaStream_t s) {
   const int dm = d.d_model;
   const int h = routed ? d.d_hidden : d.shared_hidden;
-  CUtensorMap a, b0;
+  Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
   q.n_nt = dm / BN;
@@ -63,22 +66,23 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
   q.ld_out = dm;
   q.facc = p.y_acc;
   if (routed) {
-    if (!make_map(&a, p.h_buf, L.PPcap, h, 64, 128)) return false;
-    if (!make_map(&b0, p.w_down, (uint64_t)d.experts * h, dm, 64, 64)) return false;
+    if (!make_map(&mp.a, p.h_buf, L.PPcap, h, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.w_down, (uint64_t)d.experts * h, dm, 64, 64)) return false;
+    mp.b1 = mp.b0;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
-    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, true>>(a, b0, b0, q, L.MTcap * q.n_nt,
-                                                         "tc_down", s);
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_down", s);
   } else {
-    if (!make_map(&a, p.hs_buf, d.tokens, h, 64, 128)) return false;
-    if (!make_map(&b0, p.ws_down, h, dm, 64, 64)) return false;
+    if (!make_map(&mp.a, p.hs_buf, d.tokens, h, 64, 128)) return false;
+    if (!make_map(&mp.b0, p.ws_down, h, dm, 64, 64)) return false;
+    mp.b1 = mp.b0;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, false>>(a, b0, b0, q, (int64_t)q.n_mt * q.n_nt,
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt,
                                                           "tc_down", s);
   }
   return true;
