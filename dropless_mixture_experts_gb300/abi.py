@@ -61,10 +61,8 @@ _SIGS = {
     "moe_padded_rows": ([_D, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
     "moe_route": ([_D, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_permute": ([_D, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
-    "moe_grouped_ffn_fwd": ([_D, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P],
-                            ctypes.c_int),
-    "moe_combine": ([_D, ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P],
-                    ctypes.c_int),
+    "moe_grouped_ffn_fwd": ([_D, ctypes.c_int] + [_P] * 9 + [_S, _P], ctypes.c_int),
+    "moe_combine": ([_D, ctypes.c_int] + [_P] * 11 + [_S, _P], ctypes.c_int),
     "moe_backward": ([_D] + [_P] * 24 + [_S, _P], ctypes.c_int),
     "moe_read_device_status": ([_P, _S, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "moe_profile_enable": ([ctypes.c_int], ctypes.c_int),
@@ -140,20 +138,20 @@ def moe_permute(dims, topk_idx, counts, offsets, perm, inv_perm, ws, ws_bytes, s
 
 
 def moe_grouped_ffn_fwd(dims, mode, x, gates, w_gate, w_up, w_down, h_buf, a_gate_saved,
-                        a_up_saved, y_acc, ws, ws_bytes, stream, check=True):
+                        a_up_saved, ws, ws_bytes, stream, check=True):
     s = load().moe_grouped_ffn_fwd(ctypes.byref(dims), int(mode), _p(x), _p(gates), _p(w_gate),
                                    _p(w_up), _p(w_down), _p(h_buf), _p(a_gate_saved),
-                                   _p(a_up_saved), _p(y_acc), _p(ws), ws_bytes, _p(stream))
+                                   _p(a_up_saved), _p(ws), ws_bytes, _p(stream))
     if check:
         _check(s, "moe_grouped_ffn_fwd")
     return s
 
 
-def moe_combine(dims, mode, x, ws_gate, ws_up, ws_down, y_acc, y, hs_buf, as_gate_saved,
-                as_up_saved, upstream, loss, ws, ws_bytes, stream, check=True):
+def moe_combine(dims, mode, x, ws_gate, ws_up, ws_down, y, hs_buf, as_gate_saved, as_up_saved,
+                upstream, loss, ws, ws_bytes, stream, check=True):
     s = load().moe_combine(ctypes.byref(dims), int(mode), _p(x), _p(ws_gate), _p(ws_up),
-                           _p(ws_down), _p(y_acc), _p(y), _p(hs_buf), _p(as_gate_saved),
-                           _p(as_up_saved), _p(upstream), _p(loss), _p(ws), ws_bytes, _p(stream))
+                           _p(ws_down), _p(y), _p(hs_buf), _p(as_gate_saved), _p(as_up_saved),
+                           _p(upstream), _p(loss), _p(ws), ws_bytes, _p(stream))
     if check:
         _check(s, "moe_combine")
     return s

@@ -121,13 +121,12 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
 
 moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x, const float* gates,
                                const void* w_gate, const void* w_up, const void* w_down,
-                               void* h_buf, void* a_gate_saved, void* a_up_saved, float* y_acc,
-                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                               void* h_buf, void* a_gate_saved, void* a_up_saved, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
   if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
   if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
   if (dims->tokens > 0) {
-    if (!x || !gates || !w_gate || !w_up || !w_down || !h_buf || !y_acc)
-      return MOE_ERR_INVALID_ARG;
+    if (!x || !gates || !w_gate || !w_up || !w_down || !h_buf) return MOE_ERR_INVALID_ARG;
     if (mode == MOE_SAVE_FOR_BWD && (!a_gate_saved || !a_up_saved)) return MOE_ERR_INVALID_ARG;
   }
   MOE_TRY(shape_supported(dims));
@@ -143,7 +142,6 @@ moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x, co
   p.h_buf = h_buf;
   p.a_gate = a_gate_saved;
   p.a_up = a_up_saved;
-  p.y_acc = y_acc;
   if (dims->dtype == MOE_BF16) {
     if (!tc_grouped_fwd(*dims, L, mode, p, workspace, stream)) return MOE_ERR_CUDA;
   } else {
@@ -153,14 +151,14 @@ moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x, co
 }
 
 moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
-                       const void* ws_up, const void* ws_down, float* y_acc, void* y,
+                       const void* ws_up, const void* ws_down, void* y,
                        void* hs_buf, void* as_gate_saved, void* as_up_saved, const void* upstream,
                        float* loss, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
   if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
   const bool shared = dims->shared_hidden > 0;
   if (dims->tokens > 0) {
-    if (!y_acc || !y) return MOE_ERR_INVALID_ARG;
+    if (!y) return MOE_ERR_INVALID_ARG;
     if (shared && (!x || !ws_gate || !ws_up || !ws_down || !hs_buf)) return MOE_ERR_INVALID_ARG;
     if (shared && mode == MOE_SAVE_FOR_BWD && (!as_gate_saved || !as_up_saved))
       return MOE_ERR_INVALID_ARG;
@@ -178,14 +176,13 @@ moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void
     p.hs_buf = hs_buf;
     p.as_gate = as_gate_saved;
     p.as_up = as_up_saved;
-    p.y_acc = y_acc;
     if (dims->dtype == MOE_BF16) {
       if (!tc_shared_fwd(*dims, L, mode, p, workspace, stream)) return MOE_ERR_CUDA;
     } else {
       simt_shared_fwd(*dims, L, mode, p, workspace, stream);
     }
   }
-  launch_finalize_y(*dims, L, y_acc, y, upstream, loss, workspace, stream);
+  launch_combine(*dims, L, y, upstream, loss, workspace, stream);
   return cuda_status();
 }
 

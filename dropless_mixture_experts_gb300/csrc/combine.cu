@@ -1,35 +1,101 @@
-// Output cast with the train step's value, and the router backward.
+// Combine (unpermute + gate-weighted sum) with the train step's value, and
+// the router backward.
 //
-// Value: L = sum(y * G) for the upstream gradient G (the train step of
-// gpu_moe_h100.json is value_and_grad of the layer), reduced in a fixed
-// order so repeated runs give the same bits.
+// Combine: the grouped down projection leaves, for every pair p = t*k + j,
+// its gate-weighted expert output g_j O_{e_j}(x_t) as one row of the
+// expert-sorted buffer; y[t] = shared(x_t) + sum_j row(pairrow[t*k + j]),
+// summed in slot order (the unpermute_combine piece of kernel_gmm_gpu.json).
+// The value of the train step (gpu_moe_h100.json: value_and_grad) is
+// L = sum(y * G), reduced in a fixed order so repeated runs give the same
+// bits.
 //
 // Router backward: the gates are a softmax over the k selected logits, so
 // the logit gradient of slot j is g_j (dg_j - sum_i g_i dg_i), with dg_j the
 // gradient of the gate (the row-dot <dy_t W_down[e]^T, H_r> produced by the
 // grouped backward), and zero on the experts that were not selected.  Then
-// dW_r = x^T dlogits and dx = dx_acc + dlogits W_r^T.
+// dW_r = x^T dlogits and dx = (shared + sum of the pairs' rows) + dlogits W_r^T.
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
 
+// 16-byte vector of storage elements as floats
 template <typename T>
-__global__ void __launch_bounds__(256) finalize_y_kernel(const float* __restrict__ y_acc, T* y,
-                                                         const T* __restrict__ G, int64_t n,
-                                                         float* loss_part) {
+__device__ __forceinline__ void ld16(const T* p, float (&v)[16 / sizeof(T)]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  } else {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[3] = __uint_as_float(u.w);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void st16(T* p, const float (&v)[16 / sizeof(T)]) {
+  if constexpr (sizeof(T) == 2) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      w[j] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+// y[t] = ys[t] + sum_j osort[pairrow[t*k + j]] (16-byte chunks, one per
+// thread), cast to the storage type, plus the block's share of sum(y * G).
+template <typename T>
+__global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ osort,
+                                                      const int32_t* __restrict__ pairrow,
+                                                      const T* __restrict__ ys, T* __restrict__ y,
+                                                      const T* __restrict__ G, int64_t Tn, int d,
+                                                      int k, float* loss_part) {
+  constexpr int VE = 16 / sizeof(T);
   __shared__ float red[8];
-  float acc = 0.f;
+  const int cpt = d / VE;
+  const int64_t n = Tn * cpt;
+  float lacc = 0.f;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
-    const T v = from_f32<T>(y_acc[i]);
-    y[i] = v;
-    if (G) acc = fmaf(to_f32(v), to_f32(G[i]), acc);
+    const int64_t t = i / cpt;
+    const int c = (int)(i % cpt);
+    float acc[VE];
+    if (ys) {
+      ld16(ys + t * d + c * VE, acc);
+    } else {
+#pragma unroll
+      for (int q = 0; q < VE; ++q) acc[q] = 0.f;
+    }
+    for (int j = 0; j < k; ++j) {
+      float v[VE];
+      ld16(osort + (int64_t)pairrow[t * k + j] * d + c * VE, v);
+#pragma unroll
+      for (int q = 0; q < VE; ++q) acc[q] += v[q];
+    }
+    st16(y + t * d + c * VE, acc);
+    if (G) {
+      float g[VE];
+      ld16(G + t * d + c * VE, g);
+#pragma unroll
+      for (int q = 0; q < VE; ++q) lacc = fmaf(to_f32(from_f32<T>(acc[q])), g[q], lacc);
+    }
   }
   if (!G) return;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  for (int o = 16; o > 0; o >>= 1) lacc += __shfl_xor_sync(0xffffffffu, lacc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lacc;
   __syncthreads();
   if (threadIdx.x == 0) {
     float s = 0.f;
@@ -71,16 +137,15 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
   }
 }
 
-// dx[t, :] = dx_acc[t, :] + sum_j dsel[t, j] W_r[:, e_j]: each thread takes
-// four consecutive input dimensions of one token (W_r^T staged in shared
-// memory), blocks loop over token groups.
+// dx[t] = dxs[t] + sum_j dxsort[pairrow[t*k + j]] + sum_j dsel[t, j] W_r[:, e_j]:
+// each thread takes one 16-byte chunk of one token (W_r^T staged in shared
+// memory); blocks loop over token groups.
 template <typename T>
-__global__ void __launch_bounds__(256) router_dx_kernel(const int32_t* __restrict__ idx,
-                                                        const float* __restrict__ dsel,
-                                                        const T* __restrict__ w_router,
-                                                        const float* __restrict__ dx_acc,
-                                                        T* __restrict__ dx, int64_t Tn, int d,
-                                                        int E, int k) {
+__global__ void __launch_bounds__(256) router_dx_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ dsel, const T* __restrict__ w_router,
+    const T* __restrict__ dxsort, const int32_t* __restrict__ pairrow, const T* __restrict__ dxs,
+    T* __restrict__ dx, int64_t Tn, int d, int E, int k) {
+  constexpr int VE = 16 / sizeof(T);
   extern __shared__ __align__(16) unsigned char s_raw[];
   T* s_wt = reinterpret_cast<T*>(s_raw);  // [E][d]
   for (int i = threadIdx.x; i < E * d; i += blockDim.x) {
@@ -88,26 +153,29 @@ __global__ void __launch_bounds__(256) router_dx_kernel(const int32_t* __restric
     s_wt[e * d + r] = w_router[i];
   }
   __syncthreads();
-  const int cpt = d / 4;                  // float4 chunks per token
-  const int tpb = blockDim.x / cpt;       // tokens per block pass
-  const int c = threadIdx.x % cpt, u = threadIdx.x / cpt;
-  if (u >= tpb) return;
-  for (int64_t t = (int64_t)blockIdx.x * tpb + u; t < Tn; t += (int64_t)gridDim.x * tpb) {
-    float4 v = reinterpret_cast<const float4*>(dx_acc + t * d)[c];
-    for (int j = 0; j < k; ++j) {
-      const int e = __ldg(idx + t * k + j);
-      const float ds = __ldg(dsel + t * k + j);
-      const T* w = s_wt + e * d + 4 * c;
-      v.x = fmaf(ds, to_f32(w[0]), v.x);
-      v.y = fmaf(ds, to_f32(w[1]), v.y);
-      v.z = fmaf(ds, to_f32(w[2]), v.z);
-      v.w = fmaf(ds, to_f32(w[3]), v.w);
+  const int cpt = d / VE;
+  const int64_t n = Tn * cpt;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / cpt;
+    const int c = (int)(i % cpt);
+    float acc[VE];
+    if (dxs) {
+      ld16(dxs + t * d + c * VE, acc);
+    } else {
+#pragma unroll
+      for (int q = 0; q < VE; ++q) acc[q] = 0.f;
     }
-    T* o = dx + t * d + 4 * c;
-    o[0] = from_f32<T>(v.x);
-    o[1] = from_f32<T>(v.y);
-    o[2] = from_f32<T>(v.z);
-    o[3] = from_f32<T>(v.w);
+    for (int j = 0; j < k; ++j) {
+      const int64_t p = t * k + j;
+      float v[VE], w[VE];
+      ld16(dxsort + (int64_t)pairrow[p] * d + c * VE, v);
+      ld16(s_wt + idx[p] * d + c * VE, w);
+      const float ds = dsel[p];
+#pragma unroll
+      for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds, w[q], v[q]);
+    }
+    st16(dx + t * d + c * VE, acc);
   }
 }
 
@@ -170,18 +238,21 @@ __global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __re
   const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (i >= n) return;
   float s = 0.f;
+#pragma unroll 8
   for (int r = 0; r < ranges; ++r) s += part[(int64_t)r * n + i];
   dw[i] = s;
 }
 
 template <typename T>
-void finalize_y_t(const moe_dims& d, const Layout& L, const float* y_acc, void* y,
-                  const void* G, float* loss, void* ws, cudaStream_t s) {
-  const int64_t n = d.tokens * (int64_t)d.d_model;
+void combine_t(const moe_dims& d, const Layout& L, void* y, const void* G, float* loss, void* ws,
+               cudaStream_t s) {
   float* part = at<float>(ws, L.loss_part);
-  MOE_LAUNCH("finalize_y", s,
-             finalize_y_kernel<T><<<kLossBlocks, 256, 0, s>>>(
-                 y_acc, reinterpret_cast<T*>(y), reinterpret_cast<const T*>(G), n, part));
+  const T* ys = d.shared_hidden > 0 ? at<const T>(ws, L.ys) : nullptr;
+  MOE_LAUNCH("combine", s,
+             combine_kernel<T><<<kLossBlocks, 256, 0, s>>>(
+                 at<const T>(ws, L.osort), at<const int32_t>(ws, L.pairrow), ys,
+                 reinterpret_cast<T*>(y), reinterpret_cast<const T*>(G), d.tokens, d.d_model,
+                 d.top_k, part));
   if (G && loss)
     MOE_LAUNCH("loss_reduce", s, loss_reduce_kernel<<<1, 32, 0, s>>>(part, kLossBlocks, loss));
 }
@@ -212,12 +283,14 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
              router_dsel_kernel<<<(unsigned)((d.tokens + 255) / 256), 256, 0, s>>>(
                  p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, dsel));
 
-  const int tpb = 256 / (dm / 4) > 0 ? 256 / (dm / 4) : 1;
-  int64_t bx = (d.tokens + tpb - 1) / tpb;
+  const int VE = 16 / sizeof(T);
+  int64_t bx = (d.tokens * (dm / VE) + 255) / 256;
   if (bx > (int64_t)sms * 4) bx = (int64_t)sms * 4;
+  const T* dxs = d.shared_hidden > 0 ? at<const T>(ws, L.dxs) : nullptr;
   MOE_LAUNCH("router_dx", s,
              router_dx_kernel<T><<<(unsigned)bx, 256, sizeof(T) * E * dm, s>>>(
-                 p.topk_idx, dsel, reinterpret_cast<const T*>(p.w_router), at<float>(ws, L.dx_acc),
+                 p.topk_idx, dsel, reinterpret_cast<const T*>(p.w_router),
+                 at<const T>(ws, L.dxsort), at<const int32_t>(ws, L.pairrow), dxs,
                  reinterpret_cast<T*>(p.dx), d.tokens, dm, E, k));
 
   const int ny = (dm + 255) / 256;
@@ -239,14 +312,14 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
 
 }  // namespace
 
-void launch_finalize_y(const moe_dims& d, const Layout& L, const float* y_acc, void* y,
-                       const void* upstream, float* loss, void* ws, cudaStream_t s) {
+void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* upstream, float* loss,
+                    void* ws, cudaStream_t s) {
   if (d.tokens == 0) {
     if (upstream && loss) zero_fill_f32(loss, 1, s);
     return;
   }
-  if (d.dtype == MOE_BF16) finalize_y_t<__nv_bfloat16>(d, L, y_acc, y, upstream, loss, ws, s);
-  else finalize_y_t<float>(d, L, y_acc, y, upstream, loss, ws, s);
+  if (d.dtype == MOE_BF16) combine_t<__nv_bfloat16>(d, L, y, upstream, loss, ws, s);
+  else combine_t<float>(d, L, y, upstream, loss, ws, s);
 }
 
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
@@ -258,8 +331,7 @@ void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs&
 bool router_backward_supported(const moe_dims& d) {
   const size_t elem = d.dtype == MOE_BF16 ? 2 : 4;
   return (size_t)d.experts * d.d_model * elem <= (size_t)kRouterBwdSmem &&
-         (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem && d.d_model % 4 == 0 &&
-         d.d_model <= 1024;
+         (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem;
 }
 
 }  // namespace moe

@@ -40,8 +40,11 @@ __device__ __forceinline__ void report_error(int* status, int code, int detail) 
 struct Layout {
   size_t status, warp_counts, warp_base, counts, poff, rowpair, tokrow, tiles, ntiles,
       loss_part, logits;
-  size_t xs;  // expert-sorted copy of the token rows [padded rows, d]
-  size_t dg_part, dA, gH, dx_acc, dAs, gHs, dys, dsel, dwr_part;
+  size_t xs;       // expert-sorted copy of the token rows [padded rows, d]
+  size_t pairrow;  // pair -> padded row [P]
+  size_t osort;    // gate-weighted expert output per sorted row [padded rows, d]
+  size_t ys;       // shared-expert output [T, d]
+  size_t dg_part, dA, gH, dxsort, dxs, dAs, gHs, dys, dsel, dwr_part;
   size_t total;
   int64_t P, PPcap, MTcap, NWc;
   int elem;  // bytes per storage element
@@ -82,11 +85,15 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.loss_part = take(sizeof(float) * kLossBlocks);
   L.logits = take(sizeof(float) * T * E);
   L.xs = take((size_t)L.elem * L.PPcap * dm);
+  L.pairrow = take(sizeof(int) * L.P);
+  L.osort = take((size_t)L.elem * L.PPcap * dm);
+  L.ys = take((size_t)L.elem * (hs > 0 ? T : 0) * dm);
   if (mode == MOE_SAVE_FOR_BWD) {
     L.dg_part = take(sizeof(float) * L.P * 2 * (h / 64));
     L.dA = take((size_t)L.elem * L.PPcap * 2 * h);
     L.gH = take((size_t)L.elem * L.PPcap * h);
-    L.dx_acc = take(sizeof(float) * T * dm);
+    L.dxsort = take((size_t)L.elem * L.PPcap * dm);
+    L.dxs = take((size_t)L.elem * (hs > 0 ? T : 0) * dm);
     L.dAs = take((size_t)L.elem * T * 2 * hs);
     L.gHs = take((size_t)L.elem * T * hs);
     L.dys = take((size_t)L.elem * L.PPcap * dm);

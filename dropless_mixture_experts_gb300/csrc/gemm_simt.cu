@@ -6,10 +6,10 @@
 //   LOGITS  logits = x W_r
 //   GU      a_g = x_t W_gate[e], a_u = x_t W_up[e], H = silu(a_g) * a_u
 //           (gather of the token rows fused into the operand load)
-//   DOWN    y_acc[t] += gate * (H W_down[e])   (combine fused in the epilogue)
+//   DOWN    gate * (H W_down[e]) per sorted row (the pair's share of y[t])
 //   DZ      Z = dy_t W_down[e]^T; dgate = <Z, H>; dA_g, dA_u by the SwiGLU
 //           chain rule; gH = gate * H kept for the W_down gradient
-//   DX      dx_acc[t] += dA_g W_gate[e]^T + dA_u W_up[e]^T
+//   DX      dA_g W_gate[e]^T + dA_u W_up[e]^T per sorted row (share of dx[t])
 //   DWD     dW_down[e] = sum_r gH_r^T dy_t           (ragged K = expert rows)
 //   DWGU    dW_gate[e] | dW_up[e] = sum_r x_t^T [dA_g | dA_u]
 // Each kind also runs densely (one expert, identity row map) for the shared
@@ -53,7 +53,8 @@ struct SimtArgs {
   void* gH_out = nullptr;        // DZ  [rows, h]
   float* dg_part = nullptr;      // DZ  [rows, dg_ld]
   int dg_ld = 0;
-  float* acc_out = nullptr;      // LOGITS / DOWN / DX / DWD / DWGU (gate half)
+  void* slot_out = nullptr;      // DOWN / DX: one row per sorted (or dense) row
+  float* acc_out = nullptr;      // LOGITS / DWD / DWGU (gate half)
   float* acc_out2 = nullptr;     // DWGU (up half)
   int ldo = 0;
   int n_ntiles = 1, n_mtiles = 1;
@@ -285,19 +286,16 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
           AU[r * a.ldo + n] = from_f32<T>(u);
         }
       }
-    } else if constexpr (KIND == DOWN) {
+    } else if constexpr (KIND == DOWN || KIND == DX) {
+      // one output row per sorted row (routed: the pair's share of its
+      // token's output, gate applied for DOWN; dense: the shared expert's
+      // row); the combine gathers the shares of a token in a fixed order
       if (m >= nvalid) continue;
-      if constexpr (ROUTED) {
-        const int32_t p = a.rowpair[r];
-        const int64_t t = p / a.top_k;
-        const float gt = a.gates[p];
+      float sc = 1.f;
+      if constexpr (ROUTED && KIND == DOWN) sc = a.gates[a.rowpair[r]];
+      T* out = reinterpret_cast<T*>(a.slot_out);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          atomicAdd(&a.acc_out[t * a.ldo + n0 + tx * 4 + j], gt * acc[i][j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a.acc_out[r * a.ldo + n0 + tx * 4 + j] += acc[i][j];
-      }
+      for (int j = 0; j < 4; ++j) out[r * a.ldo + n0 + tx * 4 + j] = from_f32<T>(sc * acc[i][j]);
     } else if constexpr (KIND == DZ) {
       const bool exists = ROUTED || r < a.rows;
       const bool valid = m < nvalid;
@@ -332,16 +330,6 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, o);
       if (ROUTED && tx == 0 && valid) a.dg_part[(int64_t)a.rowpair[r] * a.dg_ld + ntile] = dgp;
-    } else if constexpr (KIND == DX) {
-      if (m >= nvalid) continue;
-      if constexpr (ROUTED) {
-        const int64_t t = a.rowpair[r] / a.top_k;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) atomicAdd(&a.acc_out[t * a.ldo + n0 + tx * 4 + j], acc[i][j]);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a.acc_out[r * a.ldo + n0 + tx * 4 + j] = acc[i][j];
-      }
     } else {  // DWD / DWGU: plain stores of the expert's gradient tile
       const int64_t om = m0 + m;
       const int64_t eoff = (int64_t)e * a.n_mtiles * BM;  // expert offset in rows
@@ -389,7 +377,6 @@ template <typename T>
 void grouped_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                    cudaStream_t s) {
   const int h = d.d_hidden, dm = d.d_model;
-  zero_fill_f32(p.y_acc, d.tokens * (int64_t)dm, s);
   SimtArgs a;
   a.tiles = at<int4>(ws, L.tiles);
   a.ntiles = at<int>(ws, L.ntiles);
@@ -421,7 +408,7 @@ void grouped_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs
   b.b_estride = (int64_t)h * dm;
   b.N = dm;
   b.K = h;
-  b.acc_out = p.y_acc;
+  b.slot_out = at<void>(ws, L.osort);
   b.ldo = dm;
   b.n_ntiles = dm / BN;
   launch<DOWN, T, true>(b, b.n_ntiles * 2 * L.MTcap, s);
@@ -455,18 +442,15 @@ void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs&
   b.ldb = dm;
   b.N = dm;
   b.K = hs;
-  b.acc_out = p.y_acc;
+  b.slot_out = at<void>(ws, L.ys);
   b.ldo = dm;
   b.n_ntiles = dm / BN;
   launch<DOWN, T, false>(b, b.n_ntiles * mt, s);
-  (void)L;
-  (void)ws;
 }
 
 template <typename T>
 void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, cudaStream_t s) {
   const int h = d.d_hidden, dm = d.d_model, E = d.experts, hs = d.shared_hidden;
-  float* dx_acc = at<float>(ws, L.dx_acc);
   void* dA = at<void>(ws, L.dA);
   void* gH = at<void>(ws, L.gH);
   const int64_t mt_dense = (d.tokens + BM - 1) / BM;
@@ -501,7 +485,7 @@ void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws
     x.N = dm;
     x.K = 2 * hs;
     x.h = hs;
-    x.acc_out = dx_acc;
+    x.slot_out = at<void>(ws, L.dxs);
     x.ldo = dm;
     x.n_ntiles = dm / BN;
     launch<DX, T, false>(x, x.n_ntiles * mt_dense, s);
@@ -529,8 +513,6 @@ void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws
     g.n_mtiles = dm / BM;
     g.n_ntiles = 2 * hs / BN;
     launch<DWGU, T, false>(g, (int64_t)g.n_ntiles * g.n_mtiles, s);
-  } else {
-    zero_fill_f32(dx_acc, d.tokens * (int64_t)dm, s);
   }
 
   // routed experts
@@ -570,7 +552,7 @@ void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws
   x.N = dm;
   x.K = 2 * h;
   x.h = h;
-  x.acc_out = dx_acc;
+  x.slot_out = at<void>(ws, L.dxsort);
   x.ldo = dm;
   x.n_ntiles = dm / BN;
   launch<DX, T, true>(x, x.n_ntiles * 2 * L.MTcap, s);

@@ -89,7 +89,9 @@ struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per-warp staging: 2 KB per bf16 32x32 tile
-  static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048 : EK == E_DZ ? 5 * 2048 : 0;
+  static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048
+                                   : EK == E_DZ ? 5 * 2048
+                                   : (EK == E_DOWN || EK == E_DX) ? 2048 : 0;
   static constexpr int FIXED = kEpiWarps * EPI_BYTES + 1024 + 256;
   static constexpr int STAGES = (kSmemLimit - FIXED) / STAGE_BYTES > 8
                                     ? 8
@@ -383,10 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // per-row metadata of this tile (routed kinds): issued before the wait
       int32_t pr = -1;
       float gt = 1.f;
-      if constexpr (C::ROUTED && (C::EK == E_DOWN || C::EK == E_DZ || C::EK == E_DX)) {
+      if constexpr (C::ROUTED && (C::EK == E_DOWN || C::EK == E_DZ)) {
         if (row < tl.nvalid) {
           pr = p.rowpair[(int64_t)tl.row0 + row];
-          if constexpr (C::EK != E_DX) gt = p.gates[pr];
+          gt = p.gates[pr];
         } else {
           gt = 0.f;
         }
@@ -435,34 +437,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::bulk_commit();
           }
         }
-      } else if constexpr (C::EK == E_DOWN) {
-        // gate-weighted combine: y_acc[token] += gate * (H W_down) (routed,
-        // atomic float4 adds) or y_acc[token] += H_s Ws_down (shared expert)
-        const bool valid = row < tl.nvalid;
-        const int64_t r = (int64_t)tl.row0 + row;
-        const int64_t t_out = C::ROUTED ? (valid ? pr / p.top_k : 0) : r;
-        float* dst = p.facc + t_out * p.ld_out + tl.n0;
+      } else if constexpr (C::EK == E_DOWN || C::EK == E_DX) {
+        // one output row per sorted row, stored by TMA as bf16 tiles:
+        //   DOWN: gate * (H W_down), the pair's share of its token's output
+        //         (the shared expert: its whole output row)
+        //   DX:   [dA_g | dA_u] [W_gate | W_up]^T, the pair's share of dx
+        // the combine gathers the k shares of a token in a fixed order
+        const float sc = C::EK == E_DOWN ? gt : 1.f;
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t v[32];
           tc::tmem_ld32(tacc + 32 * c, v);
           tc::tmem_ld_wait();
-          if (!valid) continue;
+          float o[32];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 f = make_float4(gt * __uint_as_float(v[4 * i]), gt * __uint_as_float(v[4 * i + 1]),
-                                         gt * __uint_as_float(v[4 * i + 2]), gt * __uint_as_float(v[4 * i + 3]));
-            float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * i);
-            if constexpr (C::ROUTED) {
-              atomicAdd(a, f);
-            } else {
-              float4 o = *a;
-              o.x += f.x;
-              o.y += f.y;
-              o.z += f.z;
-              o.w += f.w;
-              *a = o;
-            }
+          for (int i = 0; i < 32; ++i) o[i] = sc * __uint_as_float(v[i]);
+          if (lane == 0) tc::bulk_wait_read0();
+          __syncwarp();
+          stage_write_row(stg, lane, o);
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_store_2d(&m.o0, stg, tl.n0 + 32 * c, yrow);
+            tc::bulk_commit();
           }
         }
       } else if constexpr (C::EK == E_DZ) {
@@ -527,28 +524,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (aborted) break;
         if (C::ROUTED && pr >= 0) p.dg_part[(int64_t)pr * p.dg_ld + 2 * tl.nt + half] = dgp;
-      } else if constexpr (C::EK == E_DX) {
-        // input gradient: dx_acc[token] += dA [W_gate | W_up]^T (routed, atomic
-        // float4 adds) or dx_acc = dA_s [Ws_gate | Ws_up]^T (shared, first writer)
-        const bool valid = row < tl.nvalid;
-        const int64_t r = (int64_t)tl.row0 + row;
-        const int64_t t_out = C::ROUTED ? (valid ? pr / p.top_k : 0) : r;
-        float* dst = p.facc + t_out * p.ld_out + tl.n0;
-#pragma unroll 1
-        for (int c = half; c < C::BN / 32; c += 2) {
-          uint32_t v[32];
-          tc::tmem_ld32(tacc + 32 * c, v);
-          tc::tmem_ld_wait();
-          if (!valid) continue;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                         __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-            float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * i);
-            if constexpr (C::ROUTED) atomicAdd(a, f);
-            else *a = f;
-          }
-        }
       } else {  // E_DW: one expert's gradient tile (rows m0.., columns n0..)
         const int om = tl.m0 + row;
         float* base = p.facc;
@@ -597,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tl = tn;
       have = have_next;
     }
-    if constexpr (C::EK == E_GU || C::EK == E_DZ) {
+    if constexpr (C::EPI_BYTES > 0) {
       if (lane == 0) tc::bulk_wait0();  // this warp's tile stores are complete
       __syncwarp();
     }

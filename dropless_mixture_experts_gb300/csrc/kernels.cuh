@@ -54,7 +54,6 @@ struct LayerPtrs {
   void* hs_buf = nullptr;
   void* as_gate = nullptr;
   void* as_up = nullptr;
-  float* y_acc = nullptr;
   float* logits = nullptr;
   // backward outputs
   void* dx = nullptr;
@@ -87,8 +86,10 @@ bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
 int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials per row)
 
 // combine / loss / router backward (combine.cu)
-void launch_finalize_y(const moe_dims& d, const Layout& L, const float* y_acc, void* y,
-                       const void* upstream, float* loss, void* ws, cudaStream_t s);
+// y = shared + sum of each token's pair rows (from the workspace), and the
+// value sum(y * upstream) when upstream is given
+void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* upstream, float* loss,
+                    void* ws, cudaStream_t s);
 bool router_backward_supported(const moe_dims& d);
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                             int dg_ld, void* ws, cudaStream_t s);

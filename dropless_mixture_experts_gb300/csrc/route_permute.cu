@@ -251,7 +251,7 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
                                            int k, int64_t chunk, int* hist, const int* base_e,
                                            const int* off_e, const int* poff_e, int32_t* perm,
                                            int32_t* inv_perm, int32_t* rowpair, int32_t* tokrow,
-                                           int* status) {
+                                           int32_t* pairrow, int* status) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   for (int r = 0; r < kPermRounds; ++r) {
@@ -279,6 +279,7 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
       inv_perm[p] = pos;
       rowpair[ppos] = (int32_t)p;
       tokrow[ppos] = (int32_t)(p / k);
+      pairrow[p] = ppos;
     }
   }
 }
@@ -293,7 +294,7 @@ __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restric
   __syncwarp();
   if (chunk >= NW) return;
   walk_chunk<false>(idx, P, E, k, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, nullptr,
-                    nullptr, nullptr, status);
+                    nullptr, nullptr, nullptr, status);
   for (int e = lane; e < E; e += 32) warp_counts[chunk * E + e] = hist[w][e];
 }
 
@@ -379,7 +380,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
     const int32_t* __restrict__ idx, int64_t P, int E, int k, int64_t NW,
     const int* __restrict__ warp_base, const int32_t* __restrict__ offsets,
     const int* __restrict__ poff, int32_t* perm, int32_t* inv_perm, int32_t* rowpair,
-    int32_t* tokrow, int* status) {
+    int32_t* tokrow, int32_t* pairrow, int* status) {
   __shared__ int hist[8][kMaxExperts];
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
   const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
   if (chunk >= NW) return;
   walk_chunk<true>(idx, P, E, k, chunk, hist[w], warp_base + chunk * E, s_off, s_poff, perm,
-                   inv_perm, rowpair, tokrow, status);
+                   inv_perm, rowpair, tokrow, pairrow, status);
 }
 
 void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
@@ -425,7 +426,7 @@ void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int3
     MOE_LAUNCH("perm_scatter", s,
                perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, k, NW, warp_base, offsets,
                                                           poff, perm, inv_perm, rowpair, tokrow,
-                                                          status));
+                                                          at<int32_t>(ws, L.pairrow), status));
 }
 
 }  // namespace moe

@@ -71,7 +71,9 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   q.kb_total = 2 * h / 64;
   q.kb_split = h / 64;
   q.ld_out = dm;
-  q.facc = at<float>(ws, L.dx_acc);
+  if (!make_map_sw64(&mp.o0, at<void>(ws, routed ? L.dxsort : L.dxs),
+                     routed ? L.PPcap : d.tokens, dm))
+    return false;
   if (routed) {
     if (!make_map(&mp.a, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 128)) return false;
     if (!make_map(&mp.b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, BN)) return false;
@@ -209,12 +211,7 @@ bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
                        cudaStream_t s) {
   launch_gather_rows(p.dy, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1,
                      at<void>(ws, L.dys), L.PPcap, (int64_t)d.d_model * 2, s);
-  // the shared expert's DX is the first writer of dx_acc; without it, zero it
-  if (d.shared_hidden > 0) {
-    if (!backward_one(d, L, p, ws, false, s)) return false;
-  } else {
-    zero_fill_f32(at<float>(ws, L.dx_acc), d.tokens * (int64_t)d.d_model, s);
-  }
+  if (d.shared_hidden > 0 && !backward_one(d, L, p, ws, false, s)) return false;
   return backward_one(d, L, p, ws, true, s);
 }
 

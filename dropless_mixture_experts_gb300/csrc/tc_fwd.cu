@@ -64,7 +64,9 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
   q.n_nt = dm / BN;
   q.kb_total = h / 64;
   q.ld_out = dm;
-  q.facc = p.y_acc;
+  if (!make_map_sw64(&mp.o0, at<void>(ws, routed ? L.osort : L.ys), routed ? L.PPcap : d.tokens,
+                     dm))
+    return false;
   if (routed) {
     if (!make_map(&mp.a, p.h_buf, L.PPcap, h, 64, 128)) return false;
     if (!make_map(&mp.b0, p.w_down, (uint64_t)d.experts * h, dm, 64, 64)) return false;
@@ -107,7 +109,6 @@ bool down_any(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, 
 
 bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                     cudaStream_t s) {
-  zero_fill_f32(p.y_acc, d.tokens * (int64_t)d.d_model, s);
   launch_gather_rows(p.x, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1, at<void>(ws, L.xs),
                      L.PPcap, (int64_t)d.d_model * 2, s);
   if (!gateup_any(d, L, mode, p, ws, true, s)) return false;

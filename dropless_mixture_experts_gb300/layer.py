@@ -49,7 +49,6 @@ class MoELayer:
         self.h_buf = torch.empty(self.PP, h, dtype=td, device=dev)
         self.a_gate = torch.empty(self.PP, h, dtype=td, device=dev) if train else None
         self.a_up = torch.empty(self.PP, h, dtype=td, device=dev) if train else None
-        self.y_acc = torch.empty(T, d, dtype=f32, device=dev)
         self.y = torch.empty(T, d, dtype=td, device=dev)
         self.hs_buf = torch.empty(T, hs, dtype=td, device=dev) if hs else None
         self.as_gate = torch.empty(T, hs, dtype=td, device=dev) if (hs and train) else None
@@ -83,12 +82,12 @@ class MoELayer:
     def grouped_ffn_fwd(self, x, p, mode):
         abi.moe_grouped_ffn_fwd(self.dims, mode, _ptr(x), _ptr(self.gates), _ptr(p["w_gate"]),
                                 _ptr(p["w_up"]), _ptr(p["w_down"]), _ptr(self.h_buf),
-                                _ptr(self.a_gate), _ptr(self.a_up), _ptr(self.y_acc),
-                                self.ws_ptr, self.ws_bytes, self._stream())
+                                _ptr(self.a_gate), _ptr(self.a_up), self.ws_ptr, self.ws_bytes,
+                                self._stream())
 
     def combine(self, x, p, mode, upstream=None):
         abi.moe_combine(self.dims, mode, _ptr(x), _ptr(p.get("ws_gate")), _ptr(p.get("ws_up")),
-                        _ptr(p.get("ws_down")), _ptr(self.y_acc), _ptr(self.y),
+                        _ptr(p.get("ws_down")), _ptr(self.y),
                         _ptr(self.hs_buf), _ptr(self.as_gate if mode else None),
                         _ptr(self.as_up if mode else None), _ptr(upstream),
                         _ptr(self.loss if upstream is not None else None),

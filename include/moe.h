@@ -26,7 +26,7 @@
  *   [E, d, h]; w_down [E, h, d]; ws_gate, ws_up [d, hs]; ws_down [hs, d].
  * - dtype MOE_F32: every activation, weight and gradient is float32.
  *   dtype MOE_BF16: x, y, dy, dx, weights and the saved activations are
- *   bfloat16; logits, gates, y_acc and every weight gradient are float32.
+ *   bfloat16; logits, gates and every weight gradient are float32.
  *   Accumulation is float32 in both.
  * - The library allocates nothing.  Scratch is the caller's workspace of
  *   moe_workspace_bytes() bytes (256-byte aligned).  The SAME workspace must
@@ -122,35 +122,36 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Grouped SwiGLU experts over the expert-sorted rows, gather of the token
- * rows fused into the first GEMM's operand load and the gate-weighted
- * combine fused into the down projection:
- *   h_buf[r]   = silu(x_t W_gate[e]) * (x_t W_up[e])   [padded_rows, h] (dtype)
- *   y_acc[t]  += gates[t, j] * (h_buf[r] W_down[e])    [T, d] f32, ZEROED HERE
+/* Grouped SwiGLU experts over the expert-sorted rows (the token rows are
+ * first gathered into expert-sorted order inside the workspace):
+ *   h_buf[r] = silu(x_t W_gate[e]) * (x_t W_up[e])     [padded_rows, h] (dtype)
+ *   then, for the down projection, gates[t, j] * (h_buf[r] W_down[e]) is
+ *   kept in the workspace as pair (t, j)'s share of y[t], for moe_combine.
  * In MOE_SAVE_FOR_BWD mode a_gate_saved / a_up_saved [padded_rows, h]
  * (dtype) receive x_t W_gate[e] and x_t W_up[e]; in MOE_FWD_ONLY they may
  * be NULL.  gates is moe_route's output. */
 moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x,
                                const float* gates, const void* w_gate, const void* w_up,
                                const void* w_down, void* h_buf, void* a_gate_saved,
-                               void* a_up_saved, float* y_acc, void* workspace,
-                               size_t workspace_bytes, cudaStream_t stream);
+                               void* a_up_saved, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
 
-/* Combine: y = y_acc + shared(x) cast to dtype, where shared(x) =
- * (silu(x Ws_gate) * (x Ws_up)) Ws_down when hs > 0 (its weights are
- * ignored and may be NULL when hs == 0).
+/* Combine: y[t] = shared(x_t) + sum over slots j of the pairs' shares left
+ * by moe_grouped_ffn_fwd, summed in slot order and cast to dtype, where
+ * shared(x) = (silu(x Ws_gate) * (x Ws_up)) Ws_down when hs > 0 (its
+ * weights are ignored and may be NULL when hs == 0).
+ *   y [T, d] (dtype) out
  *   hs_buf [T, hs] (dtype) scratch for the shared hidden activations
  *                          (NULL when hs == 0)
  *   as_gate_saved, as_up_saved [T, hs] (dtype): saved shared
  *                          pre-activations in MOE_SAVE_FOR_BWD, else NULL
  *   upstream [T, d] (dtype), nullable; when given, *loss (f32, device)
  *   receives sum(y * upstream), the train step's value, reduced in a fixed
- *   order.  y_acc is consumed (it may be overwritten). */
+ *   order.  The result is bit-identical from run to run. */
 moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
-                       const void* ws_up, const void* ws_down, float* y_acc, void* y,
-                       void* hs_buf, void* as_gate_saved, void* as_up_saved,
-                       const void* upstream, float* loss, void* workspace,
-                       size_t workspace_bytes, cudaStream_t stream);
+                       const void* ws_up, const void* ws_down, void* y, void* hs_buf,
+                       void* as_gate_saved, void* as_up_saved, const void* upstream, float* loss,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Backward of the train step for L = sum(y * dy):
  *   inputs : dy [T, d], x, all weights, topk_idx, gates, and the saved

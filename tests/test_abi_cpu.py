@@ -86,9 +86,15 @@ def test_null_pointers_rejected(lib):
     need = abi.moe_workspace_bytes(d, abi.MOE_FWD_ONLY)
     assert abi.moe_route(d, None, None, None, None, 256, 256, 0x1000, need, None, check=False) == abi.MOE_ERR_INVALID_ARG
     assert abi.moe_route(d, 256, 256, None, None, None, 256, 0x1000, need, None, check=False) == abi.MOE_ERR_INVALID_ARG
-    assert abi.moe_grouped_ffn_fwd(d, 1, 256, 256, 256, 256, 256, 256, None, None, 256, 0x1000, need, None,
+    # train mode without the saved pre-activation buffers
+    assert abi.moe_grouped_ffn_fwd(d, 1, 256, 256, 256, 256, 256, 256, None, None, 0x1000, need, None,
                                    check=False) == abi.MOE_ERR_INVALID_ARG
-    assert abi.moe_grouped_ffn_fwd(d, 5, 256, 256, 256, 256, 256, 256, 256, 256, 256, 0x1000, need, None,
+    # unknown mode
+    assert abi.moe_grouped_ffn_fwd(d, 5, 256, 256, 256, 256, 256, 256, 256, 256, 0x1000, need, None,
                                    check=False) == abi.MOE_ERR_INVALID_ARG
-    assert abi.moe_combine(d, 0, None, None, None, None, None, 256, None, None, None, None, None, 0x1000,
+    # no output buffer
+    assert abi.moe_combine(d, 0, None, None, None, None, None, None, None, None, None, None, 0x1000,
+                           need, None, check=False) == abi.MOE_ERR_INVALID_ARG
+    # a value without a place to put it
+    assert abi.moe_combine(d, 0, None, None, None, None, 256, None, None, None, 256, None, 0x1000,
                            need, None, check=False) == abi.MOE_ERR_INVALID_ARG
