@@ -1,0 +1,33 @@
+"""Parity at the full sizes of the benchmark workloads (the E8/k2 layer at
+4k, 32k and 128k tokens in float32 and bfloat16, the fine-grained E64/k4
+layer and the E64/k8 decoder block with a shared expert at 16k and 128k
+tokens), in the launch configuration the bench times, against the float64
+oracle run on the same device routing.  The oracle is run in full (a few
+seconds to ~15 s of host BLAS per configuration)."""
+
+import numpy as np
+import pytest
+
+from dropless_mixture_experts_gb300.synthetic import CONFIGS
+from gpu_util import TOL, check_routing_bit_exact, compare_layer, run_layer
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+NAMES = list(CONFIGS)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_full_size_train_step(name):
+    cfg = CONFIGS[name]
+    inp, layer, dev, res = run_layer(cfg, train=True)
+    assert res["status"] == 0
+    check_routing_bit_exact(res, cfg)
+    errs = compare_layer(inp, res, cfg, train=True)
+    bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
+    assert not bad, (name, errs)
+    # routing sanity against the pages' layer runs: no empty expert, the
+    # busiest expert near 1/E of the pairs
+    counts = res["counts"]
+    assert counts.sum() == cfg.tokens * cfg.top_k
+    assert np.count_nonzero(counts == 0) == 0
+    assert counts.max() / counts.sum() < 2.0 / cfg.experts
