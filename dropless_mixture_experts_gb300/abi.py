@@ -28,7 +28,7 @@ MOE_SAVE_FOR_BWD = 1
 EXPORTS = (
     "moe_status_string", "moe_workspace_bytes", "moe_padded_rows", "moe_route",
     "moe_permute", "moe_grouped_ffn_fwd", "moe_combine", "moe_backward",
-    "moe_read_device_status", "moe_profile_enable", "moe_profile_read",
+    "moe_read_device_status", "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc",
 )
 
 
@@ -66,6 +66,7 @@ _SIGS = {
     "moe_backward": ([_D] + [_P] * 24 + [_S, _P], ctypes.c_int),
     "moe_read_device_status": ([_P, _S, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "moe_profile_enable": ([ctypes.c_int], ctypes.c_int),
+    "moe_permute_noalloc": ([_D, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_profile_read": ([ctypes.c_int, ctypes.c_char_p, ctypes.POINTER(ctypes.c_int64),
                           ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)],
                          ctypes.c_int),
@@ -193,3 +194,14 @@ def moe_profile_read(max_entries: int = 64):
         nm = names.raw[64 * i:64 * (i + 1)].split(b"\0", 1)[0].decode()
         out[nm] = (int(launches[i]), float(ms[i]))
     return out
+
+
+def moe_permute_noalloc(dims, topk_idx, counts, offsets, perm, inv_perm, stream, check=True):
+    """The counting sort of moe_permute without a workspace, for callers that
+    cannot allocate device memory (its scratch is a fixed array inside the
+    library; see include/moe.h for the size limit and the sharing rules)."""
+    s = load().moe_permute_noalloc(ctypes.byref(dims), _p(topk_idx), _p(counts), _p(offsets),
+                                   _p(perm), _p(inv_perm), _p(stream))
+    if check:
+        _check(s, "moe_permute_noalloc")
+    return s

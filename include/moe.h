@@ -180,6 +180,32 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x,
 moe_status moe_read_device_status(void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream, int32_t* detail);
 
+/* moe_permute_noalloc: the same counting sort as moe_permute (counts,
+ * offsets, perm, inv_perm; identical results) for callers that cannot
+ * allocate device memory -- code running where cudaMalloc is unavailable or
+ * not allowed, such as an engine plugin handed no workspace, a serving loop
+ * whose memory was reserved up front by another allocator, or a caller that
+ * must not risk the implicit device synchronisation of an allocation.  The
+ * benchmark pages have no counterpart to this entry; it exists for them.
+ *
+ * It takes no workspace.  Its scratch is one array of 4 MiB + 1.5 KiB inside
+ * the library (a __device__ variable: every GPU that loads the library keeps
+ * it until the process exits).  It is sized for (T*k / 512, rounded up) x E
+ * <= 524288, e.g. up to 2^20 pairs with 256 experts or 2^22 pairs with 64;
+ * larger problems return MOE_ERR_UNSUPPORTED before anything is launched.
+ * It does not write the expert-padded tables the grouped calls read, so it
+ * is not a substitute for moe_permute inside a layer invocation.
+ *
+ * All calls share the array and each call leaves its contents behind;
+ * calls that overlap on the GPU (other streams, unsynchronised threads)
+ * race.  The first call on a device looks up the array's device address,
+ * which loads the library's device code there; make that first call before
+ * any stream capture.  Expert indices outside [0, E) are skipped (their
+ * outputs stay unwritten). */
+moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
+                               int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                               cudaStream_t stream);
+
 /* Kernel timing records, a measurement aid outside the layer itself: while
  * enabled, every kernel the library launches is bracketed by two CUDA events
  * recorded on its stream.  Enabling or disabling discards earlier records.
