@@ -86,6 +86,11 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
   if (T == 0) return MOE_OK;
   const float* logits = logits_in;
   if (!logits_in) {
+    if (tc_router_supported(*dims)) {
+      if (!tc_router(*dims, L, x, w_router, logits_out, topk_idx, gates, workspace, stream))
+        return MOE_ERR_CUDA;
+      return cuda_status();
+    }
     if (router_fused_supported(*dims)) {
       // router GEMM, selection and softmax in one pass over x
       launch_router_fused(*dims, x, w_router, logits_out, topk_idx, gates, stream);

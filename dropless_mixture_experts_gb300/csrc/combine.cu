@@ -78,11 +78,21 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ osor
 #pragma unroll
       for (int q = 0; q < VE; ++q) acc[q] = 0.f;
     }
-    for (int j = 0; j < k; ++j) {
-      float v[VE];
-      ld16(osort + (int64_t)pairrow[t * k + j] * d + c * VE, v);
+    // the token's rows in groups of four: all row indices, then all row
+    // loads, then the adds (in slot order)
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      int rows[4];
 #pragma unroll
-      for (int q = 0; q < VE; ++q) acc[q] += v[q];
+      for (int j = 0; j < 4; ++j) rows[j] = j0 + j < k ? pairrow[t * k + j0 + j] : -1;
+      float v[4][VE];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (rows[j] >= 0) ld16(osort + (int64_t)rows[j] * d + c * VE, v[j]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (rows[j] >= 0)
+#pragma unroll
+          for (int q = 0; q < VE; ++q) acc[q] += v[j][q];
     }
     st16(y + t * d + c * VE, acc);
     if (G) {
@@ -166,14 +176,29 @@ __global__ void __launch_bounds__(256) router_dx_kernel(
 #pragma unroll
       for (int q = 0; q < VE; ++q) acc[q] = 0.f;
     }
-    for (int j = 0; j < k; ++j) {
-      const int64_t p = t * k + j;
-      float v[VE], w[VE];
-      ld16(dxsort + (int64_t)pairrow[p] * d + c * VE, v);
-      ld16(s_wt + idx[p] * d + c * VE, w);
-      const float ds = dsel[p];
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      int rows[4], ex[4];
+      float ds[4];
 #pragma unroll
-      for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds, w[q], v[q]);
+      for (int j = 0; j < 4; ++j) {
+        const int64_t p = t * k + j0 + j;
+        const bool ok = j0 + j < k;
+        rows[j] = ok ? pairrow[p] : -1;
+        ex[j] = ok ? idx[p] : 0;
+        ds[j] = ok ? dsel[p] : 0.f;
+      }
+      float v[4][VE];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (rows[j] >= 0) ld16(dxsort + (int64_t)rows[j] * d + c * VE, v[j]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (rows[j] < 0) continue;
+        float w[VE];
+        ld16(s_wt + ex[j] * d + c * VE, w);
+#pragma unroll
+        for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds[j], w[q], v[j][q]);
+      }
     }
     st16(dx + t * d + c * VE, acc);
   }
@@ -285,7 +310,7 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
 
   const int VE = 16 / sizeof(T);
   int64_t bx = (d.tokens * (dm / VE) + 255) / 256;
-  if (bx > (int64_t)sms * 4) bx = (int64_t)sms * 4;
+  if (bx > (int64_t)sms * 16) bx = (int64_t)sms * 16;
   const T* dxs = d.shared_hidden > 0 ? at<const T>(ws, L.dxs) : nullptr;
   MOE_LAUNCH("router_dx", s,
              router_dx_kernel<T><<<(unsigned)bx, 256, sizeof(T) * E * dm, s>>>(

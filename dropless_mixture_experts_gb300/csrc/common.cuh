@@ -15,7 +15,7 @@ constexpr int kPermRounds = 16;   // 32-pair rounds per warp chunk in the counti
 constexpr int kPermChunk = 32 * kPermRounds;
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
-constexpr int kLossBlocks = 512;  // fixed partial count of the loss reduction
+constexpr int kLossBlocks = 2048;  // fixed partial count of the loss reduction
 constexpr int kRouterBwdRanges = 608;  // max token ranges of the router-weight gradient partials
 constexpr int kRouterBwdSmem = 200 * 1024;  // router backward: W_r^T + dW_r partial in shared memory
 
@@ -29,6 +29,23 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 
 __device__ __forceinline__ float sigmoidf_(float a) { return 1.0f / (1.0f + expf(-a)); }
+
+// ---- routing selection ------------------------------------------------------
+// The total order of the top-k selection: larger logit first, the lower
+// expert index on equal logits (+0.0 == -0.0).
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// exp(sel - top) for float32 logits: the gap is exact in double; its float
+// head and tail give expf(head) * (1 + tail) to float accuracy even for
+// large gaps, where a float32 difference alone would lose the tail.
+__device__ __forceinline__ float gate_exp(float sel, float top) {
+  const double diff = (double)sel - (double)top;
+  const float head = (float)diff;
+  const float tail = (float)(diff - (double)head);
+  return expf(head) * (1.f + tail);
+}
 
 // ---- device status word ---------------------------------------------------
 // status[0] = first error code (moe_status), status[1] = detail word.

@@ -34,7 +34,7 @@ namespace tcg {
 
 enum AKind { A_K_TMA = 0, A_MN_TMA = 2 };   // A tile K-major (rows x 64 K) or MN-major
 enum BKind { B_MN_TMA = 0, B_K_TMA = 1 };   // B tile MN-major (64 K rows x BN) or K-major
-enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4 };
+enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4, E_ROUTER = 5 };
 
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -68,6 +68,8 @@ struct Params {
   // epilogue
   const float* gates = nullptr;
   int save = 0;                     // GU: also store a_g, a_u
+  void* out0 = nullptr;             // router: top-k indices [T, k]
+  void* out1 = nullptr;             // router: gates [T, k]
   float* facc = nullptr;
   float* facc2 = nullptr;
   float* dg_part = nullptr;         // DZ: [pairs, dg_ld], entry 2*column-tile + half
@@ -524,6 +526,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (aborted) break;
         if (C::ROUTED && pr >= 0) p.dg_part[(int64_t)pr * p.dg_ld + 2 * tl.nt + half] = dgp;
+      } else if constexpr (C::EK == E_ROUTER) {
+        // router: one token per thread of the first four epilogue warps; its
+        // E logits come straight from tensor memory, the top-k selection and
+        // the softmax of the selected logits run in registers
+        if (half == 0) {
+          float lg[C::BN];
+#pragma unroll
+          for (int c = 0; c < C::BN / 32; ++c) {
+            uint32_t v[32];
+            tc::tmem_ld32(tacc + 32 * c, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) lg[32 * c + i] = __uint_as_float(v[i]);
+          }
+          const int E = p.N, k = p.top_k;
+          if (row < tl.nvalid) {
+            const int64_t t = (int64_t)tl.row0 + row;
+            if (p.facc) {
+              float4* lo = reinterpret_cast<float4*>(p.facc + t * E);
+#pragma unroll
+              for (int e4 = 0; e4 < C::BN / 4; ++e4)
+                if (4 * e4 < E) lo[e4] = make_float4(lg[4 * e4], lg[4 * e4 + 1], lg[4 * e4 + 2], lg[4 * e4 + 3]);
+            }
+            int32_t* idx = reinterpret_cast<int32_t*>(p.out0) + t * k;
+            float* gates = reinterpret_cast<float*>(p.out1) + t * k;
+            unsigned long long taken = 0ull;
+            float top = 0.f, sum = 0.f;
+            for (int r = 0; r < k; ++r) {
+              float bv = 0.f;
+              int bi = -1;
+#pragma unroll
+              for (int e = 0; e < C::BN; ++e) {
+                if (e < E && !((taken >> e) & 1ull) && (bi < 0 || better(lg[e], e, bv, bi))) {
+                  bv = lg[e];
+                  bi = e;
+                }
+              }
+              taken |= 1ull << bi;
+              if (r == 0) top = bv;
+              const float z = gate_exp(bv, top);
+              sum += z;
+              idx[r] = bi;
+              gates[r] = z;
+            }
+            for (int r = 0; r < k; ++r) gates[r] = gates[r] / sum;
+          }
+        }
       } else {  // E_DW: one expert's gradient tile (rows m0.., columns n0..)
         const int om = tl.m0 + row;
         float* base = p.facc;

@@ -84,6 +84,10 @@ bool tc_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs
 bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                        cudaStream_t s);
 int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials per row)
+// router GEMM + top-k + softmax on the tensor cores (bf16, E a multiple of 8, <= 64)
+bool tc_router_supported(const moe_dims& d);
+bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_router,
+               float* logits_out, int32_t* idx, float* gates, void* ws, cudaStream_t s);
 
 // combine / loss / router backward (combine.cu)
 // y = shared + sum of each token's pair rows (from the workspace), and the

@@ -15,22 +15,6 @@
 
 namespace moe {
 
-// The total order of the selection: larger logit first, the lower expert
-// index on equal logits (+0.0 == -0.0).
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// exp(sel - top) for float32 logits: the gap is exact in double; its float
-// head and tail give expf(head) * (1 + tail) to float accuracy even for
-// large gaps, where a float32 difference alone would lose the tail.
-__device__ __forceinline__ float gate_exp(float sel, float top) {
-  const double diff = (double)sel - (double)top;
-  const float head = (float)diff;
-  const float tail = (float)(diff - (double)head);
-  return expf(head) * (1.f + tail);
-}
-
 constexpr int kMaxPerLane = kMaxExperts / 32;
 
 // ---------------------------------------------------------------------------

@@ -107,6 +107,34 @@ bool down_any(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, 
 
 }  // namespace
 
+bool tc_router_supported(const moe_dims& d) {
+  return d.dtype == MOE_BF16 && d.experts % 8 == 0 && d.experts <= 64 && d.d_model % 64 == 0;
+}
+
+// logits = x W_r on the tensor cores (x: K-major rows; W_r [d, E]: MN-major
+// tile of 64 columns, the columns past E read as zero), top-k and softmax in
+// the epilogue
+bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_router,
+               float* logits_out, int32_t* idx, float* gates, void* ws, cudaStream_t s) {
+  Maps mp;
+  Params q;
+  q.status = at<int>(ws, L.status);
+  if (!make_map(&mp.a, x, d.tokens, d.d_model, 64, 128)) return false;
+  if (!make_map(&mp.b0, w_router, d.d_model, d.experts, 64, 64)) return false;
+  mp.b1 = mp.b0;
+  q.rows = d.tokens;
+  q.n_mt = (int)((d.tokens + 127) / 128);
+  q.n_nt = 1;
+  q.kb_total = d.d_model / 64;
+  q.N = d.experts;
+  q.top_k = d.top_k;
+  q.out0 = idx;
+  q.out1 = gates;
+  q.facc = logits_out;
+  launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_ROUTER, 64, false>>(mp, q, q.n_mt, "tc_router", s);
+  return true;
+}
+
 bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                     cudaStream_t s) {
   launch_gather_rows(p.x, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1, at<void>(ws, L.xs),
