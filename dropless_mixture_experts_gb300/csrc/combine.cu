@@ -130,7 +130,9 @@ __global__ void __launch_bounds__(32) loss_reduce_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restrict__ gates,
                                                           const float* __restrict__ dg_part,
                                                           int dg_ld, int dg_n, int64_t Tn, int k,
-                                                          float* __restrict__ dsel) {
+                                                          float* __restrict__ dsel,
+                                                          const int32_t* __restrict__ idx, int E,
+                                                          __nv_bfloat16* __restrict__ dl) {
   const int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
   if (t >= Tn) return;
   float sgd = 0.f;
@@ -141,28 +143,38 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
     dsel[p] = dg;
     sgd = fmaf(gates[p], dg, sgd);
   }
+  if (dl) {  // dense bf16 row of the logit gradient (zero off the selection)
+    for (int e = 0; e < E; ++e) dl[t * E + e] = __float2bfloat16_rn(0.f);
+  }
   for (int j = 0; j < k; ++j) {
     const int64_t p = t * k + j;
-    dsel[p] = gates[p] * (dsel[p] - sgd);
+    const float v = gates[p] * (dsel[p] - sgd);
+    dsel[p] = v;
+    if (dl) dl[t * E + idx[p]] = __float2bfloat16_rn(v);
+  }
+}
+
+// W_r^T [E, d] from W_r [d, E] (storage type unchanged)
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_router_kernel(const T* __restrict__ w, int d,
+                                                               int E, T* __restrict__ wt) {
+  const int64_t n = (int64_t)d * E;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / E, e = i % E;
+    wt[e * d + r] = w[i];
   }
 }
 
 // dx[t] = dxs[t] + sum_j dxsort[pairrow[t*k + j]] + sum_j dsel[t, j] W_r[:, e_j]:
-// each thread takes one 16-byte chunk of one token (W_r^T staged in shared
-// memory); blocks loop over token groups.
+// each thread takes one 16-byte chunk of one token; W_r^T [E, d] rows are
+// read through the cache.
 template <typename T>
 __global__ void __launch_bounds__(256) router_dx_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ dsel, const T* __restrict__ w_router,
+    const int32_t* __restrict__ idx, const float* __restrict__ dsel, const T* __restrict__ s_wt,
     const T* __restrict__ dxsort, const int32_t* __restrict__ pairrow, const T* __restrict__ dxs,
     T* __restrict__ dx, int64_t Tn, int d, int E, int k) {
   constexpr int VE = 16 / sizeof(T);
-  extern __shared__ __align__(16) unsigned char s_raw[];
-  T* s_wt = reinterpret_cast<T*>(s_raw);  // [E][d]
-  for (int i = threadIdx.x; i < E * d; i += blockDim.x) {
-    const int r = i / E, e = i % E;  // coalesced read of W_r[r][e]
-    s_wt[e * d + r] = w_router[i];
-  }
-  __syncthreads();
   const int cpt = d / VE;
   const int64_t n = Tn * cpt;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
@@ -294,8 +306,6 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
   float* part = at<float>(ws, L.dwr_part);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaFuncSetAttribute(router_dx_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         kRouterBwdSmem);
     cudaFuncSetAttribute(router_dw_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          kRouterBwdSmem);
     attr_set = true;
@@ -303,21 +313,31 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
   int dev = 0, sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool tc_dw = tc_router_dw_supported(d);
 
   MOE_LAUNCH("router_dsel", s,
              router_dsel_kernel<<<(unsigned)((d.tokens + 255) / 256), 256, 0, s>>>(
-                 p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, dsel));
+                 p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, dsel, p.topk_idx, E,
+                 tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr));
+
+  T* wt = at<T>(ws, L.wrt);
+  MOE_LAUNCH("router_transpose", s,
+             transpose_router_kernel<T><<<(unsigned)((dm * E + 255) / 256), 256, 0, s>>>(
+                 reinterpret_cast<const T*>(p.w_router), dm, E, wt));
 
   const int VE = 16 / sizeof(T);
   int64_t bx = (d.tokens * (dm / VE) + 255) / 256;
   if (bx > (int64_t)sms * 16) bx = (int64_t)sms * 16;
   const T* dxs = d.shared_hidden > 0 ? at<const T>(ws, L.dxs) : nullptr;
   MOE_LAUNCH("router_dx", s,
-             router_dx_kernel<T><<<(unsigned)bx, 256, sizeof(T) * E * dm, s>>>(
-                 p.topk_idx, dsel, reinterpret_cast<const T*>(p.w_router),
-                 at<const T>(ws, L.dxsort), at<const int32_t>(ws, L.pairrow), dxs,
-                 reinterpret_cast<T*>(p.dx), d.tokens, dm, E, k));
+             router_dx_kernel<T><<<(unsigned)bx, 256, 0, s>>>(
+                 p.topk_idx, dsel, wt, at<const T>(ws, L.dxsort), at<const int32_t>(ws, L.pairrow),
+                 dxs, reinterpret_cast<T*>(p.dx), d.tokens, dm, E, k));
 
+  if (tc_dw) {
+    tc_router_dw(d, L, p, ws, s);
+    return;
+  }
   const int ny = (dm + 255) / 256;
   int64_t ranges = (int64_t)sms * 4 / ny;
   const int64_t by_tokens = (d.tokens + 63) / 64;
@@ -354,9 +374,8 @@ void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs&
 }
 
 bool router_backward_supported(const moe_dims& d) {
-  const size_t elem = d.dtype == MOE_BF16 ? 2 : 4;
-  return (size_t)d.experts * d.d_model * elem <= (size_t)kRouterBwdSmem &&
-         (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem;
+  // the CUDA-core dW_r path keeps one [E][256] f32 accumulator per block
+  return tc_router_dw_supported(d) || (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem;
 }
 
 }  // namespace moe

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -62,6 +64,9 @@ struct Layout {
   size_t osort;    // gate-weighted expert output per sorted row [padded rows, d]
   size_t ys;       // shared-expert output [T, d]
   size_t dg_part, dA, gH, dxsort, dxs, dAs, gHs, dys, dsel, dwr_part;
+  size_t dl;      // dense router-logit gradient [T, E] (bf16 path)
+  size_t wrt;     // W_r^T [E, d]
+  size_t dwpart;  // per-split partials of the weight-gradient GEMMs
   size_t total;
   int64_t P, PPcap, MTcap, NWc;
   int elem;  // bytes per storage element
@@ -73,6 +78,17 @@ inline int64_t padded_rows(const moe_dims& d) {
   int64_t P = d.tokens * (int64_t)d.top_k;
   int64_t cap = P + (int64_t)d.experts * (kRowPad - 1);
   return (cap + kRowPad - 1) / kRowPad * kRowPad;
+}
+
+// Column tile of a grouped GEMM with n output columns.
+inline int pick_bn(int n) { return n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 64; }
+
+// Most K splits a weight-gradient GEMM with `tiles` output tiles may use
+// (a power of two; 1 when the tiles alone fill any GPU of <= 256 SMs).
+inline int split_bound(int64_t tiles) {
+  int s = 1;
+  while (s < 16 && tiles * s < 256) s *= 2;
+  return s;
 }
 
 inline Layout make_layout(const moe_dims& d, int mode) {
@@ -116,6 +132,23 @@ inline Layout make_layout(const moe_dims& d, int mode) {
     L.dys = take((size_t)L.elem * L.PPcap * dm);
     L.dsel = take(sizeof(float) * T * d.top_k);
     L.dwr_part = take(sizeof(float) * kRouterBwdRanges * dm * E);
+    L.dl = take((size_t)2 * T * E);
+    L.wrt = take((size_t)L.elem * E * dm);
+    // partials of the split weight-gradient GEMMs (one launch at a time)
+    auto need = [&](int64_t experts, int64_t M, int64_t N, int bn, bool always) -> int64_t {
+      const int64_t ldp = (N + bn - 1) / bn * bn;
+      const int64_t tiles = experts * ((M + 127) / 128) * (ldp / bn);
+      const int s = split_bound(tiles);
+      return (s > 1 || always) ? s * experts * M * ldp : 0;
+    };
+    int64_t pf = need(E, h, dm, pick_bn((int)dm), false);
+    pf = std::max(pf, need(E, dm, 2 * h, pick_bn((int)h), false));
+    if (hs > 0) {
+      pf = std::max(pf, need(1, hs, dm, pick_bn((int)dm), false));
+      pf = std::max(pf, need(1, dm, 2 * hs, pick_bn((int)hs), false));
+    }
+    pf = std::max(pf, need(1, dm, E, 64, true));
+    L.dwpart = take(sizeof(float) * pf);
   }
   L.total = o;
   return L;

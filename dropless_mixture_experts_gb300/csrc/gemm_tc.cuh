@@ -59,7 +59,9 @@ struct Params {
   int64_t rows = 0;                 // dense kinds: number of tokens
   int n_nt = 1;                     // column tiles
   int n_mt = 1;                     // DW kinds: output row tiles; dense row kinds: row tiles
-  int splits = 1;                   // DW kinds: K splits (atomic adds when > 1)
+  int splits = 1;                   // DW kinds: K splits
+  float* part = nullptr;            // DW kinds: per-split partials [splits][E][M][ldp]
+  int ldp = 0;                      //   (reduced in a fixed order by a second kernel)
   int experts = 1;
   int kb_total = 0;                 // row kinds: K / 64
   int kb_split = 0;                 // dual-K B (dx): K blocks taken from the first map
@@ -110,6 +112,7 @@ struct Cfg {
 
 struct Tile {
   int e, row0, nvalid, m0, n0, kb0, kb1, nt;
+  int s;  // DW kinds: K split
 };
 
 // Tile t of the persistent schedule.  META=false skips the per-tile
@@ -146,6 +149,7 @@ __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles,
     const int mt = r % p.n_mt;
     r /= p.n_mt;
     const int s = r % p.splits;
+    tl.s = s;
     tl.e = r / p.splits;
     if (tl.e >= p.experts) return false;
     int64_t ne;
@@ -584,7 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ncol = tl.n0 - p.hsplit;
           }
         }
-        float* dst = base + ((int64_t)tl.e * p.M + om) * ld + ncol;
+        // one split's partial (reduced later in split order) or the final
+        // gradient; every element of the tile is written once (zeros when
+        // this split's K range is empty)
+        float* dst = p.part ? p.part + ((int64_t)tl.s * p.experts * p.M + (int64_t)tl.e * p.M + om) *
+                                           p.ldp + tl.n0
+                            : base + ((int64_t)tl.e * p.M + om) * ld + ncol;
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t v[32];
@@ -600,12 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 8; ++i) {
               const float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                            __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-              float4* a = reinterpret_cast<float4*>(dst + 32 * c + 4 * i);
-              if (p.splits > 1) {
-                if (has_k) atomicAdd(a, f);
-              } else {
-                *a = f;
-              }
+              *reinterpret_cast<float4*>(dst + 32 * c + 4 * i) = f;
             }
           }
         }

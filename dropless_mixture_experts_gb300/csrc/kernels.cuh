@@ -19,6 +19,9 @@ void prof_end(cudaStream_t s);
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s);
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s);
 void clear_status(int* status, cudaStream_t s);
+// fixed-order sum of the K-split partials of a weight-gradient GEMM
+void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, int hsplit,
+                         float* out0, float* out1, cudaStream_t s);
 // expert-sorted copy of token rows: out[r] = src[tokrow[r]] for r < *used
 void launch_gather_rows(const void* src, const int32_t* tokrow, const int* used, void* out,
                         int64_t cap_rows, int64_t row_bytes, cudaStream_t s);
@@ -84,6 +87,10 @@ bool tc_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs
 bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                        cudaStream_t s);
 int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials per row)
+// router weight gradient x^T dlogits on the tensor cores (bf16, E a multiple of 8, <= 64)
+bool tc_router_dw_supported(const moe_dims& d);
+bool tc_router_dw(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                  cudaStream_t s);
 // router GEMM + top-k + softmax on the tensor cores (bf16, E a multiple of 8, <= 64)
 bool tc_router_supported(const moe_dims& d);
 bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_router,

@@ -65,6 +65,39 @@ void launch_gather_rows(const void* src, const int32_t* tokrow, const int* used,
                  (int)(row_bytes / 16), cap_rows));
 }
 
+// out[em][n] = sum over s of part[s][em][n] in split order (n < N, row
+// stride ldp in the partials); with hsplit > 0 columns n >= hsplit go to
+// out1 (the up half of a gate|up gradient).
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ part, int S,
+                                                           int64_t EM, int ldp, int N, int hsplit,
+                                                           float* out0, float* out1) {
+  const int64_t n_all = EM * N;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_all; i += stride) {
+    const int64_t em = i / N;
+    const int n = (int)(i % N);
+    float v = 0.f;
+    for (int s = 0; s < S; ++s) v += part[((int64_t)s * EM + em) * ldp + n];
+    if (hsplit > 0) {
+      if (n < hsplit) out0[em * hsplit + n] = v;
+      else out1[em * hsplit + (n - hsplit)] = v;
+    } else {
+      out0[em * N + n] = v;
+    }
+  }
+}
+
+void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, int hsplit,
+                         float* out0, float* out1, cudaStream_t s) {
+  const int64_t n = EM * N;
+  if (n <= 0) return;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  MOE_LAUNCH("split_reduce", s,
+             split_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(part, S, EM, ldp, N, hsplit, out0,
+                                                                  out1));
+}
+
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s) { zero_fill<int32_t>(p, n, s); }
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s) { zero_fill<float>(p, n, s); }
 void clear_status(int* status, cudaStream_t s) { zero_fill<int>(status, 2, s); }

@@ -3,19 +3,19 @@
 // the forward's sorted copy of x is reused.  Then
 //   DZ  Z = dy_t W_down[e]^T with the SwiGLU backward and the gate-gradient
 //       partials in the epilogue
-//   DX  dx_acc[t] += [dA_g | dA_u] [W_gate[e] | W_up[e]]^T
+//   DX  [dA_g | dA_u] [W_gate[e] | W_up[e]]^T per sorted row
 //   DW  dW_down[e] = gH^T dy_t and dW_gate[e] | dW_up[e] = x_t^T [dA_g | dA_u]
 //       with K the expert's own rows (ragged), split over CTAs when the
-//       output has too few tiles to fill the GPU
-// and the dense (shared-expert) instances of each.
+//       output has too few tiles to fill the GPU; splits write partials that
+//       a second kernel sums in split order (deterministic)
+// and the dense (shared-expert) instances of each, plus the router weight
+// gradient dW_r = x^T dlogits as a dense DW GEMM.
 #include "gemm_tc.cuh"
 
 namespace moe {
 using namespace tcg;
 
 namespace {
-
-int pick_bn(int n) { return n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 64; }
 
 template <int BN>
 bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
@@ -96,11 +96,27 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   return true;
 }
 
+// K splits of a weight-gradient GEMM: enough CTAs to fill the GPU, at least
+// four 64-row K blocks per split, never beyond the workspace's bound
 int splits_for(int64_t tiles, int64_t kblocks_per_tile) {
   const int sms = sm_count();
+  const int cap = split_bound(tiles);
   int s = 1;
-  while (tiles * s < sms && s < 16 && kblocks_per_tile / (s * 2) >= 4) s *= 2;
+  while (tiles * s < sms && s < cap && kblocks_per_tile / (s * 2) >= 4) s *= 2;
   return s;
+}
+
+// Shared tail of the DW launches: partials when split, the fixed-order
+// reduction afterwards.
+void set_splits(Params& q, const Layout& L, void* ws, int64_t kblocks, bool always_partials) {
+  q.splits = splits_for((int64_t)q.experts * q.n_mt * q.n_nt, kblocks);
+  if (q.splits > 1 || always_partials) q.part = at<float>(ws, L.dwpart);
+}
+
+void reduce_splits(const Params& q, float* out0, float* out1, cudaStream_t s) {
+  if (!q.part) return;
+  launch_split_reduce(q.part, q.splits, (int64_t)q.experts * q.M, q.ldp, q.N, q.hsplit, out0,
+                      out1, s);
 }
 
 // dW_down[e] = sum over the expert's rows of gH_r^T dy_r: A = gH (MN-major:
@@ -120,9 +136,9 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   q.n_nt = dm / BN;
   q.experts = E;
   const int64_t rows_per_e = routed ? L.P / E : d.tokens;
-  q.splits = splits_for((int64_t)E * q.n_mt * q.n_nt, (rows_per_e + 63) / 64);
+  set_splits(q, L, ws, (rows_per_e + 63) / 64, false);
+  q.ldp = dm;
   float* out = routed ? p.dw_down : p.dws_down;
-  if (q.splits > 1) zero_fill_f32(out, (int64_t)E * h * dm, s);
   q.facc = out;
   if (routed) {
     if (!make_map(&mp.a, at<void>(ws, L.gH), L.PPcap, h, 64, 64)) return false;
@@ -140,6 +156,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
         mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
   }
+  reduce_splits(q, out, nullptr, s);
   return true;
 }
 
@@ -161,13 +178,10 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
   q.n_nt = 2 * h / BN;
   q.experts = E;
   const int64_t rows_per_e = routed ? L.P / E : d.tokens;
-  q.splits = splits_for((int64_t)E * q.n_mt * q.n_nt, (rows_per_e + 63) / 64);
+  set_splits(q, L, ws, (rows_per_e + 63) / 64, false);
+  q.ldp = 2 * h;
   float* g = routed ? p.dw_gate : p.dws_gate;
   float* u = routed ? p.dw_up : p.dws_up;
-  if (q.splits > 1) {
-    zero_fill_f32(g, (int64_t)E * dm * h, s);
-    zero_fill_f32(u, (int64_t)E * dm * h, s);
-  }
   q.facc = g;
   q.facc2 = u;
   if (routed) {
@@ -186,6 +200,7 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
         mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
   }
+  reduce_splits(q, g, u, s);
   return true;
 }
 
@@ -213,6 +228,37 @@ bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
                      at<void>(ws, L.dys), L.PPcap, (int64_t)d.d_model * 2, s);
   if (d.shared_hidden > 0 && !backward_one(d, L, p, ws, false, s)) return false;
   return backward_one(d, L, p, ws, true, s);
+}
+
+bool tc_router_dw_supported(const moe_dims& d) {
+  return d.dtype == MOE_BF16 && d.experts % 8 == 0 && d.experts <= 64;
+}
+
+// dW_r [d, E] = x^T dl with dl the dense bf16 router-logit gradient [T, E]
+// (zero off the selected experts): a dense DW GEMM, M = d, N = E (one
+// 64-column tile, the columns past E read as zero), K = the tokens, split
+// over CTAs into partials reduced in split order.
+bool tc_router_dw(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                  cudaStream_t s) {
+  Maps mp;
+  Params q;
+  q.status = at<int>(ws, L.status);
+  q.M = d.d_model;
+  q.N = d.experts;
+  q.n_mt = (d.d_model + 127) / 128;
+  q.n_nt = 1;
+  q.experts = 1;
+  q.rows = d.tokens;
+  set_splits(q, L, ws, (d.tokens + 63) / 64, true);
+  q.ldp = 64;
+  q.facc = p.dw_router;
+  if (!make_map(&mp.a, p.x, d.tokens, d.d_model, 64, 64)) return false;
+  if (!make_map(&mp.b0, at<void>(ws, L.dl), d.tokens, d.experts, 64, 64)) return false;
+  mp.b1 = mp.b0;
+  launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, 64, false>>(mp, q, (int64_t)q.n_mt * q.splits,
+                                                       "tc_router_dw", s);
+  reduce_splits(q, p.dw_router, nullptr, s);
+  return true;
 }
 
 }  // namespace moe
