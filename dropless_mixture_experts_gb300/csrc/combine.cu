@@ -143,8 +143,10 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
     dsel[p] = dg;
     sgd = fmaf(gates[p], dg, sgd);
   }
-  if (dl) {  // dense bf16 row of the logit gradient (zero off the selection)
-    for (int e = 0; e < E; ++e) dl[t * E + e] = __float2bfloat16_rn(0.f);
+  if (dl) {  // dense bf16 row of the logit gradient (zero off the selection);
+             // E is a multiple of 8 on this path: 16-byte stores
+    uint4* row = reinterpret_cast<uint4*>(dl + t * E);
+    for (int e8 = 0; e8 < E / 8; ++e8) row[e8] = make_uint4(0u, 0u, 0u, 0u);
   }
   for (int j = 0; j < k; ++j) {
     const int64_t p = t * k + j;

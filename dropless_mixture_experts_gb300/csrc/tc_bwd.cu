@@ -96,13 +96,14 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   return true;
 }
 
-// K splits of a weight-gradient GEMM: enough CTAs to fill the GPU, at least
-// four 64-row K blocks per split, never beyond the workspace's bound
+// K splits of a weight-gradient GEMM: split only while the tiles fill less
+// than half of the GPU (a split costs a partial write and a reduction), at
+// least four 64-row K blocks per split, never beyond the workspace's bound
 int splits_for(int64_t tiles, int64_t kblocks_per_tile) {
   const int sms = sm_count();
   const int cap = split_bound(tiles);
   int s = 1;
-  while (tiles * s < sms && s < cap && kblocks_per_tile / (s * 2) >= 4) s *= 2;
+  while (tiles * s * 2 <= sms && s < cap && kblocks_per_tile / (s * 2) >= 4) s *= 2;
   return s;
 }
 
