@@ -1,5 +1,7 @@
 // The C ABI (include/moe.h): argument validation and the launch sequence of
 // each call.  Nothing here computes; every step runs in the kernels.
+#include <initializer_list>
+
 #include "kernels.cuh"
 
 using namespace moe;
@@ -28,6 +30,14 @@ moe_status check_ws(const moe_dims* d, int mode, const void* ws, size_t bytes) {
   if (reinterpret_cast<uintptr_t>(ws) % 256) return MOE_ERR_WORKSPACE;
   if (bytes < make_layout(*d, mode).total) return MOE_ERR_WORKSPACE;
   return MOE_OK;
+}
+
+// Row data (activations, weights, their gradients) moves in 16-byte vectors
+// and bulk copies: every such array must start on a 16-byte boundary.
+bool aligned16(std::initializer_list<const void*> ptrs) {
+  for (const void* q : ptrs)
+    if (reinterpret_cast<uintptr_t>(q) % 16) return false;
+  return true;
 }
 
 moe_status cuda_status() {
@@ -78,6 +88,7 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
     if (!topk_idx || !gates) return MOE_ERR_INVALID_ARG;
     if (!logits_in && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
   }
+  if (!aligned16({x, w_router})) return MOE_ERR_INVALID_ARG;
   MOE_TRY(shape_supported(dims));
   MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
   const Layout L = make_layout(*dims, MOE_FWD_ONLY);
@@ -134,6 +145,8 @@ moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x, co
     if (!x || !gates || !w_gate || !w_up || !w_down || !h_buf) return MOE_ERR_INVALID_ARG;
     if (mode == MOE_SAVE_FOR_BWD && (!a_gate_saved || !a_up_saved)) return MOE_ERR_INVALID_ARG;
   }
+  if (!aligned16({x, w_gate, w_up, w_down, h_buf, a_gate_saved, a_up_saved}))
+    return MOE_ERR_INVALID_ARG;
   MOE_TRY(shape_supported(dims));
   MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
   if (dims->tokens == 0) return MOE_OK;
@@ -169,6 +182,8 @@ moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void
       return MOE_ERR_INVALID_ARG;
   }
   if (upstream && !loss) return MOE_ERR_INVALID_ARG;
+  if (!aligned16({x, ws_gate, ws_up, ws_down, y, hs_buf, as_gate_saved, as_up_saved, upstream}))
+    return MOE_ERR_INVALID_ARG;
   MOE_TRY(shape_supported(dims));
   MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
   const Layout L = make_layout(*dims, MOE_FWD_ONLY);
@@ -210,6 +225,10 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
       return MOE_ERR_INVALID_ARG;
     if (shared && (!as_gate_saved || !as_up_saved)) return MOE_ERR_INVALID_ARG;
   }
+  if (!aligned16({dy, x, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, a_gate_saved,
+                  a_up_saved, as_gate_saved, as_up_saved, dx, dw_router, dw_gate, dw_up, dw_down,
+                  dws_gate, dws_up, dws_down}))
+    return MOE_ERR_INVALID_ARG;
   MOE_TRY(shape_supported(dims));
   // the router backward keeps W_r^T and one dW_r column block in shared memory
   if (!router_backward_supported(*dims)) return MOE_ERR_UNSUPPORTED;

@@ -57,7 +57,7 @@ __device__ __forceinline__ void report_error(int* status, int code, int detail) 
 
 // ---- workspace layout -------------------------------------------------------
 struct Layout {
-  size_t status, warp_counts, warp_base, counts, poff, rowpair, tokrow, tiles, ntiles,
+  size_t status, warp_counts, warp_base, counts, poff, rowpair, tiles, ntiles,
       loss_part, logits;
   size_t xs;       // expert-sorted copy of the token rows [padded rows, d]
   size_t pairrow;  // pair -> padded row [P]
@@ -112,7 +112,6 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.counts = take(sizeof(int) * E);
   L.poff = take(sizeof(int) * (E + 1));
   L.rowpair = take(sizeof(int) * L.PPcap);
-  L.tokrow = take(sizeof(int) * L.PPcap);
   L.tiles = take(sizeof(int4) * L.MTcap);
   L.ntiles = take(sizeof(int) * 4);
   L.loss_part = take(sizeof(float) * kLossBlocks);

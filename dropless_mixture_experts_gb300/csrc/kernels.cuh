@@ -22,9 +22,6 @@ void clear_status(int* status, cudaStream_t s);
 // fixed-order sum of the K-split partials of a weight-gradient GEMM
 void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, int hsplit,
                          float* out0, float* out1, cudaStream_t s);
-// expert-sorted copy of token rows: out[r] = src[tokrow[r]] for r < *used
-void launch_gather_rows(const void* src, const int32_t* tokrow, const int* used, void* out,
-                        int64_t cap_rows, int64_t row_bytes, cudaStream_t s);
 
 // routing and permutation (route_permute.cu)
 void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
@@ -96,11 +93,20 @@ bool tc_router_supported(const moe_dims& d);
 bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_router,
                float* logits_out, int32_t* idx, float* gates, void* ws, cudaStream_t s);
 
-// combine / loss / router backward (combine.cu)
+// row streams (stream.cu)
+// expert-sorted copy of token rows: out[pairrow[t*k + j]] = src[t], padding
+// rows zeroed
+void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, void* out, void* ws,
+                         cudaStream_t s);
 // y = shared + sum of each token's pair rows (from the workspace), and the
 // value sum(y * upstream) when upstream is given
 void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* upstream, float* loss,
                     void* ws, cudaStream_t s);
+// dx = shared + sum of each token's pair rows + dlogits W_r^T (wt = W_r^T [E, d])
+void launch_router_dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, const float* dsel,
+                      const void* wt, void* ws, cudaStream_t s);
+
+// router backward (router_bwd.cu)
 bool router_backward_supported(const moe_dims& d);
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                             int dg_ld, void* ws, cudaStream_t s);

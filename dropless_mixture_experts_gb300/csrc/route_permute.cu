@@ -234,8 +234,8 @@ template <bool SCATTER>
 __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int64_t P, int E,
                                            int k, int64_t chunk, int* hist, const int* base_e,
                                            const int* off_e, const int* poff_e, int32_t* perm,
-                                           int32_t* inv_perm, int32_t* rowpair, int32_t* tokrow,
-                                           int32_t* pairrow, int* status) {
+                                           int32_t* inv_perm, int32_t* rowpair, int32_t* pairrow,
+                                           int* status) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   for (int r = 0; r < kPermRounds; ++r) {
@@ -262,7 +262,6 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
       perm[pos] = (int32_t)p;
       inv_perm[p] = pos;
       rowpair[ppos] = (int32_t)p;
-      tokrow[ppos] = (int32_t)(p / k);
       pairrow[p] = ppos;
     }
   }
@@ -278,7 +277,7 @@ __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restric
   __syncwarp();
   if (chunk >= NW) return;
   walk_chunk<false>(idx, P, E, k, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, nullptr,
-                    nullptr, nullptr, nullptr, status);
+                    nullptr, nullptr, status);
   for (int e = lane; e < E; e += 32) warp_counts[chunk * E + e] = hist[w][e];
 }
 
@@ -317,7 +316,7 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restri
                                                              int E, int32_t* counts_out,
                                                              int32_t* offsets_out, int* poff,
                                                              int4* tiles, int* ntiles,
-                                                             int32_t* rowpair, int32_t* tokrow) {
+                                                             int32_t* rowpair) {
   __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1], s_toff[kMaxExperts + 1];
   const int tid = threadIdx.x;
   if (tid == 0) {
@@ -351,12 +350,9 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restri
       const int valid = min(kRowPad, c - j * kRowPad);
       tiles[s_toff[e] + j] = make_int4(e, s_poff[e] + j * kRowPad, valid, 0);
     }
-    // padding rows of this expert's last tile: no pair, token 0
+    // padding rows of this expert's last tile: no pair
     const int pad_lo = s_poff[e] + c, pad_hi = s_poff[e + 1];
-    for (int r = pad_lo + tid; r < pad_hi; r += blockDim.x) {
-      rowpair[r] = -1;
-      tokrow[r] = 0;
-    }
+    for (int r = pad_lo + tid; r < pad_hi; r += blockDim.x) rowpair[r] = -1;
   }
 }
 
@@ -364,7 +360,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
     const int32_t* __restrict__ idx, int64_t P, int E, int k, int64_t NW,
     const int* __restrict__ warp_base, const int32_t* __restrict__ offsets,
     const int* __restrict__ poff, int32_t* perm, int32_t* inv_perm, int32_t* rowpair,
-    int32_t* tokrow, int32_t* pairrow, int* status) {
+    int32_t* pairrow, int* status) {
   __shared__ int hist[8][kMaxExperts];
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -377,7 +373,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
   const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
   if (chunk >= NW) return;
   walk_chunk<true>(idx, P, E, k, chunk, hist[w], warp_base + chunk * E, s_off, s_poff, perm,
-                   inv_perm, rowpair, tokrow, pairrow, status);
+                   inv_perm, rowpair, pairrow, status);
 }
 
 void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
@@ -390,7 +386,6 @@ void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int3
   int* counts_ws = at<int>(ws, L.counts);
   int* poff = at<int>(ws, L.poff);
   int32_t* rowpair = at<int32_t>(ws, L.rowpair);
-  int32_t* tokrow = at<int32_t>(ws, L.tokrow);
   int4* tiles = at<int4>(ws, L.tiles);
   int* ntiles = at<int>(ws, L.ntiles);
   const int64_t NW = L.NWc;
@@ -405,11 +400,11 @@ void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int3
   }
   MOE_LAUNCH("perm_finalize", s,
              perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, counts, offsets, poff, tiles,
-                                                     ntiles, rowpair, tokrow));
+                                                     ntiles, rowpair));
   if (NW > 0)
     MOE_LAUNCH("perm_scatter", s,
                perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, k, NW, warp_base, offsets,
-                                                          poff, perm, inv_perm, rowpair, tokrow,
+                                                          poff, perm, inv_perm, rowpair,
                                                           at<int32_t>(ws, L.pairrow), status));
 }
 

@@ -1,0 +1,193 @@
+// Router backward.  The gates are a softmax over the k selected logits, so
+// the logit gradient of slot j is g_j (dg_j - sum_i g_i dg_i), with dg_j the
+// gradient of the gate (the row-dot <dy_t W_down[e]^T, H_r> produced by the
+// grouped backward), and zero on the experts that were not selected
+// (gpu_moe_h100.json: value_and_grad through the router).  Then
+// dW_r = x^T dlogits, and dx gains dlogits W_r^T (a row stream, stream.cu).
+#include "kernels.cuh"
+
+namespace moe {
+namespace {
+
+// dsel[t, j] = g_j (dg_j - sum_i g_i dg_i); dg_j is the sum (in column-tile
+// order) of the grouped backward's partials of pair t*k+j.  A group of G
+// lanes (the power of two >= k) takes one token, lane j of the group its
+// slot j.  With dl given, the token's dense bf16 row of the logit gradient
+// (zero off the selection; E a multiple of 8) is written as well.
+__global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restrict__ gates,
+                                                          const float* __restrict__ dg_part,
+                                                          int dg_ld, int dg_n, int64_t Tn, int k,
+                                                          int G, float* __restrict__ dsel,
+                                                          const int32_t* __restrict__ idx, int E,
+                                                          __nv_bfloat16* __restrict__ dl) {
+  const int j = threadIdx.x & (G - 1);
+  const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
+  const bool live = t < Tn;  // every lane stays for the shuffles
+  const bool own = live && j < k;
+  const int64_t p = t * k + j;
+  float dg = 0.f, g = 0.f;
+  if (own) {
+    const float* src = dg_part + p * dg_ld;
+    for (int q = 0; q < dg_n; ++q) dg += src[q];
+    g = gates[p];
+  }
+  float sgd = g * dg;
+  for (int o = G / 2; o > 0; o >>= 1) sgd += __shfl_xor_sync(0xffffffffu, sgd, o);
+  const float v = g * (dg - sgd);
+  if (own) dsel[p] = v;
+  if (dl) {
+    if (live) {
+      uint4* row = reinterpret_cast<uint4*>(dl + t * E);
+      for (int e8 = j; e8 < E / 8; e8 += G) row[e8] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();  // the zeros land before the selected entries
+    if (own) dl[t * E + idx[p]] = __float2bfloat16_rn(v);
+  }
+}
+
+// W_r^T [E, d] from W_r [d, E] (storage type unchanged)
+template <typename T>
+__global__ void __launch_bounds__(256) transpose_router_kernel(const T* __restrict__ w, int d,
+                                                               int E, T* __restrict__ wt) {
+  const int64_t n = (int64_t)d * E;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / E, e = i % E;
+    wt[e * d + r] = w[i];
+  }
+}
+
+// dW_r partial of one token range: thread i owns input dimension i and its
+// column of the shared accumulator [E][256], so the order of the adds is
+// fixed; the range's (expert, dsel) pairs are staged in shared memory.
+template <typename T>
+__global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
+                                                        const int32_t* __restrict__ idx,
+                                                        const float* __restrict__ dsel,
+                                                        int64_t Tn, int d, int E, int k,
+                                                        int64_t per_range, float* part) {
+  extern __shared__ __align__(16) float s_acc[];  // [E][256]
+  __shared__ int s_e[256];
+  __shared__ float s_ds[256];
+  const int tid = threadIdx.x;
+  const int i = blockIdx.y * 256 + tid;
+  for (int e = 0; e < E; ++e) s_acc[e * 256 + tid] = 0.f;
+  const int64_t t0 = blockIdx.x * per_range;
+  const int64_t t1 = t0 + per_range < Tn ? t0 + per_range : Tn;
+  const int CH = 256 / k;
+  for (int64_t tc = t0; tc < t1; tc += CH) {
+    const int nt = (int)(t1 - tc < CH ? t1 - tc : CH);
+    __syncthreads();
+    if (tid < nt * k) {
+      s_e[tid] = idx[tc * k + tid];
+      s_ds[tid] = dsel[tc * k + tid];
+    }
+    __syncthreads();
+    if (i < d) {
+      int u = 0;
+      for (; u + 8 <= nt; u += 8) {
+        float xv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) xv[q] = to_f32(x[(tc + u + q) * d + i]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          for (int j = 0; j < k; ++j) {
+            const int e = s_e[(u + q) * k + j];
+            s_acc[e * 256 + tid] = fmaf(xv[q], s_ds[(u + q) * k + j], s_acc[e * 256 + tid]);
+          }
+      }
+      for (; u < nt; ++u) {
+        const float xv = to_f32(x[(tc + u) * d + i]);
+        for (int j = 0; j < k; ++j) {
+          const int e = s_e[u * k + j];
+          s_acc[e * 256 + tid] = fmaf(xv, s_ds[u * k + j], s_acc[e * 256 + tid]);
+        }
+      }
+    }
+  }
+  if (i < d) {
+    float* out = part + ((int64_t)blockIdx.x * d + i) * E;
+    for (int e = 0; e < E; ++e) out[e] = s_acc[e * 256 + tid];
+  }
+}
+
+__global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __restrict__ part,
+                                                               int ranges, int64_t n, float* dw) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float s = 0.f;
+#pragma unroll 8
+  for (int r = 0; r < ranges; ++r) s += part[(int64_t)r * n + i];
+  dw[i] = s;
+}
+
+template <typename T>
+void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
+                       int dg_ld, void* ws, cudaStream_t s) {
+  const int dm = d.d_model, E = d.experts, k = d.top_k;
+  if (d.tokens == 0) {
+    zero_fill_f32(p.dw_router, (int64_t)dm * E, s);
+    return;
+  }
+  float* dsel = at<float>(ws, L.dsel);
+  float* part = at<float>(ws, L.dwr_part);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(router_dw_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         kRouterBwdSmem);
+    attr_set = true;
+  }
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const bool tc_dw = tc_router_dw_supported(d);
+
+  int G = 1;
+  while (G < k) G *= 2;
+  MOE_LAUNCH("router_dsel", s,
+             router_dsel_kernel<<<(unsigned)((d.tokens * G + 255) / 256), 256, 0, s>>>(
+                 p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, G, dsel,
+                 p.topk_idx, E, tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr));
+
+  T* wt = at<T>(ws, L.wrt);
+  MOE_LAUNCH("router_transpose", s,
+             transpose_router_kernel<T><<<(unsigned)((dm * E + 255) / 256), 256, 0, s>>>(
+                 reinterpret_cast<const T*>(p.w_router), dm, E, wt));
+
+  launch_router_dx(d, L, p, dsel, wt, ws, s);
+
+  if (tc_dw) {
+    tc_router_dw(d, L, p, ws, s);
+    return;
+  }
+  const int ny = (dm + 255) / 256;
+  int64_t ranges = (int64_t)sms * 4 / ny;
+  const int64_t by_tokens = (d.tokens + 63) / 64;
+  if (ranges > by_tokens) ranges = by_tokens;
+  if (ranges > kRouterBwdRanges) ranges = kRouterBwdRanges;
+  if (ranges < 1) ranges = 1;
+  const int64_t per_range = (d.tokens + ranges - 1) / ranges;
+  MOE_LAUNCH("router_dw", s,
+             router_dw_kernel<T><<<dim3((unsigned)ranges, ny), 256, sizeof(float) * E * 256, s>>>(
+                 reinterpret_cast<const T*>(p.x), p.topk_idx, dsel, d.tokens, dm, E, k, per_range,
+                 part));
+  const int64_t n = (int64_t)dm * E;
+  MOE_LAUNCH("router_dw_reduce", s,
+             router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+                 part, (int)ranges, n, p.dw_router));
+}
+
+}  // namespace
+
+void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
+                            int dg_ld, void* ws, cudaStream_t s) {
+  if (d.dtype == MOE_BF16) router_backward_t<__nv_bfloat16>(d, L, p, dg_n, dg_ld, ws, s);
+  else router_backward_t<float>(d, L, p, dg_n, dg_ld, ws, s);
+}
+
+bool router_backward_supported(const moe_dims& d) {
+  // the CUDA-core dW_r path keeps one [E][256] f32 accumulator per block
+  return tc_router_dw_supported(d) || (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem;
+}
+
+}  // namespace moe

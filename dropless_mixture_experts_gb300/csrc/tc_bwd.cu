@@ -225,8 +225,7 @@ int tc_dz_bn(int h) { return pick_bn(h); }
 
 bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                        cudaStream_t s) {
-  launch_gather_rows(p.dy, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1,
-                     at<void>(ws, L.dys), L.PPcap, (int64_t)d.d_model * 2, s);
+  launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s);
   if (d.shared_hidden > 0 && !backward_one(d, L, p, ws, false, s)) return false;
   return backward_one(d, L, p, ws, true, s);
 }

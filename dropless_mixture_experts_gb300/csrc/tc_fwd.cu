@@ -137,8 +137,7 @@ bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_
 
 bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                     cudaStream_t s) {
-  launch_gather_rows(p.x, at<int32_t>(ws, L.tokrow), at<int>(ws, L.ntiles) + 1, at<void>(ws, L.xs),
-                     L.PPcap, (int64_t)d.d_model * 2, s);
+  launch_scatter_rows(d, L, p.x, at<void>(ws, L.xs), ws, s);
   if (!gateup_any(d, L, mode, p, ws, true, s)) return false;
   return down_any(d, L, p, ws, true, s);
 }

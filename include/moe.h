@@ -24,6 +24,10 @@
  * - All tensor pointers are DEVICE pointers owned by the caller.  Every
  *   tensor is dense and row-major.  Weights: w_router [d, E]; w_gate, w_up
  *   [E, d, h]; w_down [E, h, d]; ws_gate, ws_up [d, hs]; ws_down [hs, d].
+ * - Activations, weights and their gradients move in 16-byte vectors and
+ *   bulk copies: each of those arrays must start on a 16-byte boundary
+ *   (MOE_ERR_INVALID_ARG otherwise).  Index, gate and logit arrays need only
+ *   their element alignment.
  * - dtype MOE_F32: every activation, weight and gradient is float32.
  *   dtype MOE_BF16: x, y, dy, dx, weights and the saved activations are
  *   bfloat16; logits, gates and every weight gradient are float32.

@@ -98,3 +98,21 @@ def test_null_pointers_rejected(lib):
     # a value without a place to put it
     assert abi.moe_combine(d, 0, None, None, None, None, 256, None, None, None, 256, None, 0x1000,
                            need, None, check=False) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_misaligned_row_data_rejected(lib):
+    # row data moves in 16-byte vectors and bulk copies: an array that does
+    # not start on a 16-byte boundary is refused before anything launches
+    d = abi.make_dims(64, 128, 128, 8, 2, 0, abi.MOE_BF16)
+    need = abi.moe_workspace_bytes(d, abi.MOE_FWD_ONLY)
+    need_t = abi.moe_workspace_bytes(d, abi.MOE_SAVE_FOR_BWD)
+    assert abi.moe_route(d, 0x108, 256, None, None, 256, 256, 0x1000, need, None,
+                         check=False) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_grouped_ffn_fwd(d, 0, 256, 256, 256, 256, 0x2008, 256, None, None, 0x1000,
+                                   need, None, check=False) == abi.MOE_ERR_INVALID_ARG
+    assert abi.moe_combine(d, 0, None, None, None, None, 0x2004, None, None, None, None, None,
+                           0x1000, need, None, check=False) == abi.MOE_ERR_INVALID_ARG
+    ptrs = [256] * 23
+    ptrs[15] = 0x3002  # dx
+    assert abi.moe_backward(d, *ptrs[:15], *ptrs[15:23], 0x1000, need_t, None,
+                            check=False) == abi.MOE_ERR_INVALID_ARG

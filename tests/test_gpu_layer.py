@@ -22,6 +22,11 @@ SMALL = [
     MoEConfig(1, 128, 64, 4, 1, 0, "f32", "f32_one_token"),
     MoEConfig(4097, 128, 64, 16, 4, 0, "bf16", "bf16_e16k4"),
     MoEConfig(2050, 256, 128, 64, 8, 256, "bf16", "bf16_decoder_small"),
+    # the largest top-k (a single-stage row stream) and rows that end inside
+    # a 512-byte stream piece
+    MoEConfig(300, 192, 64, 32, 32, 64, "bf16", "bf16_k32_shared"),
+    MoEConfig(200, 64, 64, 32, 32, 0, "f32", "f32_k32"),
+    MoEConfig(333, 640, 128, 8, 2, 0, "bf16", "bf16_d640"),
 ]
 
 
