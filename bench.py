@@ -54,20 +54,28 @@ def step_flops(cfg):
 
 
 def kernel_work(cfg):
-    """Algorithmic work per step of each grouped-GEMM kernel name:
-    (unit, amount).  Contractions count 2*M*N*K flops over real rows."""
+    """Algorithmic work per step of each kernel name: ("flop", n) for the
+    contractions (2*M*N*K over real rows; the routed experts' launches, and
+    the shared expert's with suffix _sh), ("byte", n) for the row streams
+    (each row read or written once)."""
     T, d, h, E, k, hs = cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k, cfg.shared_hidden
     P = T * k
-    fl = {
-        "gateup": 2 * P * d * 2 * h + 2 * T * d * 2 * hs,
-        "down": 2 * P * h * d + 2 * T * hs * d,
-        "dz": 2 * P * d * h + 2 * T * d * hs,
-        "dx": 2 * P * 2 * h * d + 2 * T * 2 * hs * d,
-        "dw_down": 2 * P * h * d + 2 * T * hs * d,
-        "dw_gateup": 2 * P * d * 2 * h + 2 * T * d * 2 * hs,
-        "logits": 2 * T * d * E,
-    }
-    return fl
+    el = 2 if cfg.dtype == "bf16" else 4
+    w = {"logits": ("flop", 2 * T * d * E), "router": ("flop", 2 * T * d * E),
+         "router_dw": ("flop", 2 * T * d * E)}
+    for name, n in (("gateup", 2), ("down", 1), ("dz", 1), ("dx", 2), ("dw_down", 1),
+                    ("dw_gateup", 2)):
+        w[name] = ("flop", 2 * P * d * h * n)
+        if hs:
+            w[name + "_sh"] = ("flop", 2 * T * d * hs * n)
+    shared_rows = T if hs else 0
+    # x -> xs and dy -> dys: each token row read once, written to its k rows
+    w["scatter_rows"] = ("byte", 2 * (T + P) * d * el)
+    # pair rows + shared rows + upstream read, y written
+    w["combine"] = ("byte", (P + shared_rows + T + T) * d * el)
+    # pair rows + shared rows read, dx written
+    w["router_dx"] = ("byte", (P + shared_rows + T) * d * el)
+    return w
 
 
 def src_hash():
@@ -327,19 +335,27 @@ def main():
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except Exception:
         pass
-    top = max(rec.items(), key=lambda kv: kv[1][1])
-    tname, (tn, tms) = top
-    key = tname.split("_", 1)[1] if "_" in tname else tname
+    # the dominant kernel with a known algorithmic amount of work
+    def work_of(name):
+        return work.get(name.split("_", 1)[1] if name.startswith(("tc_", "simt_")) else name)
+    known = [kv for kv in rec.items() if work_of(kv[0])]
+    tname, (tn, tms) = max(known, key=lambda kv: kv[1][1])
+    unit, amount = work_of(tname)
+    amount *= prof_steps
     alu = tname.startswith("simt_")
-    flops = work.get(key, 0) * prof_steps
-    achieved = flops / (tms / 1e3) / 1e12 if tms > 0 else 0.0
-    if alu:
+    if unit == "byte":
+        achieved = amount / (tms / 1e3) / 1e9 if tms > 0 else 0.0
+        peak = float(peaks.get("hbm_gbs", 6800.0))
+        bound, runit = "hbm", "GB/s"
+    elif alu:
+        achieved = amount / (tms / 1e3) / 1e12 if tms > 0 else 0.0
         # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock
         peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
-        bound = "alu"
+        bound, runit = "alu", "TFLOP/s"
     else:
+        achieved = amount / (tms / 1e3) / 1e12 if tms > 0 else 0.0
         peak = float(peaks.get("bf16_tflops", 1900.0))
-        bound = "tensor"
+        bound, runit = "tensor", "TFLOP/s"
     traffic = None
     try:
         tr = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
@@ -348,13 +364,24 @@ def main():
             traffic = ent["bytes_per_launch"]
     except Exception:
         pass
-    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
                 "frac": achieved / peak if peak else None, "traffic": traffic,
                 "kernel": tname, "launch_ms": tms / tn,
-                "peak_source": "measured bf16 burst" if bound == "tensor"
-                else "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"}
-    kernels = {k: {"launches_per_step": n / prof_steps, "ms_per_step": t / prof_steps}
-               for k, (n, t) in sorted(rec.items(), key=lambda kv: -kv[1][1])}
+                "peak_source": {"tensor": "measured bf16 burst", "hbm": "measured HBM copy",
+                                "alu": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"}[bound]}
+    kernels = {}
+    for k_, (n, t) in sorted(rec.items(), key=lambda kv: -kv[1][1]):
+        ent = {"launches_per_step": n / prof_steps, "ms_per_step": t / prof_steps}
+        wk = work_of(k_)
+        if wk and t > 0:
+            u, a = wk
+            if u == "byte":
+                ent["gbs"] = a / (t / prof_steps / 1e3) / 1e9
+                ent["frac_hbm"] = ent["gbs"] / float(peaks.get("hbm_gbs", 6800.0))
+            elif not k_.startswith("simt_"):
+                ent["tflops"] = a / (t / prof_steps / 1e3) / 1e12
+                ent["frac_bf16"] = ent["tflops"] / float(peaks.get("bf16_tflops", 1900.0))
+        kernels[k_] = ent
 
     f_fwd, f_train = step_flops(cfg)
     bf16_peak = float(peaks.get("bf16_tflops", 1900.0))

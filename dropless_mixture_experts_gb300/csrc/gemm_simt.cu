@@ -352,9 +352,12 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 template <Kind KIND, typename T, bool ROUTED>
 void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
   if (blocks <= 0) return;
-  static const char* names[] = {"simt_logits", "simt_gateup", "simt_down", "simt_dz", "simt_dx",
-                                "simt_dw_down", "simt_dw_gateup"};
-  MOE_LAUNCH(names[KIND], s, simt_gemm_kernel<KIND, T, ROUTED><<<(unsigned)blocks, NT, 0, s>>>(a));
+  static const char* names[2][7] = {
+      {"simt_logits", "simt_gateup_sh", "simt_down_sh", "simt_dz_sh", "simt_dx_sh",
+       "simt_dw_down_sh", "simt_dw_gateup_sh"},
+      {"simt_logits", "simt_gateup", "simt_down", "simt_dz", "simt_dx", "simt_dw_down",
+       "simt_dw_gateup"}};
+  MOE_LAUNCH(names[ROUTED ? 1 : 0][KIND], s, simt_gemm_kernel<KIND, T, ROUTED><<<(unsigned)blocks, NT, 0, s>>>(a));
 }
 
 template <typename T>

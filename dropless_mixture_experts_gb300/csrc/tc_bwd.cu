@@ -53,7 +53,7 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     mp.b1 = mp.b0;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dz",
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dz_sh",
                                                        s);
   }
   return true;
@@ -90,7 +90,7 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     if (!make_map(&mp.b1, p.ws_up, dm, h, 64, BN)) return false;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dx",
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dx_sh",
                                                        s);
   }
   return true;
@@ -155,7 +155,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     mp.b1 = mp.b0;
     q.rows = d.tokens;
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
-        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
+        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_down_sh", s);
   }
   reduce_splits(q, out, nullptr, s);
   return true;
@@ -199,7 +199,7 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     mp.b1 = mp.b0;
     q.rows = d.tokens;
     launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
-        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
+        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_gateup_sh", s);
   }
   reduce_splits(q, g, u, s);
   return true;

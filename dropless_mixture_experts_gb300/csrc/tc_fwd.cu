@@ -48,7 +48,7 @@ bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, vo
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
     launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_GU, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt,
-                                                        "tc_gateup", s);
+                                                        "tc_gateup_sh", s);
   }
   return true;
 }
@@ -85,7 +85,7 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
     launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt,
-                                                          "tc_down", s);
+                                                          "tc_down_sh", s);
   }
   return true;
 }
