@@ -39,13 +39,17 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// exp(sel - top) for float32 logits: the gap is exact in double; its float
-// head and tail give expf(head) * (1 + tail) to float accuracy even for
-// large gaps, where a float32 difference alone would lose the tail.
+// exp(sel - top) for float32 logits.  The gap sel - top is split exactly
+// into its float rounding (head) and the rounding error (tail) with Knuth's
+// TwoSum, so expf(head) * (1 + tail) is accurate to float even for large
+// gaps, where a float32 difference alone would lose the tail (no float64
+// arithmetic, which is slow on this part).
 __device__ __forceinline__ float gate_exp(float sel, float top) {
-  const double diff = (double)sel - (double)top;
-  const float head = (float)diff;
-  const float tail = (float)(diff - (double)head);
+  const float b = -top;
+  const float head = sel + b;
+  const float bv = head - sel;
+  const float av = head - bv;
+  const float tail = (sel - av) + (b - bv);
   return expf(head) * (1.f + tail);
 }
 
@@ -88,6 +92,15 @@ inline int pick_bn(int n) { return n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 64;
 inline int split_bound(int64_t tiles) {
   int s = 1;
   while (s < 16 && tiles * s < 256) s *= 2;
+  return s;
+}
+
+// K splits of the router-weight gradient x^T dlogits, a d x E product over
+// every token: enough splits that its few output tiles fill the GPU twice
+// over (a power of two, at most 64).
+inline int router_dw_split_bound(int64_t tiles) {
+  int s = 1;
+  while (s < 64 && tiles * s * 2 <= 512) s *= 2;
   return s;
 }
 
@@ -146,7 +159,7 @@ inline Layout make_layout(const moe_dims& d, int mode) {
       pf = std::max(pf, need(1, hs, dm, pick_bn((int)dm), false));
       pf = std::max(pf, need(1, dm, 2 * hs, pick_bn((int)hs), false));
     }
-    pf = std::max(pf, need(1, dm, E, 64, true));
+    pf = std::max(pf, (int64_t)router_dw_split_bound((dm + 127) / 128) * dm * 64);
     L.dwpart = take(sizeof(float) * pf);
   }
   L.total = o;

@@ -100,6 +100,7 @@ struct Cfg {
   static constexpr int STAGES = (kSmemLimit - FIXED) / STAGE_BYTES > 8
                                     ? 8
                                     : (kSmemLimit - FIXED) / STAGE_BYTES;
+
   static constexpr bool A_MN = AK == A_MN_TMA;
   static constexpr bool B_MN = BKIND == B_MN_TMA;
   static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
@@ -191,6 +192,62 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sh
       sh->abort = 1;
       report_error(status, MOE_ERR_TIMEOUT, where);
       return false;
+    }
+  }
+}
+
+// The router's selection for one row: the top k of its E (<= EN) logits in
+// the selection order (larger logit first, the lower expert index on equal
+// logits) and the softmax of the selected logits.  KR > 0 (k <= KR): one
+// pass, the unnormalised gates kept per thread; KR == 0: a first pass for
+// the denominator and a second that repeats the selection for the gates.
+template <int EN, int KR>
+__device__ __forceinline__ void router_topk(const float (&lg)[64], int E, int k, int32_t* idx,
+                                            float* gates) {
+  auto next = [&](unsigned long long taken, float& bv) {
+    int bi = -1;
+    bv = 0.f;
+#pragma unroll
+    for (int e = 0; e < EN; ++e) {
+      if (e < E && !((taken >> e) & 1ull) && (bi < 0 || better(lg[e], e, bv, bi))) {
+        bv = lg[e];
+        bi = e;
+      }
+    }
+    return bi;
+  };
+  unsigned long long taken = 0ull;
+  float top = 0.f, sum = 0.f;
+  if constexpr (KR > 0) {
+    // a pass loop (the unrolled selection is long: kept once in the code);
+    // the unnormalised gates in a small per-thread array
+    float z[KR];
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+      float bv;
+      const int bi = next(taken, bv);
+      taken |= 1ull << bi;
+      if (r == 0) top = bv;
+      z[r] = gate_exp(bv, top);
+      sum += z[r];
+      idx[r] = bi;
+    }
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) gates[r] = z[r] / sum;
+  } else {
+    for (int r = 0; r < k; ++r) {
+      float bv;
+      const int bi = next(taken, bv);
+      taken |= 1ull << bi;
+      if (r == 0) top = bv;
+      sum += gate_exp(bv, top);
+      idx[r] = bi;
+    }
+    taken = 0ull;
+    for (int r = 0; r < k; ++r) {
+      float bv;
+      taken |= 1ull << next(taken, bv);
+      gates[r] = gate_exp(bv, top) / sum;
     }
   }
 }
@@ -555,26 +612,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int32_t* idx = reinterpret_cast<int32_t*>(p.out0) + t * k;
             float* gates = reinterpret_cast<float*>(p.out1) + t * k;
-            unsigned long long taken = 0ull;
-            float top = 0.f, sum = 0.f;
-            for (int r = 0; r < k; ++r) {
-              float bv = 0.f;
-              int bi = -1;
-#pragma unroll
-              for (int e = 0; e < C::BN; ++e) {
-                if (e < E && !((taken >> e) & 1ull) && (bi < 0 || better(lg[e], e, bv, bi))) {
-                  bv = lg[e];
-                  bi = e;
-                }
-              }
-              taken |= 1ull << bi;
-              if (r == 0) top = bv;
-              const float z = gate_exp(bv, top);
-              sum += z;
-              idx[r] = bi;
-              gates[r] = z;
-            }
-            for (int r = 0; r < k; ++r) gates[r] = gates[r] / sum;
+            if (k <= 8 && E <= 8) router_topk<8, 8>(lg, E, k, idx, gates);
+            else if (k <= 8 && E <= 16) router_topk<16, 8>(lg, E, k, idx, gates);
+            else if (k <= 8 && E <= 32) router_topk<32, 8>(lg, E, k, idx, gates);
+            else if (k <= 8) router_topk<64, 8>(lg, E, k, idx, gates);
+            else router_topk<64, 0>(lg, E, k, idx, gates);
           }
         }
       } else {  // E_DW: one expert's gradient tile (rows m0.., columns n0..)

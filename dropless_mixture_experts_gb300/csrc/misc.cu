@@ -28,8 +28,20 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restri
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_all; i += stride) {
     const int64_t em = i / N;
     const int n = (int)(i % N);
+    // four partials loaded at a time, added in split order
+    const float* src = part + em * ldp + n;
+    const int64_t sstride = EM * ldp;
     float v = 0.f;
-    for (int s = 0; s < S; ++s) v += part[((int64_t)s * EM + em) * ldp + n];
+    int s = 0;
+    for (; s + 4 <= S; s += 4) {
+      const float a0 = src[(s + 0) * sstride], a1 = src[(s + 1) * sstride];
+      const float a2 = src[(s + 2) * sstride], a3 = src[(s + 3) * sstride];
+      v += a0;
+      v += a1;
+      v += a2;
+      v += a3;
+    }
+    for (; s < S; ++s) v += src[s * sstride];
     if (hsplit > 0) {
       if (n < hsplit) out0[em * hsplit + n] = v;
       else out1[em * hsplit + (n - hsplit)] = v;

@@ -238,11 +238,19 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
                                            int* status) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
+  // every round's expert index is loaded before the walk starts
+  int ev[kPermRounds];
+#pragma unroll
+  for (int r = 0; r < kPermRounds; ++r) {
+    const int64_t p = chunk * kPermChunk + (int64_t)r * 32 + lane;
+    ev[r] = p < P ? __ldg(idx + p) : -1;
+  }
+#pragma unroll
   for (int r = 0; r < kPermRounds; ++r) {
     const int64_t p = chunk * kPermChunk + (int64_t)r * 32 + lane;
     int e = -1;
     if (p < P) {
-      e = idx[p];
+      e = ev[r];
       if (e < 0 || e >= E) {
         report_error(status, MOE_ERR_DEVICE_CHECK, 1);
         e = -1;
@@ -255,6 +263,7 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
     __syncwarp();
     if (e >= 0 && before == 0) hist[e] += __popc(peers);
     __syncwarp();
+    if (SCATTER && p < P && e < 0) pairrow[p] = -1;  // no row: every consumer skips it
     if (SCATTER && e >= 0) {
       const int within = base_e[e] + rank;  // rank of the pair inside its expert
       const int pos = off_e[e] + within;

@@ -41,7 +41,10 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
       for (int e8 = j; e8 < E / 8; e8 += G) row[e8] = make_uint4(0u, 0u, 0u, 0u);
     }
     __syncwarp();  // the zeros land before the selected entries
-    if (own) dl[t * E + idx[p]] = __float2bfloat16_rn(v);
+    if (own) {
+      const int e = idx[p];
+      if (e >= 0 && e < E) dl[t * E + e] = __float2bfloat16_rn(v);  // a rejected index is skipped
+    }
   }
 }
 
@@ -79,8 +82,10 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
     const int nt = (int)(t1 - tc < CH ? t1 - tc : CH);
     __syncthreads();
     if (tid < nt * k) {
-      s_e[tid] = idx[tc * k + tid];
-      s_ds[tid] = dsel[tc * k + tid];
+      const int e = idx[tc * k + tid];
+      const bool ok = e >= 0 && e < E;  // a rejected index contributes nothing
+      s_e[tid] = ok ? e : 0;
+      s_ds[tid] = ok ? dsel[tc * k + tid] : 0.f;
     }
     __syncthreads();
     if (i < d) {

@@ -90,7 +90,10 @@ __global__ void __launch_bounds__(kThreads)
       const int64_t t = i / cpt;
       const int c = (int)(i % cpt);
       const uint4 v = __ldg(src + i);
-      for (int j = 0; j < k; ++j) out[(int64_t)__ldg(pairrow + t * k + j) * cpt + c] = v;
+      for (int j = 0; j < k; ++j) {
+        const int64_t r = __ldg(pairrow + t * k + j);
+        if (r >= 0) out[r * cpt + c] = v;  // a pair without a row (a rejected index) is skipped
+      }
     } else {
       const int64_t q = i - n;
       const int e = (int)(q / per_e);
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(kThreads)
     uint4 v[KM];
 #pragma unroll
     for (int j = 0; j < KM; ++j)
-      if (j < k) v[j] = ldg16(osort + (int64_t)rows[j] * d + col);
+      if (j < k && rows[j] >= 0) v[j] = ldg16(osort + (int64_t)rows[j] * d + col);
     if (i + stride < n) index_ahead(i + stride);
     float acc[VE];
     if (ys) {
@@ -145,7 +148,7 @@ __global__ void __launch_bounds__(kThreads)
     }
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      if (j < k) {
+      if (j < k && rows[j] >= 0) {
         float f[VE];
         cvt16<T>(v[j], f);
 #pragma unroll
@@ -154,11 +157,13 @@ __global__ void __launch_bounds__(kThreads)
     }
     for (int j0 = KM; j0 < k; j0 += KM) {  // k > KM: further slots, in order
 #pragma unroll
-      for (int j = 0; j < KM; ++j)
-        if (j0 + j < k) v[j] = ldg16(osort + (int64_t)__ldg(pairrow + t * k + j0 + j) * d + col);
+      for (int j = 0; j < KM; ++j) {
+        rows[j] = j0 + j < k ? __ldg(pairrow + t * k + j0 + j) : -1;
+        if (rows[j] >= 0) v[j] = ldg16(osort + (int64_t)rows[j] * d + col);
+      }
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
-        if (j0 + j < k) {
+        if (rows[j] >= 0) {
           float f[VE];
           cvt16<T>(v[j], f);
 #pragma unroll
@@ -234,9 +239,9 @@ __global__ void __launch_bounds__(kThreads)
     const uint4 us = dxs ? ldg16(dxs + t * d + col) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      ex[j] = ne[j];
+      ex[j] = j < k && nr[j] >= 0 ? ne[j] : -1;  // -1: no slot, or a pair without a row
       ds[j] = nd[j];
-      if (j < k) v[j] = ldg16(dxsort + (int64_t)nr[j] * d + col);
+      if (ex[j] >= 0) v[j] = ldg16(dxsort + (int64_t)nr[j] * d + col);
     }
     if (i + stride < n) index_ahead(i + stride);
     float acc[VE];
@@ -248,7 +253,7 @@ __global__ void __launch_bounds__(kThreads)
     }
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      if (j < k) {
+      if (ex[j] >= 0) {
         float fv[VE], fw[VE];
         cvt16<T>(v[j], fv);
         cvt16<T>(ldg16(wt + (int64_t)ex[j] * d + col), fw);
@@ -259,16 +264,20 @@ __global__ void __launch_bounds__(kThreads)
     for (int j0 = KM; j0 < k; j0 += KM) {  // k > KM: further slots, in order
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
+        ex[j] = -1;
         if (j0 + j < k) {
           const int64_t p = t * k + j0 + j;
-          ex[j] = __ldg(idx + p);
-          ds[j] = __ldg(dsel + p);
-          v[j] = ldg16(dxsort + (int64_t)__ldg(pairrow + p) * d + col);
+          const int64_t r = __ldg(pairrow + p);
+          if (r >= 0) {
+            ex[j] = __ldg(idx + p);
+            ds[j] = __ldg(dsel + p);
+            v[j] = ldg16(dxsort + r * d + col);
+          }
         }
       }
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
-        if (j0 + j < k) {
+        if (ex[j] >= 0) {
           float fv[VE], fw[VE];
           cvt16<T>(v[j], fv);
           cvt16<T>(ldg16(wt + (int64_t)ex[j] * d + col), fw);

@@ -249,7 +249,11 @@ bool tc_router_dw(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* 
   q.n_nt = 1;
   q.experts = 1;
   q.rows = d.tokens;
-  set_splits(q, L, ws, (d.tokens + 63) / 64, true);
+  // splits of at least four 64-row K blocks each
+  const int64_t kblocks = (d.tokens + 63) / 64;
+  q.splits = router_dw_split_bound(q.n_mt);
+  while (q.splits > 1 && kblocks / q.splits < 4) q.splits /= 2;
+  q.part = at<float>(ws, L.dwpart);
   q.ldp = 64;
   q.facc = p.dw_router;
   if (!make_map(&mp.a, p.x, d.tokens, d.d_model, 64, 64)) return false;

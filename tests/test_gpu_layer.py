@@ -130,3 +130,37 @@ def test_out_of_range_expert_index_is_reported_not_faulted():
     status, detail = layer.device_status()
     assert status == abi.MOE_ERR_DEVICE_CHECK
     assert layer.device_status()[0] == 0   # cleared by the read
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_rejected_expert_index_is_skipped_through_the_train_step(dtype):
+    # a pair whose expert index is out of range gets no sorted row: the
+    # permutation reports it and every later kernel skips the pair, so the
+    # other tokens' outputs and input gradients equal a clean run's
+    from dropless_mixture_experts_gb300 import abi
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    cfg = MoEConfig(300, 128, 64, 8, 2, 64, dtype, "rejected_index")
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, dtype)
+    p = {k: dev[k] for k in params_of(inp)}
+    runs = []
+    for corrupt in (False, True):
+        layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                         cfg.shared_hidden, dtype, train=True)
+        layer.route(dev["x"], p["w_router"])
+        if corrupt:
+            layer.idx[5, 1] = 99
+            layer.idx[17, 0] = -3
+        layer.permute()
+        layer.grouped_ffn_fwd(dev["x"], p, abi.MOE_SAVE_FOR_BWD)
+        layer.combine(dev["x"], p, abi.MOE_SAVE_FOR_BWD, upstream=dev["upstream"])
+        layer.backward(dev["x"], p, dev["upstream"])
+        torch.cuda.synchronize()
+        status, _ = layer.device_status()
+        runs.append((status, layer.y.clone(), layer.dx.clone()))
+    assert runs[0][0] == 0
+    assert runs[1][0] == abi.MOE_ERR_DEVICE_CHECK
+    keep = torch.ones(cfg.tokens, dtype=torch.bool, device="cuda")
+    keep[[5, 17]] = False
+    assert torch.equal(runs[0][1][keep], runs[1][1][keep])
+    assert torch.equal(runs[0][2][keep], runs[1][2][keep])
