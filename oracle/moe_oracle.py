@@ -23,7 +23,12 @@ What it computes (plain definitions, in float64, no blocking or fusion):
   gpu_moe_h100 benchmark page's ``v10_decoder`` rows);
 * the train step's value and gradients with respect to the input and every
   parameter (the gpu_moe_h100 page's description: value_and_grad w.r.t. params
-  and input), for the scalar L = sum(y * G) with G the upstream gradient.
+  and input), for the scalar L = sum(y * G) with G the upstream gradient;
+* optionally capacity routing (the ``routing: capacity`` rows of the
+  kernel_gmm_gpu page, which give neither the capacity nor the drop rule):
+  each expert keeps its first ``capacity`` pairs in increasing pair id and
+  drops the rest; a dropped pair contributes nothing to y, while the gates
+  stay the softmax over all k selected logits.
 
 Pins (``tests/test_oracle_*.py``) tie every function to something other than
 itself: brute-force subset enumeration, library sorts and softmax, the
@@ -40,6 +45,7 @@ __all__ = [
     "param_count",
     "router_logits",
     "route_from_logits",
+    "capacity_keep",
     "counting_sort",
     "silu",
     "swiglu_expert",
@@ -93,7 +99,19 @@ def route_from_logits(logits, top_k: int):
     return idx, gates
 
 
-def counting_sort(idx, experts: int):
+def capacity_keep(idx, experts: int, capacity=None):
+    """Which pairs capacity routing keeps: for each expert, its first
+    ``capacity`` pairs in increasing pair id p = t*k + j (capacity None or 0:
+    every pair, the dropless layer).  Returns a bool array shaped like idx."""
+    flat = np.asarray(idx, dtype=np.int64).reshape(-1)
+    keep = np.zeros(flat.size, dtype=bool)
+    for e in range(experts):
+        members = np.nonzero(flat == e)[0]  # increasing pair id
+        keep[members if not capacity else members[:capacity]] = True
+    return keep.reshape(np.shape(idx))
+
+
+def counting_sort(idx, experts: int, capacity=None):
     """Counting sort of the T*k token-expert pairs by expert.
 
     Pair p = t*k + j carries expert idx[t, j].  counts[e] = number of pairs on
@@ -101,18 +119,23 @@ def counting_sort(idx, experts: int):
     at expert-sorted position r, pairs of one expert kept in increasing pair
     id (a token picks distinct experts, so this is also increasing token id);
     inv_perm[perm[r]] = r.
+
+    With a capacity, only the pairs ``capacity_keep`` keeps are sorted:
+    counts and offsets count kept pairs, perm[r] = -1 for r >= offsets[E]
+    and inv_perm[p] = -1 for a dropped pair.
     """
     flat = np.asarray(idx, dtype=np.int64).reshape(-1)
     P = flat.size
+    keep = capacity_keep(idx, experts, capacity).reshape(-1)
     counts = np.zeros(experts, dtype=np.int64)
     for e in range(experts):
-        counts[e] = int(np.count_nonzero(flat == e))
+        counts[e] = int(np.count_nonzero((flat == e) & keep))
     offsets = np.zeros(experts + 1, dtype=np.int64)
     offsets[1:] = np.cumsum(counts)
-    perm = np.empty(P, dtype=np.int64)
-    inv_perm = np.empty(P, dtype=np.int64)
+    perm = np.full(P, -1, dtype=np.int64)
+    inv_perm = np.full(P, -1, dtype=np.int64)
     for e in range(experts):
-        members = np.nonzero(flat == e)[0]  # increasing pair id
+        members = np.nonzero((flat == e) & keep)[0]  # increasing pair id
         pos = offsets[e] + np.arange(members.size)
         perm[pos] = members
         inv_perm[members] = pos
@@ -142,7 +165,7 @@ def swiglu_expert(X, w_gate, w_up, w_down):
     return A_g, A_u, H, O
 
 
-def forward(x, params, top_k: int, idx=None, logits=None):
+def forward(x, params, top_k: int, idx=None, logits=None, capacity=None):
     """Layer forward pass.
 
     params: dict with w_router [d,E], w_gate [E,d,h], w_up [E,d,h],
@@ -152,9 +175,11 @@ def forward(x, params, top_k: int, idx=None, logits=None):
     ``idx`` may be given to impose the routing (for parity runs that feed the
     routing decided on the device); the gates are then the softmax of the
     given or computed logits at those indices.  ``logits`` may be given to
-    route from fed logits.
+    route from fed logits.  ``capacity`` (pairs per expert) switches on
+    capacity routing (``capacity_keep``).
 
-    y[t] = sum_j gates[t, j] * O[inv_perm[t*k + j]]  (slot order)  + shared(x[t]).
+    y[t] = sum over kept slots j of gates[t, j] * O[inv_perm[t*k + j]]
+    (slot order)  + shared(x[t]).
     Returns a dict holding every intermediate.
     """
     x = _f64(x)
@@ -171,7 +196,7 @@ def forward(x, params, top_k: int, idx=None, logits=None):
         sel = np.take_along_axis(logits, idx, axis=1)
         z = np.exp(sel - sel.max(axis=1, keepdims=True))
         gates = z / z.sum(axis=1, keepdims=True)
-    counts, offsets, perm, inv_perm = counting_sort(idx, E)
+    counts, offsets, perm, inv_perm = counting_sort(idx, E, capacity)
 
     P = T * top_k
     h = w_gate.shape[2]
@@ -190,7 +215,9 @@ def forward(x, params, top_k: int, idx=None, logits=None):
 
     y = np.zeros((T, d))
     for j in range(top_k):
-        y += gates[:, j:j + 1] * O[inv_perm[np.arange(T) * top_k + j]]
+        rows = inv_perm[np.arange(T) * top_k + j]
+        kept = rows >= 0
+        y[kept] += gates[kept, j:j + 1] * O[rows[kept]]
 
     shared = None
     if params.get("ws_down") is not None:
@@ -202,11 +229,12 @@ def forward(x, params, top_k: int, idx=None, logits=None):
                 A_u=A_u, H=H, O=O, shared=shared)
 
 
-def dense_masked_forward(x, params, top_k: int, idx=None):
+def dense_masked_forward(x, params, top_k: int, idx=None, capacity=None):
     """Brute-force formulation: every expert on every token, weighted by a
     dense [T, E] gate matrix that is zero off the selected experts (the
-    ``dense`` routing of the kernel_gmm_gpu benchmark page).  No permutation
-    is involved, so it checks the sorted dispatch end to end."""
+    ``dense`` routing of the kernel_gmm_gpu benchmark page) and, with a
+    capacity, at the dropped pairs.  No permutation is involved, so it checks
+    the sorted dispatch end to end."""
     x = _f64(x)
     T, _ = x.shape
     E = _f64(params["w_gate"]).shape[0]
@@ -219,7 +247,7 @@ def dense_masked_forward(x, params, top_k: int, idx=None):
         z = np.exp(sel - sel.max(axis=1, keepdims=True))
         gates = z / z.sum(axis=1, keepdims=True)
     G = np.zeros((T, E))
-    np.put_along_axis(G, idx, gates, axis=1)
+    np.put_along_axis(G, idx, gates * capacity_keep(idx, E, capacity), axis=1)
     y = np.zeros_like(x)
     for e in range(E):
         O = swiglu_expert(x, params["w_gate"][e], params["w_up"][e], params["w_down"][e])[3]
@@ -259,7 +287,7 @@ def backward(x, params, top_k: int, upstream, fwd):
 
     Per pair (t, j) on expert e at sorted row r, with dy = G:
       dO_r = gates[t, j] * dy_t                (expert output gradient)
-      dgate[t, j] = <dy_t, O_r>
+      dgate[t, j] = <dy_t, O_r>                (0 for a pair capacity dropped)
       expert weight / input gradients through the SwiGLU chain rule;
     router: the gates are a softmax of the selected logits, so
       dlogit[t, idx[t, j]] = g_j * (dgate_j - sum_i g_i dgate_i),
@@ -317,8 +345,8 @@ def backward(x, params, top_k: int, upstream, fwd):
     return out
 
 
-def train_step(x, params, top_k: int, upstream, idx=None, logits=None):
+def train_step(x, params, top_k: int, upstream, idx=None, logits=None, capacity=None):
     """value_and_grad: returns (L, fwd dict, grads dict)."""
-    fwd = forward(x, params, top_k, idx=idx, logits=logits)
+    fwd = forward(x, params, top_k, idx=idx, logits=logits, capacity=capacity)
     grads = backward(x, params, top_k, upstream, fwd)
     return loss(fwd["y"], upstream), fwd, grads

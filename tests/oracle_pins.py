@@ -73,10 +73,54 @@ def permutation_discrepancy(oracle, idx, E):
     return bad
 
 
-def torch_dense_layer(x, params, k, idx=None):
+def capacity_permutation_discrepancy(oracle, idx, E, capacity):
+    """0 when the oracle's capacity-routed counting sort equals an
+    independent construction: pairs visited in increasing id with one running
+    counter per expert decide what is kept; bincount, cumsum and a
+    lexicographic sort by (expert, pair) of the kept pairs give counts,
+    offsets and perm (-1 past the kept rows); inv_perm is -1 on dropped
+    pairs."""
+    counts, offsets, perm, inv = oracle.counting_sort(idx, E, capacity)
+    flat = np.asarray(idx).reshape(-1)
+    seen = [0] * E
+    kept = []
+    for p_, e in enumerate(flat):
+        if seen[e] < capacity:
+            kept.append(p_)
+        seen[e] += 1
+    kept = np.array(kept, dtype=np.int64)
+    ref_counts = np.bincount(flat[kept], minlength=E)
+    ref_offsets = np.concatenate([[0], np.cumsum(ref_counts)])
+    ref_perm = np.full(flat.size, -1)
+    ref_perm[:kept.size] = kept[np.lexsort((kept, flat[kept]))]
+    ref_inv = np.full(flat.size, -1)
+    ref_inv[ref_perm[:kept.size]] = np.arange(kept.size)
+    bad = 0
+    bad += int(not np.array_equal(counts, ref_counts))
+    bad += int(not np.array_equal(offsets, ref_offsets))
+    bad += int(not np.array_equal(perm, ref_perm))
+    bad += int(not np.array_equal(inv, ref_inv))
+    return bad
+
+
+def torch_keep_mask(sel_idx, E, capacity):
+    """Capacity keep mask [T, k] from torch library ops: a pair's rank in its
+    expert is the running count (cumsum over pairs in id order) of the
+    one-hot expert matrix, minus one; kept when the rank is below the
+    capacity (None: every pair)."""
+    T, k = sel_idx.shape
+    if not capacity:
+        return torch.ones((T, k), dtype=torch.float64)
+    onehot = torch.nn.functional.one_hot(sel_idx.reshape(-1), E).to(torch.float64)
+    rank = (torch.cumsum(onehot, dim=0) * onehot).sum(dim=1) - 1.0
+    return (rank < capacity).to(torch.float64).reshape(T, k)
+
+
+def torch_dense_layer(x, params, k, idx=None, capacity=None):
     """The dense-masked layer written with torch library ops in float64 and
-    differentiated by torch autograd.  Returns (y, {name: tensor}) with the
-    tensors requiring grad."""
+    differentiated by torch autograd (with a capacity, the gates of dropped
+    pairs are masked out of the mixture, not out of the softmax).  Returns
+    (y, {name: tensor}) with the tensors requiring grad."""
     t = {kk: (None if v is None else torch.tensor(np.asarray(v, np.float64), requires_grad=True))
          for kk, v in params.items()}
     tx = torch.tensor(np.asarray(x, np.float64), requires_grad=True)
@@ -88,7 +132,8 @@ def torch_dense_layer(x, params, k, idx=None):
         sel = torch.gather(logits, 1, sel_idx)
     gates = torch.softmax(sel, dim=1)
     E = t["w_gate"].shape[0]
-    mask = torch.zeros(logits.shape, dtype=torch.float64).scatter(1, sel_idx, gates)
+    keep = torch_keep_mask(sel_idx, E, capacity)
+    mask = torch.zeros(logits.shape, dtype=torch.float64).scatter(1, sel_idx, gates * keep)
     y = torch.zeros_like(tx)
     for e in range(E):
         a = torch.nn.functional.silu(tx @ t["w_gate"][e]) * (tx @ t["w_up"][e])
@@ -105,13 +150,13 @@ GRAD_NAMES = {"x": "dx", "w_router": "dw_router", "w_gate": "dw_gate", "w_up": "
               "w_down": "dw_down", "ws_gate": "dws_gate", "ws_up": "dws_up", "ws_down": "dws_down"}
 
 
-def autograd_discrepancy(oracle, x, params, k, G):
+def autograd_discrepancy(oracle, x, params, k, G, capacity=None):
     """Max relative difference between the oracle's value and gradients and
     torch autograd through the dense-masked torch formulation."""
-    y, leaves, idx = torch_dense_layer(x, params, k)
+    y, leaves, idx = torch_dense_layer(x, params, k, capacity=capacity)
     L = (y * torch.tensor(np.asarray(G, np.float64))).sum()
     L.backward()
-    Lo, fwd, grads = oracle.train_step(x, params, k, G)
+    Lo, fwd, grads = oracle.train_step(x, params, k, G, capacity=capacity)
     worst = abs(Lo - L.item()) / max(1.0, abs(L.item()))
     worst = max(worst, float(np.max(np.abs(fwd["y"] - y.detach().numpy()))))
     for name, leaf in leaves.items():
@@ -160,10 +205,10 @@ def fd_discrepancy(oracle, x, params, k, G, n_probe=6, eps=1e-6, seed=0):
     return worst
 
 
-def dense_discrepancy(oracle, x, params, k):
+def dense_discrepancy(oracle, x, params, k, capacity=None):
     """Sorted-dispatch forward vs the brute-force dense-masked forward."""
-    y_sorted = oracle.forward(x, params, k)["y"]
-    y_dense = oracle.dense_masked_forward(x, params, k)
+    y_sorted = oracle.forward(x, params, k, capacity=capacity)["y"]
+    y_dense = oracle.dense_masked_forward(x, params, k, capacity=capacity)
     return float(np.max(np.abs(y_sorted - y_dense)))
 
 

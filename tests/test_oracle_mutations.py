@@ -10,8 +10,9 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle_pins import (autograd_discrepancy, dense_discrepancy, permutation_discrepancy,
-                         routing_discrepancy, tiny_problem)
+from oracle_pins import (autograd_discrepancy, capacity_permutation_discrepancy,
+                         dense_discrepancy, permutation_discrepancy, routing_discrepancy,
+                         tiny_problem)
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(__file__)), "oracle", "moe_oracle.py")
 
@@ -33,11 +34,11 @@ MUTATIONS = [
     ("gates_all", "gates = z / z.sum(axis=1, keepdims=True)\n    return idx, gates",
      "gates = z / np.exp(logits - sel[:, :1]).sum(axis=1, keepdims=True)\n    return idx, gates"),
     # unstable order inside an expert
-    ("unstable", "members = np.nonzero(flat == e)[0]  # increasing pair id",
-     "members = np.nonzero(flat == e)[0][::-1]"),
+    ("unstable", "members = np.nonzero((flat == e) & keep)[0]  # increasing pair id",
+     "members = np.nonzero((flat == e) & keep)[0][::-1]"),
     # combine takes the other slot's expert output
-    ("slot", "y += gates[:, j:j + 1] * O[inv_perm[np.arange(T) * top_k + j]]",
-     "y += gates[:, j:j + 1] * O[inv_perm[np.arange(T) * top_k + (top_k - 1 - j)]]"),
+    ("slot", "rows = inv_perm[np.arange(T) * top_k + j]",
+     "rows = inv_perm[np.arange(T) * top_k + (top_k - 1 - j)]"),
     # silu with the wrong sign inside the sigmoid
     ("silu_sign", "return a / (1.0 + np.exp(-a))", "return a / (1.0 + np.exp(a))"),
     # dropped softmax-Jacobian term in the router gradient
@@ -51,6 +52,14 @@ MUTATIONS = [
     ("gate_twice", "dO = g * G[toks]", "dO = g * g * G[toks]"),
     # router input-gradient term dropped
     ("router_dx", "dx += dlogits @ _f64(params[\"w_router\"]).T", "pass"),
+    # capacity keeps an expert's last pairs instead of its first
+    ("capacity_last", "keep[members if not capacity else members[:capacity]] = True",
+     "keep[members if not capacity else members[-capacity:]] = True"),
+    # capacity renormalises the gates over the kept slots
+    ("capacity_renorm", "        y[kept] += gates[kept, j:j + 1] * O[rows[kept]]",
+     "        kg = gates * capacity_keep(idx, E, capacity)\n"
+     "        kg = kg / np.maximum(kg.sum(axis=1, keepdims=True), 1e-300)\n"
+     "        y[kept] += kg[kept, j:j + 1] * O[rows[kept]]"),
 ]
 
 
@@ -62,8 +71,14 @@ def any_pin_fails(mod):
     idx = np.stack([rng.permutation(6)[:3] for _ in range(40)])
     if permutation_discrepancy(mod, idx, 6) != 0:
         return True
+    if capacity_permutation_discrepancy(mod, idx, 6, 15) != 0:
+        return True
     x, p, G = tiny_problem(T=13, d=8, h=12, E=4, k=2, hs=5, seed=3)
     if dense_discrepancy(mod, x, p, 2) > 1e-12:
+        return True
+    if dense_discrepancy(mod, x, p, 2, capacity=4) > 1e-12:
+        return True
+    if autograd_discrepancy(mod, x, p, 2, G, capacity=4) > 1e-9:
         return True
     return autograd_discrepancy(mod, x, p, 2, G) > 1e-9
 
