@@ -41,6 +41,7 @@ class moe_dims(ctypes.Structure):
         ("top_k", ctypes.c_int32),
         ("shared_hidden", ctypes.c_int32),
         ("dtype", ctypes.c_int32),
+        ("capacity", ctypes.c_int32),
     ]
 
 
@@ -98,9 +99,10 @@ def _check(status: int, where: str):
         raise MoEError(status, where)
 
 
-def make_dims(tokens, d_model, d_hidden, experts, top_k, shared_hidden=0, dtype=MOE_BF16):
+def make_dims(tokens, d_model, d_hidden, experts, top_k, shared_hidden=0, dtype=MOE_BF16,
+              capacity=0):
     return moe_dims(int(tokens), int(d_model), int(d_hidden), int(experts), int(top_k),
-                    int(shared_hidden), int(dtype))
+                    int(shared_hidden), int(dtype), int(capacity))
 
 
 def _p(v):

@@ -15,6 +15,7 @@ bool dims_ok(const moe_dims* d) {
   if (d->top_k < 1 || d->top_k > d->experts || d->top_k > kMaxTopK) return false;
   if (d->d_model < 64 || d->d_hidden < 64 || d->shared_hidden < 0) return false;
   if (d->dtype != MOE_F32 && d->dtype != MOE_BF16) return false;
+  if (d->capacity < 0) return false;
   if (d->tokens * (int64_t)d->top_k + (int64_t)d->experts * kRowPad >= (int64_t(1) << 31))
     return false;
   return true;

@@ -169,6 +169,7 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* t
   const int64_t NW = (P + kNaChunk - 1) / kNaChunk;
   // the fixed scratch holds NW x E histogram entries at most
   if (P >= (int64_t(1) << 31) || NW * E > kNaHist) return MOE_ERR_UNSUPPORTED;
+  if (dims->capacity != 0) return MOE_ERR_UNSUPPORTED;  // dropless sort only
   int* scratch = nullptr;
   const moe_status st = na_scratch(&scratch);
   if (st != MOE_OK) return st;

@@ -235,7 +235,7 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
                                            int k, int64_t chunk, int* hist, const int* base_e,
                                            const int* off_e, const int* poff_e, int32_t* perm,
                                            int32_t* inv_perm, int32_t* rowpair, int32_t* pairrow,
-                                           int* status) {
+                                           int capacity, int* status) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   // every round's expert index is loaded before the walk starts
@@ -263,9 +263,16 @@ __device__ __forceinline__ void walk_chunk(const int32_t* __restrict__ idx, int6
     __syncwarp();
     if (e >= 0 && before == 0) hist[e] += __popc(peers);
     __syncwarp();
-    if (SCATTER && p < P && e < 0) pairrow[p] = -1;  // no row: every consumer skips it
-    if (SCATTER && e >= 0) {
-      const int within = base_e[e] + rank;  // rank of the pair inside its expert
+    // rank of the pair inside its expert, in increasing pair id
+    const int within = SCATTER && e >= 0 ? base_e[e] + rank : 0;
+    // a rejected index, or a pair past its expert's capacity: no sorted
+    // position and no row (every consumer of the row map skips it)
+    const bool dropped = e < 0 || (capacity > 0 && within >= capacity);
+    if (SCATTER && p < P && dropped) {
+      pairrow[p] = -1;
+      inv_perm[p] = -1;
+    }
+    if (SCATTER && !dropped) {
       const int pos = off_e[e] + within;
       const int ppos = poff_e[e] + within;
       perm[pos] = (int32_t)p;
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restric
   __syncwarp();
   if (chunk >= NW) return;
   walk_chunk<false>(idx, P, E, k, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, nullptr,
-                    nullptr, nullptr, status);
+                    nullptr, nullptr, 0, status);
   for (int e = lane; e < E; e += 32) warp_counts[chunk * E + e] = hist[w][e];
 }
 
@@ -321,12 +328,17 @@ __global__ void __launch_bounds__(1024) perm_colscan_kernel(const int* __restric
 }
 
 // Offsets, padded offsets, the tile list and the padding rows (one block).
-__global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restrict__ counts_ws,
-                                                             int E, int32_t* counts_out,
+// With a capacity the counts become the kept counts (in the workspace too:
+// the weight-gradient GEMMs take their K ranges from there), and perm past
+// the kept rows reads -1.
+__global__ void __launch_bounds__(1024) perm_finalize_kernel(int* __restrict__ counts_ws, int E,
+                                                             int capacity, int64_t P,
+                                                             int32_t* counts_out,
                                                              int32_t* offsets_out, int* poff,
                                                              int4* tiles, int* ntiles,
-                                                             int32_t* rowpair) {
+                                                             int32_t* rowpair, int32_t* perm) {
   __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1], s_toff[kMaxExperts + 1];
+  __shared__ int s_cnt[kMaxExperts];
   const int tid = threadIdx.x;
   if (tid == 0) {
     int o = 0, po = 0, to = 0;
@@ -334,7 +346,8 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restri
       s_off[e] = o;
       s_poff[e] = po;
       s_toff[e] = to;
-      const int c = counts_ws[e];
+      const int c = capacity > 0 && counts_ws[e] > capacity ? capacity : counts_ws[e];
+      s_cnt[e] = c;
       const int nt = (c + kRowPad - 1) / kRowPad;
       o += c;
       po += nt * kRowPad;
@@ -350,10 +363,14 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(const int* __restri
   for (int e = tid; e <= E; e += blockDim.x) {
     offsets_out[e] = s_off[e];
     poff[e] = s_poff[e];
-    if (e < E) counts_out[e] = counts_ws[e];
+    if (e < E) {
+      counts_out[e] = s_cnt[e];
+      counts_ws[e] = s_cnt[e];
+    }
   }
+  for (int64_t r = s_off[E] + tid; r < P; r += blockDim.x) perm[r] = -1;  // past the kept rows
   for (int e = 0; e < E; ++e) {
-    const int c = counts_ws[e];
+    const int c = s_cnt[e];
     const int nt = s_toff[e + 1] - s_toff[e];
     for (int j = tid; j < nt; j += blockDim.x) {
       const int valid = min(kRowPad, c - j * kRowPad);
@@ -369,7 +386,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
     const int32_t* __restrict__ idx, int64_t P, int E, int k, int64_t NW,
     const int* __restrict__ warp_base, const int32_t* __restrict__ offsets,
     const int* __restrict__ poff, int32_t* perm, int32_t* inv_perm, int32_t* rowpair,
-    int32_t* pairrow, int* status) {
+    int32_t* pairrow, int capacity, int* status) {
   __shared__ int hist[8][kMaxExperts];
   __shared__ int s_off[kMaxExperts], s_poff[kMaxExperts];
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -382,7 +399,7 @@ __global__ void __launch_bounds__(256) perm_scatter_kernel(
   const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
   if (chunk >= NW) return;
   walk_chunk<true>(idx, P, E, k, chunk, hist[w], warp_base + chunk * E, s_off, s_poff, perm,
-                   inv_perm, rowpair, pairrow, status);
+                   inv_perm, rowpair, pairrow, capacity, status);
 }
 
 void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
@@ -408,13 +425,15 @@ void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int3
     zero_fill_i32(counts_ws, E, s);
   }
   MOE_LAUNCH("perm_finalize", s,
-             perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, counts, offsets, poff, tiles,
-                                                     ntiles, rowpair));
+             perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, d.capacity, L.P, counts,
+                                                     offsets, poff, tiles, ntiles, rowpair,
+                                                     perm));
   if (NW > 0)
     MOE_LAUNCH("perm_scatter", s,
                perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, k, NW, warp_base, offsets,
                                                           poff, perm, inv_perm, rowpair,
-                                                          at<int32_t>(ws, L.pairrow), status));
+                                                          at<int32_t>(ws, L.pairrow), d.capacity,
+                                                          status));
 }
 
 }  // namespace moe

@@ -10,7 +10,8 @@ namespace moe {
 namespace {
 
 // dsel[t, j] = g_j (dg_j - sum_i g_i dg_i); dg_j is the sum (in column-tile
-// order) of the grouped backward's partials of pair t*k+j.  A group of G
+// order) of the grouped backward's partials of pair t*k+j, and 0 for a pair
+// without a row (capacity-dropped or a rejected index).  A group of G
 // lanes (the power of two >= k) takes one token, lane j of the group its
 // slot j.  With dl given, the token's dense bf16 row of the logit gradient
 // (zero off the selection; E a multiple of 8) is written as well.
@@ -19,6 +20,7 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
                                                           int dg_ld, int dg_n, int64_t Tn, int k,
                                                           int G, float* __restrict__ dsel,
                                                           const int32_t* __restrict__ idx, int E,
+                                                          const int32_t* __restrict__ pairrow,
                                                           __nv_bfloat16* __restrict__ dl) {
   const int j = threadIdx.x & (G - 1);
   const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
@@ -27,8 +29,10 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
   const int64_t p = t * k + j;
   float dg = 0.f, g = 0.f;
   if (own) {
-    const float* src = dg_part + p * dg_ld;
-    for (int q = 0; q < dg_n; ++q) dg += src[q];
+    if (pairrow[p] >= 0) {
+      const float* src = dg_part + p * dg_ld;
+      for (int q = 0; q < dg_n; ++q) dg += src[q];
+    }
     g = gates[p];
   }
   float sgd = g * dg;
@@ -152,7 +156,8 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
   MOE_LAUNCH("router_dsel", s,
              router_dsel_kernel<<<(unsigned)((d.tokens * G + 255) / 256), 256, 0, s>>>(
                  p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, G, dsel,
-                 p.topk_idx, E, tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr));
+                 p.topk_idx, E, at<const int32_t>(ws, L.pairrow),
+                 tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr));
 
   T* wt = at<T>(ws, L.wrt);
   MOE_LAUNCH("router_transpose", s,

@@ -205,13 +205,16 @@ __global__ void __launch_bounds__(32) loss_reduce_kernel(const float* __restrict
 // ---- router backward: input gradient ------------------------------------------
 // dx[t] = dxs[t] + sum_j (dxsort[pairrow[t*k + j]] + dsel[t, j] W_r[:, e_j]),
 // the pair rows in slot order; W_r^T [E, d] rows come through the cache.
-// The first KM slots' indices and logit gradients are loaded one item ahead.
+// A capacity-dropped slot has no row but keeps its router term (the softmax
+// couples it to the kept slots); a rejected index (e outside [0, E)) has
+// neither.  The first KM slots' indices and logit gradients are loaded one
+// item ahead.
 template <typename T, int KM>
 __global__ void __launch_bounds__(kThreads)
     router_dx_kernel(const int32_t* __restrict__ idx, const float* __restrict__ dsel,
                      const T* __restrict__ wt, const T* __restrict__ dxsort,
                      const int32_t* __restrict__ pairrow, const T* __restrict__ dxs,
-                     T* __restrict__ dx, int64_t Tn, int d, int k) {
+                     T* __restrict__ dx, int64_t Tn, int d, int k, int E) {
   constexpr int VE = 16 / sizeof(T);
   const int cpt = d / VE;
   const int64_t n = Tn * cpt;
@@ -233,15 +236,16 @@ __global__ void __launch_bounds__(kThreads)
   for (; i < n; i += stride) {
     const int64_t t = i / cpt;
     const int64_t col = (i % cpt) * VE;
-    int ex[KM];
+    int ex[KM], rw[KM];
     float ds[KM];
     uint4 v[KM];
     const uint4 us = dxs ? ldg16(dxs + t * d + col) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      ex[j] = j < k && nr[j] >= 0 ? ne[j] : -1;  // -1: no slot, or a pair without a row
+      rw[j] = j < k ? nr[j] : -1;                           // -1: no row
+      ex[j] = j < k && ne[j] >= 0 && ne[j] < E ? ne[j] : -1;  // -1: no router term
       ds[j] = nd[j];
-      if (ex[j] >= 0) v[j] = ldg16(dxsort + (int64_t)nr[j] * d + col);
+      if (rw[j] >= 0) v[j] = ldg16(dxsort + (int64_t)rw[j] * d + col);
     }
     if (i + stride < n) index_ahead(i + stride);
     float acc[VE];
@@ -251,40 +255,41 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int q = 0; q < VE; ++q) acc[q] = 0.f;
     }
-#pragma unroll
-    for (int j = 0; j < KM; ++j) {
-      if (ex[j] >= 0) {
-        float fv[VE], fw[VE];
+    // slot j adds its row (when it has one), then its router term
+    auto add_slot = [&](int j) {
+      float fv[VE], fw[VE];
+      if (rw[j] >= 0) {
         cvt16<T>(v[j], fv);
+      } else {
+#pragma unroll
+        for (int q = 0; q < VE; ++q) fv[q] = 0.f;
+      }
+      if (ex[j] >= 0) {
         cvt16<T>(ldg16(wt + (int64_t)ex[j] * d + col), fw);
 #pragma unroll
         for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds[j], fw[q], fv[q]);
+      } else if (rw[j] >= 0) {
+#pragma unroll
+        for (int q = 0; q < VE; ++q) acc[q] += fv[q];
       }
-    }
+    };
+#pragma unroll
+    for (int j = 0; j < KM; ++j) add_slot(j);
     for (int j0 = KM; j0 < k; j0 += KM) {  // k > KM: further slots, in order
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
-        ex[j] = -1;
+        rw[j] = ex[j] = -1;
         if (j0 + j < k) {
           const int64_t p = t * k + j0 + j;
-          const int64_t r = __ldg(pairrow + p);
-          if (r >= 0) {
-            ex[j] = __ldg(idx + p);
-            ds[j] = __ldg(dsel + p);
-            v[j] = ldg16(dxsort + r * d + col);
-          }
+          const int e = __ldg(idx + p);
+          rw[j] = __ldg(pairrow + p);
+          ex[j] = e >= 0 && e < E ? e : -1;
+          ds[j] = __ldg(dsel + p);
+          if (rw[j] >= 0) v[j] = ldg16(dxsort + (int64_t)rw[j] * d + col);
         }
       }
 #pragma unroll
-      for (int j = 0; j < KM; ++j) {
-        if (ex[j] >= 0) {
-          float fv[VE], fw[VE];
-          cvt16<T>(v[j], fv);
-          cvt16<T>(ldg16(wt + (int64_t)ex[j] * d + col), fw);
-#pragma unroll
-          for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds[j], fw[q], fv[q]);
-        }
-      }
+      for (int j = 0; j < KM; ++j) add_slot(j);
     }
     st16<T>(dx + t * d + col, acc);
   }
@@ -328,7 +333,7 @@ void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const f
                kernel<<<blocks, kThreads, 0, s>>>(
                    p.topk_idx, dsel, reinterpret_cast<const T*>(wt), at<const T>(ws, L.dxsort),
                    at<const int32_t>(ws, L.pairrow), dxs, reinterpret_cast<T*>(p.dx), d.tokens,
-                   d.d_model, d.top_k));
+                   d.d_model, d.top_k, d.experts));
   };
   switch (slots_ahead(d.top_k)) {
     case 1: launch(router_dx_kernel<T, 1>); break;

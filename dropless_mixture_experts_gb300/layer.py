@@ -21,16 +21,19 @@ def _ptr(t):
 
 class MoELayer:
     """Buffers and calls for one (tokens, d_model, d_hidden, experts, top_k,
-    shared_hidden, dtype) problem on one CUDA device."""
+    shared_hidden, dtype) problem on one CUDA device.  capacity > 0 switches
+    on capacity routing (each expert keeps its first ``capacity`` pairs)."""
 
     def __init__(self, tokens, d_model, d_hidden, experts, top_k, shared_hidden=0, dtype="bf16",
-                 device="cuda", train=True):
+                 device="cuda", train=True, capacity=0):
         self.T, self.d, self.h, self.E, self.k, self.hs = (
             int(tokens), int(d_model), int(d_hidden), int(experts), int(top_k), int(shared_hidden))
         self.tdtype, cdt = _DT[dtype]
         self.dtype = dtype
         self.device = torch.device(device)
-        self.dims = abi.make_dims(self.T, self.d, self.h, self.E, self.k, self.hs, cdt)
+        self.capacity = int(capacity)
+        self.dims = abi.make_dims(self.T, self.d, self.h, self.E, self.k, self.hs, cdt,
+                                  self.capacity)
         self.mode = abi.MOE_SAVE_FOR_BWD if train else abi.MOE_FWD_ONLY
         self.ws_bytes = abi.moe_workspace_bytes(self.dims, self.mode)
         self.PP = abi.moe_padded_rows(self.dims)

@@ -34,6 +34,7 @@ class MoEConfig:
     shared_hidden: int = 0
     dtype: str = "bf16"          # "bf16" or "f32"
     name: str = field(default="", compare=False)
+    capacity: int = 0            # pairs per expert; 0 = dropless
 
     @property
     def pairs(self) -> int:

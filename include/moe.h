@@ -85,6 +85,10 @@ typedef struct {
   int32_t top_k;         /* k, 1..min(E, 32)                             */
   int32_t shared_hidden; /* hs, 0 = no shared expert, else multiple of 64 */
   int32_t dtype;         /* moe_dtype                                    */
+  int32_t capacity;      /* pairs an expert takes: 0 = dropless (every
+                            pair); C > 0 = capacity routing: each expert
+                            keeps its first C pairs in increasing pair id
+                            p = t*k + j and drops the rest               */
 } moe_dims;
 
 /* Static text for a status code. */
@@ -121,7 +125,14 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
  *   inv_perm [T*k]   int32 out: inv_perm[perm[r]] = r
  * Also writes the expert-padded row map and the tile list into the
  * workspace for the grouped calls.  Entries of topk_idx must lie in
- * [0, E) and be distinct per token. */
+ * [0, E) and be distinct per token.  With dims->capacity = C > 0 only the
+ * kept pairs (each expert's first C in increasing p) are sorted: counts and
+ * offsets count kept pairs, perm[r] = -1 for r >= offsets[E] and
+ * inv_perm[p] = -1 for a dropped pair.  A dropped pair adds nothing to y;
+ * the gates stay the softmax over all k selected logits, so the router
+ * gradient still reaches a dropped slot through its token's kept slots.
+ * An out-of-range index is reported (MOE_ERR_DEVICE_CHECK) and its pair is
+ * treated as dropped. */
 moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
@@ -196,7 +207,8 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes,
  * the library (a __device__ variable: every GPU that loads the library keeps
  * it until the process exits).  It is sized for (T*k / 512, rounded up) x E
  * <= 524288, e.g. up to 2^20 pairs with 256 experts or 2^22 pairs with 64;
- * larger problems return MOE_ERR_UNSUPPORTED before anything is launched.
+ * larger problems return MOE_ERR_UNSUPPORTED before anything is launched,
+ * and so does capacity routing (dims->capacity != 0): it sorts every pair.
  * It does not write the expert-padded tables the grouped calls read, so it
  * is not a substitute for moe_permute inside a layer invocation.
  *

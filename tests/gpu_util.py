@@ -42,7 +42,7 @@ def run_layer(cfg, seed_offset=0, train=True, inputs=None):
     inp = inputs if inputs is not None else make_inputs(cfg, seed_offset=seed_offset)
     dev = to_dev(inp, cfg.dtype)
     layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
-                     cfg.shared_hidden, cfg.dtype, train=train)
+                     cfg.shared_hidden, cfg.dtype, train=train, capacity=cfg.capacity)
     p = {k: dev[k] for k in params_of(inp)}
     res = {}
     if train:
@@ -71,7 +71,7 @@ def check_routing_bit_exact(res, cfg):
     assert np.array_equal(idx, res["idx"]), "top-k indices differ"
     g_err = np.max(np.abs(gates - res["gates"]) / np.abs(gates))
     assert g_err < 1e-6, g_err
-    counts, offsets, perm, inv = oracle.counting_sort(res["idx"], cfg.experts)
+    counts, offsets, perm, inv = oracle.counting_sort(res["idx"], cfg.experts, cfg.capacity)
     assert np.array_equal(counts, res["counts"])
     assert np.array_equal(offsets, res["offsets"])
     assert np.array_equal(perm, res["perm"])
@@ -82,9 +82,11 @@ def oracle_on_device_routing(inp, res, cfg, train=True):
     p = params_of(inp)
     if train:
         L, fwd, grads = oracle.train_step(inp["x"], p, cfg.top_k, inp["upstream"],
-                                          idx=res["idx"], logits=res["logits"])
+                                          idx=res["idx"], logits=res["logits"],
+                                          capacity=cfg.capacity)
         return L, fwd, grads
-    fwd = oracle.forward(inp["x"], p, cfg.top_k, idx=res["idx"], logits=res["logits"])
+    fwd = oracle.forward(inp["x"], p, cfg.top_k, idx=res["idx"], logits=res["logits"],
+                         capacity=cfg.capacity)
     return None, fwd, None
 
 

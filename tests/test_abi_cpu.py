@@ -52,7 +52,8 @@ def test_workspace_and_padded_rows(lib):
 
 @pytest.mark.parametrize("field,value", [("tokens", -1), ("experts", 0), ("experts", 257),
                                           ("top_k", 0), ("top_k", 9), ("d_model", 0),
-                                          ("dtype", 7), ("shared_hidden", -64)])
+                                          ("dtype", 7), ("shared_hidden", -64),
+                                          ("capacity", -1)])
 def test_invalid_dims_rejected(lib, field, value):
     d = abi.make_dims(64, 128, 128, 8, 2, 0, abi.MOE_F32)
     setattr(d, field, value)
@@ -116,3 +117,9 @@ def test_misaligned_row_data_rejected(lib):
     ptrs[15] = 0x3002  # dx
     assert abi.moe_backward(d, *ptrs[:15], *ptrs[15:23], 0x1000, need_t, None,
                             check=False) == abi.MOE_ERR_INVALID_ARG
+
+
+def test_capacity_routing_is_refused_by_the_allocation_free_sort(lib):
+    d = abi.make_dims(64, 128, 128, 8, 2, 0, abi.MOE_BF16, capacity=8)
+    assert abi.moe_permute_noalloc(d, 256, 256, 256, 256, 256, None,
+                                   check=False) == abi.MOE_ERR_UNSUPPORTED

@@ -27,6 +27,12 @@ SMALL = [
     MoEConfig(300, 192, 64, 32, 32, 64, "bf16", "bf16_k32_shared"),
     MoEConfig(200, 64, 64, 32, 32, 0, "f32", "f32_k32"),
     MoEConfig(333, 640, 128, 8, 2, 0, "bf16", "bf16_d640"),
+    # capacity routing: about half the pairs dropped; with a shared expert;
+    # float32; one pair per expert
+    MoEConfig(2000, 128, 128, 8, 2, 0, "bf16", "bf16_capacity_half", capacity=250),
+    MoEConfig(1500, 128, 64, 16, 4, 128, "bf16", "bf16_capacity_shared", capacity=300),
+    MoEConfig(700, 64, 64, 4, 2, 0, "f32", "f32_capacity", capacity=200),
+    MoEConfig(300, 128, 64, 8, 2, 0, "bf16", "bf16_capacity_1", capacity=1),
 ]
 
 
