@@ -246,7 +246,8 @@ def main():
     abi.load()
     td = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     inputs = make_inputs(cfg, seed_offset=100 * rank)
-    host = {k: (None if v is None else torch.from_numpy(v).to(td).pin_memory())
+    host = {k: (None if v is None else
+                torch.from_numpy(v).to(torch.float32 if k == "router_bias" else td).pin_memory())
             for k, v in inputs.items()}
     dev = {k: (None if v is None else v.to("cuda", non_blocking=True)) for k, v in host.items()}
     p = {k: dev[k] for k in params_of(inputs)}

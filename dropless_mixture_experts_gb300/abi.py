@@ -60,7 +60,7 @@ _SIGS = {
     "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "moe_workspace_bytes": ([_D, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "moe_padded_rows": ([_D, ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
-    "moe_route": ([_D, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
+    "moe_route": ([_D, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_permute": ([_D, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_grouped_ffn_fwd": ([_D, ctypes.c_int] + [_P] * 9 + [_S, _P], ctypes.c_int),
     "moe_combine": ([_D, ctypes.c_int] + [_P] * 11 + [_S, _P], ctypes.c_int),
@@ -123,9 +123,9 @@ def moe_padded_rows(dims: moe_dims) -> int:
 
 
 def moe_route(dims, x, w_router, logits_in, logits_out, topk_idx, gates, ws, ws_bytes, stream,
-              check=True):
-    s = load().moe_route(ctypes.byref(dims), _p(x), _p(w_router), _p(logits_in), _p(logits_out),
-                         _p(topk_idx), _p(gates), _p(ws), ws_bytes, _p(stream))
+              check=True, router_bias=None):
+    s = load().moe_route(ctypes.byref(dims), _p(x), _p(w_router), _p(router_bias), _p(logits_in),
+                         _p(logits_out), _p(topk_idx), _p(gates), _p(ws), ws_bytes, _p(stream))
     if check:
         _check(s, "moe_route")
     return s

@@ -82,8 +82,9 @@ moe_status moe_padded_rows(const moe_dims* dims, int64_t* rows) {
 }
 
 moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
-                     const float* logits_in, float* logits_out, int32_t* topk_idx, float* gates,
-                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                     const float* router_bias, const float* logits_in, float* logits_out,
+                     int32_t* topk_idx, float* gates, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
   if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
   if (dims->tokens > 0) {
     if (!topk_idx || !gates) return MOE_ERR_INVALID_ARG;
@@ -99,19 +100,21 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
   const float* logits = logits_in;
   if (!logits_in) {
     if (tc_router_supported(*dims)) {
-      if (!tc_router(*dims, L, x, w_router, logits_out, topk_idx, gates, workspace, stream))
+      if (!tc_router(*dims, L, x, w_router, router_bias, logits_out, topk_idx, gates, workspace,
+                     stream))
         return MOE_ERR_CUDA;
       return cuda_status();
     }
     if (router_fused_supported(*dims)) {
       // router GEMM, selection and softmax in one pass over x
-      launch_router_fused(*dims, x, w_router, logits_out, topk_idx, gates, stream);
+      launch_router_fused(*dims, x, w_router, router_bias, logits_out, topk_idx, gates, stream);
       return cuda_status();
     }
     float* dst = logits_out ? logits_out : at<float>(workspace, L.logits);
     LayerPtrs p;
     p.x = x;
     p.w_router = w_router;
+    p.router_bias = router_bias;
     simt_router_logits(*dims, p, dst, stream);
     logits = dst;
   } else if (logits_out && logits_out != logits_in) {

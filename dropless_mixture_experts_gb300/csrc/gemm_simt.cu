@@ -55,6 +55,7 @@ struct SimtArgs {
   int dg_ld = 0;
   void* slot_out = nullptr;      // DOWN / DX: one row per sorted (or dense) row
   float* acc_out = nullptr;      // LOGITS / DWD / DWGU (gate half)
+  const float* col_bias = nullptr;  // LOGITS: router bias [N], nullable
   float* acc_out2 = nullptr;     // DWGU (up half)
   int ldo = 0;
   int n_ntiles = 1, n_mtiles = 1;
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int n = n0 + tx * 4 + j;
-          if (n < a.N) a.acc_out[r * a.ldo + n] = acc[i][j];
+          if (n < a.N) a.acc_out[r * a.ldo + n] = acc[i][j] + (a.col_bias ? a.col_bias[n] : 0.f);
         }
     } else if constexpr (KIND == GU) {
       if (!ROUTED && r >= a.rows) continue;
@@ -371,6 +372,7 @@ void router_logits_t(const moe_dims& d, const LayerPtrs& p, float* logits, cudaS
   a.K = d.d_model;
   a.rows = d.tokens;
   a.acc_out = logits;
+  a.col_bias = p.router_bias;
   a.ldo = d.experts;
   a.n_ntiles = (d.experts + BN - 1) / BN;
   launch<LOGITS, T, false>(a, a.n_ntiles * ((d.tokens + BM - 1) / BM), s);

@@ -68,7 +68,7 @@ struct Params {
   int brow_stride = 0;              // rows of a B weight matrix per expert (0: activations)
   int M = 0, N = 0;                 // DW output dims / row-kind output columns
   // epilogue
-  const float* gates = nullptr;
+  const float* gates = nullptr;     // routed DOWN / DZ: pair gates; router: logit offsets [E]
   int save = 0;                     // GU: also store a_g, a_u
   void* out0 = nullptr;             // router: top-k indices [T, k]
   void* out1 = nullptr;             // router: gates [T, k]
@@ -602,6 +602,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) lg[32 * c + i] = __uint_as_float(v[i]);
           }
           const int E = p.N, k = p.top_k;
+          if (p.gates) {  // the router bias (a fixed offset per expert)
+#pragma unroll
+            for (int e = 0; e < C::BN; ++e)
+              if (e < E) lg[e] += __ldg(p.gates + e);
+          }
           if (row < tl.nvalid) {
             const int64_t t = (int64_t)tl.row0 + row;
             if (p.facc) {

@@ -27,8 +27,8 @@ void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, i
 void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
                          float* gates, cudaStream_t s);
 bool router_fused_supported(const moe_dims& d);
-void launch_router_fused(const moe_dims& d, const void* x, const void* w, float* logits_out,
-                         int32_t* idx, float* gates, cudaStream_t s);
+void launch_router_fused(const moe_dims& d, const void* x, const void* w, const float* bias,
+                         float* logits_out, int32_t* idx, float* gates, cudaStream_t s);
 void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv_perm, void* ws,
                     cudaStream_t s);
@@ -39,6 +39,7 @@ struct LayerPtrs {
   const void* x = nullptr;
   const void* dy = nullptr;
   const void* w_router = nullptr;
+  const float* router_bias = nullptr;  // [E] f32 routing offset, nullable
   const void* w_gate = nullptr;
   const void* w_up = nullptr;
   const void* w_down = nullptr;
@@ -91,7 +92,8 @@ bool tc_router_dw(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* 
 // router GEMM + top-k + softmax on the tensor cores (bf16, E a multiple of 8, <= 64)
 bool tc_router_supported(const moe_dims& d);
 bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_router,
-               float* logits_out, int32_t* idx, float* gates, void* ws, cudaStream_t s);
+               const float* bias, float* logits_out, int32_t* idx, float* gates, void* ws,
+               cudaStream_t s);
 
 // row streams (stream.cu)
 // expert-sorted copy of token rows: out[pairrow[t*k + j]] = src[t], padding

@@ -99,6 +99,7 @@ void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* 
 template <typename T, int EN>
 __global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__ x,
                                                            const T* __restrict__ w_router,
+                                                           const float* __restrict__ bias,
                                                            int64_t Tn, int d, int k,
                                                            float* __restrict__ logits_out,
                                                            int32_t* __restrict__ idx_out,
@@ -144,6 +145,10 @@ __global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__
         }
       }
     }
+    if (bias) {
+#pragma unroll
+      for (int e = 0; e < EN; ++e) acc[e] += __ldg(bias + e);
+    }
     if (logits_out) {
       float4* lo = reinterpret_cast<float4*>(logits_out + t * EN);
 #pragma unroll
@@ -175,8 +180,8 @@ __global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__
 }
 
 template <typename T, int EN>
-static void router_fused_t(const moe_dims& dm, const void* x, const void* w, float* logits_out,
-                           int32_t* idx, float* gates, cudaStream_t s) {
+static void router_fused_t(const moe_dims& dm, const void* x, const void* w, const float* bias,
+                           float* logits_out, int32_t* idx, float* gates, cudaStream_t s) {
   const size_t smem = sizeof(float) * dm.d_model * EN;
   static bool attr = false;
   if (!attr) {
@@ -189,7 +194,7 @@ static void router_fused_t(const moe_dims& dm, const void* x, const void* w, flo
   if (blocks > cap) blocks = cap;
   MOE_LAUNCH("router_fused", s,
              (router_fused_kernel<T, EN><<<(unsigned)blocks, 128, smem, s>>>(
-                 reinterpret_cast<const T*>(x), reinterpret_cast<const T*>(w), dm.tokens,
+                 reinterpret_cast<const T*>(x), reinterpret_cast<const T*>(w), bias, dm.tokens,
                  dm.d_model, dm.top_k, logits_out, idx, gates)));
 }
 
@@ -199,26 +204,26 @@ bool router_fused_supported(const moe_dims& d) {
          (size_t)d.d_model * E * sizeof(float) <= 160 * 1024;
 }
 
-void launch_router_fused(const moe_dims& d, const void* x, const void* w, float* logits_out,
-                         int32_t* idx, float* gates, cudaStream_t s) {
+void launch_router_fused(const moe_dims& d, const void* x, const void* w, const float* bias,
+                         float* logits_out, int32_t* idx, float* gates, cudaStream_t s) {
   if (d.tokens == 0) return;
   const bool bf = d.dtype == MOE_BF16;
   switch (d.experts) {
     case 8:
-      bf ? router_fused_t<__nv_bfloat16, 8>(d, x, w, logits_out, idx, gates, s)
-         : router_fused_t<float, 8>(d, x, w, logits_out, idx, gates, s);
+      bf ? router_fused_t<__nv_bfloat16, 8>(d, x, w, bias, logits_out, idx, gates, s)
+         : router_fused_t<float, 8>(d, x, w, bias, logits_out, idx, gates, s);
       break;
     case 16:
-      bf ? router_fused_t<__nv_bfloat16, 16>(d, x, w, logits_out, idx, gates, s)
-         : router_fused_t<float, 16>(d, x, w, logits_out, idx, gates, s);
+      bf ? router_fused_t<__nv_bfloat16, 16>(d, x, w, bias, logits_out, idx, gates, s)
+         : router_fused_t<float, 16>(d, x, w, bias, logits_out, idx, gates, s);
       break;
     case 32:
-      bf ? router_fused_t<__nv_bfloat16, 32>(d, x, w, logits_out, idx, gates, s)
-         : router_fused_t<float, 32>(d, x, w, logits_out, idx, gates, s);
+      bf ? router_fused_t<__nv_bfloat16, 32>(d, x, w, bias, logits_out, idx, gates, s)
+         : router_fused_t<float, 32>(d, x, w, bias, logits_out, idx, gates, s);
       break;
     default:
-      bf ? router_fused_t<__nv_bfloat16, 64>(d, x, w, logits_out, idx, gates, s)
-         : router_fused_t<float, 64>(d, x, w, logits_out, idx, gates, s);
+      bf ? router_fused_t<__nv_bfloat16, 64>(d, x, w, bias, logits_out, idx, gates, s)
+         : router_fused_t<float, 64>(d, x, w, bias, logits_out, idx, gates, s);
       break;
   }
 }

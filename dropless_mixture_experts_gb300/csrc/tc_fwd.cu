@@ -115,7 +115,8 @@ bool tc_router_supported(const moe_dims& d) {
 // tile of 64 columns, the columns past E read as zero), top-k and softmax in
 // the epilogue
 bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_router,
-               float* logits_out, int32_t* idx, float* gates, void* ws, cudaStream_t s) {
+               const float* bias, float* logits_out, int32_t* idx, float* gates, void* ws,
+               cudaStream_t s) {
   Maps mp;
   Params q;
   q.status = at<int>(ws, L.status);
@@ -131,6 +132,7 @@ bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_
   q.out0 = idx;
   q.out1 = gates;
   q.facc = logits_out;
+  q.gates = bias;  // the router's epilogue reads this as its logit offsets
   launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_ROUTER, 64, false>>(mp, q, q.n_mt, "tc_router", s);
   return true;
 }

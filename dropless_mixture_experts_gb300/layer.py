@@ -73,9 +73,10 @@ class MoELayer:
     def _stream(self):
         return torch.cuda.current_stream(self.device).cuda_stream
 
-    def route(self, x, w_router, logits_in=None):
+    def route(self, x, w_router, logits_in=None, router_bias=None):
         abi.moe_route(self.dims, _ptr(x), _ptr(w_router), _ptr(logits_in), _ptr(self.logits),
-                      _ptr(self.idx), _ptr(self.gates), self.ws_ptr, self.ws_bytes, self._stream())
+                      _ptr(self.idx), _ptr(self.gates), self.ws_ptr, self.ws_bytes, self._stream(),
+                      router_bias=_ptr(router_bias))
 
     def permute(self):
         abi.moe_permute(self.dims, _ptr(self.idx), _ptr(self.counts), _ptr(self.offsets),
@@ -110,7 +111,7 @@ class MoELayer:
     # -- composed passes ---------------------------------------------------
     def forward(self, x, p, logits_in=None):
         """y = layer(x); returns the output buffer (valid until the next call)."""
-        self.route(x, p["w_router"], logits_in)
+        self.route(x, p["w_router"], logits_in, p.get("router_bias"))
         self.permute()
         self.grouped_ffn_fwd(x, p, abi.MOE_FWD_ONLY)
         self.combine(x, p, abi.MOE_FWD_ONLY)
@@ -121,7 +122,7 @@ class MoELayer:
         dx, grads dict); all are the layer's buffers."""
         if self.mode != abi.MOE_SAVE_FOR_BWD:
             raise RuntimeError("layer was built with train=False")
-        self.route(x, p["w_router"], logits_in)
+        self.route(x, p["w_router"], logits_in, p.get("router_bias"))
         self.permute()
         self.grouped_ffn_fwd(x, p, abi.MOE_SAVE_FOR_BWD)
         self.combine(x, p, abi.MOE_SAVE_FOR_BWD, upstream=dy)

@@ -35,6 +35,7 @@ class MoEConfig:
     dtype: str = "bf16"          # "bf16" or "f32"
     name: str = field(default="", compare=False)
     capacity: int = 0            # pairs per expert; 0 = dropless
+    skew: float = 0.0            # router bias ramp (0 = no bias: uniform routing)
 
     @property
     def pairs(self) -> int:
@@ -78,7 +79,11 @@ def _normal(seed: int, shape, std: float) -> np.ndarray:
 def make_inputs(cfg: MoEConfig, seed_offset: int = 0, with_upstream: bool = True) -> dict:
     """All tensors of one layer invocation as float32 numpy arrays (bfloat16
     exact when cfg.dtype == "bf16").  Keys: x, w_router, w_gate, w_up, w_down,
-    ws_gate, ws_up, ws_down (None without a shared expert), upstream."""
+    ws_gate, ws_up, ws_down (None without a shared expert), upstream, and
+    router_bias: None at skew 0, else the float32 ramp
+    b_e = skew * 4 * (E - 1 - 2e) / (E - 1), +4 skew logit standard deviations
+    on expert 0 down to -4 skew on expert E-1 (the logits x W_r have unit
+    variance here), which skews the routing towards the low experts."""
     T, d, h, E, hs = cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.shared_hidden
     s = seed_offset
     out = {
@@ -98,10 +103,14 @@ def make_inputs(cfg: MoEConfig, seed_offset: int = 0, with_upstream: bool = True
         for k, v in list(out.items()):
             if v is not None:
                 out[k] = bf16_round(v)
+    out["router_bias"] = None
+    if cfg.skew and E > 1:
+        ramp = (E - 1 - 2 * np.arange(E, dtype=np.float64)) / (E - 1)
+        out["router_bias"] = (cfg.skew * 4.0 * ramp).astype(np.float32)
     return out
 
 
 def params_of(inputs: dict) -> dict:
     """The parameter subset of ``make_inputs``'s result."""
-    keys = ("w_router", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down")
+    keys = ("w_router", "w_gate", "w_up", "w_down", "ws_gate", "ws_up", "ws_down", "router_bias")
     return {k: inputs[k] for k in keys}

@@ -102,10 +102,14 @@ moe_status moe_workspace_bytes(const moe_dims* dims, int mode, size_t* bytes);
  * T*k + E*127 rounded up to 128. */
 moe_status moe_padded_rows(const moe_dims* dims, int64_t* rows);
 
-/* Router: logits = x W_r (float32 accumulate), then per token the top-k
- * experts (ties to the lower index, descending slots) and the softmax of
- * the selected logits.
+/* Router: logits = x W_r (+ router_bias) (float32 accumulate), then per
+ * token the top-k experts (ties to the lower index, descending slots) and
+ * the softmax of the selected logits.
  *   x          [T, d]  (dtype)            w_router [d, E] (dtype)
+ *   router_bias [E]    f32, nullable: a fixed per-expert offset added to the
+ *              computed logits (it skews the routing; the layer trains no
+ *              bias, so moe_backward returns no gradient for it); ignored
+ *              with logits_in
  *   logits_in  [T, E]  f32, nullable: when given, the GEMM is skipped and
  *              the selection is made on these logits (fed-logits mode;
  *              x and w_router may then be NULL)
@@ -113,8 +117,8 @@ moe_status moe_padded_rows(const moe_dims* dims, int64_t* rows);
  *   topk_idx   [T, k]  int32 out          gates [T, k] f32 out
  * Logits must be finite (a NaN makes the selection unspecified). */
 moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
-                     const float* logits_in, float* logits_out, int32_t* topk_idx,
-                     float* gates, void* workspace, size_t workspace_bytes,
+                     const float* router_bias, const float* logits_in, float* logits_out,
+                     int32_t* topk_idx, float* gates, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream);
 
 /* Counting sort of the T*k pairs p = t*k + j by expert topk_idx[p],

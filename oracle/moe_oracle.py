@@ -70,9 +70,12 @@ def param_count(d_model: int, d_hidden: int, experts: int, shared_hidden: int = 
     return experts * 3 * d_model * d_hidden + d_model * experts + 3 * d_model * shared_hidden
 
 
-def router_logits(x, w_router):
-    """logits[t, e] = sum_i x[t, i] * W_r[i, e]  (the ``route`` piece)."""
-    return _f64(x) @ _f64(w_router)
+def router_logits(x, w_router, router_bias=None):
+    """logits[t, e] = sum_i x[t, i] * W_r[i, e]  (the ``route`` piece), plus
+    an optional fixed per-expert offset (the skewed-routing runs; the layer
+    trains no bias)."""
+    logits = _f64(x) @ _f64(w_router)
+    return logits if router_bias is None else logits + _f64(router_bias)[None, :]
 
 
 def route_from_logits(logits, top_k: int):
@@ -187,7 +190,7 @@ def forward(x, params, top_k: int, idx=None, logits=None, capacity=None):
     w_gate = _f64(params["w_gate"])
     E = w_gate.shape[0]
     if logits is None:
-        logits = router_logits(x, params["w_router"])
+        logits = router_logits(x, params["w_router"], params.get("router_bias"))
     logits = _f64(logits)
     if idx is None:
         idx, gates = route_from_logits(logits, top_k)
@@ -238,7 +241,7 @@ def dense_masked_forward(x, params, top_k: int, idx=None, capacity=None):
     x = _f64(x)
     T, _ = x.shape
     E = _f64(params["w_gate"]).shape[0]
-    logits = router_logits(x, params["w_router"])
+    logits = router_logits(x, params["w_router"], params.get("router_bias"))
     if idx is None:
         idx, gates = route_from_logits(logits, top_k)
     else:

@@ -29,7 +29,9 @@ def to_dev(inp, dtype):
     td = torch.bfloat16 if dtype == "bf16" else torch.float32
     out = {}
     for k, v in inp.items():
-        out[k] = None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to("cuda").to(td)
+        # the router bias is float32 for either storage type
+        kd = torch.float32 if k == "router_bias" else td
+        out[k] = None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to("cuda").to(kd)
     return out
 
 
@@ -97,7 +99,7 @@ def compare_layer(inp, res, cfg, train=True):
     """Returns {name: rel_err} for every output of the forward / train step."""
     L, fwd, grads = oracle_on_device_routing(inp, res, cfg, train)
     errs = {"y": rel_err(res["y"], fwd["y"])}
-    logits_ref = oracle.router_logits(inp["x"], inp["w_router"])
+    logits_ref = oracle.router_logits(inp["x"], inp["w_router"], inp.get("router_bias"))
     errs["logits"] = rel_err(res["logits"], logits_ref)
     if train:
         errs["loss"] = abs(res["loss"] - L) / max(1e-30, float(np.sum(np.abs(fwd["y"] * inp["upstream"]))))

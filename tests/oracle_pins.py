@@ -122,9 +122,11 @@ def torch_dense_layer(x, params, k, idx=None, capacity=None):
     pairs are masked out of the mixture, not out of the softmax).  Returns
     (y, {name: tensor}) with the tensors requiring grad."""
     t = {kk: (None if v is None else torch.tensor(np.asarray(v, np.float64), requires_grad=True))
-         for kk, v in params.items()}
+         for kk, v in params.items() if kk != "router_bias"}
     tx = torch.tensor(np.asarray(x, np.float64), requires_grad=True)
     logits = tx @ t["w_router"]
+    if params.get("router_bias") is not None:  # a constant offset: no gradient
+        logits = logits + torch.tensor(np.asarray(params["router_bias"], np.float64))
     if idx is None:
         sel, sel_idx = torch.topk(logits, k, dim=1)
     else:

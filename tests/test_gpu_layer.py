@@ -33,6 +33,12 @@ SMALL = [
     MoEConfig(1500, 128, 64, 16, 4, 128, "bf16", "bf16_capacity_shared", capacity=300),
     MoEConfig(700, 64, 64, 4, 2, 0, "f32", "f32_capacity", capacity=200),
     MoEConfig(300, 128, 64, 8, 2, 0, "bf16", "bf16_capacity_1", capacity=1),
+    # skewed routing (router bias ramp): a few hot experts, many empty ones
+    # at E=64; and skew with a capacity
+    MoEConfig(2000, 128, 128, 8, 2, 0, "bf16", "bf16_skew", skew=0.9),
+    MoEConfig(2050, 256, 128, 64, 8, 256, "bf16", "bf16_decoder_skew", skew=0.9),
+    MoEConfig(1000, 128, 64, 8, 2, 0, "f32", "f32_skew", skew=0.9),
+    MoEConfig(2000, 128, 128, 8, 2, 0, "bf16", "bf16_skew_capacity", capacity=250, skew=0.9),
 ]
 
 

@@ -57,3 +57,21 @@ def test_fully_dropped_token_keeps_only_the_shared_expert():
     assert np.all(grads["dgate"][1:] == 0.0)
     assert np.any(grads["dlogits"][0] != 0.0)
     assert np.all(grads["dlogits"][1:] == 0.0)
+
+
+def test_router_bias_offsets_the_logits_and_trains_no_bias():
+    from oracle_pins import autograd_discrepancy
+    x, p, G = tiny_problem(T=13, d=8, h=12, E=4, k=2, hs=5, seed=3)
+    # no bias and a zero bias give the same step
+    L0, f0, g0 = oracle.train_step(x, p, 2, G)
+    pz = dict(p, router_bias=np.zeros(4))
+    L1, f1, g1 = oracle.train_step(x, pz, 2, G)
+    assert L0 == L1 and all(np.array_equal(g0[k], g1[k]) for k in g0)
+    # a bias far above every logit puts its expert in every token's first slot
+    pb = dict(p, router_bias=np.array([0.0, 0.0, 50.0, 0.0]))
+    fwd = oracle.forward(x, pb, 2)
+    assert np.all(fwd["idx"][:, 0] == 2)
+    # value and gradients agree with torch autograd with the offset held constant
+    pr = dict(p, router_bias=np.array([0.3, -0.2, 0.1, -0.4]))
+    assert autograd_discrepancy(oracle, x, pr, 2, G) < 1e-9
+    assert autograd_discrepancy(oracle, x, pr, 2, G, capacity=4) < 1e-9
