@@ -39,17 +39,58 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skew", type=float, default=0.0,
+                    help="router bias ramp: skew * 4 logit std from expert 0 down to expert E-1")
+    ap.add_argument("--capacity-factor", type=float, default=0.0,
+                    help="capacity routing: each expert keeps ceil(F * T * k / E) pairs (0: dropless)")
+    ap.add_argument("--sweep", default="", choices=["", "maxtok"],
+                    help="maxtok: the largest train-step token count that fits in free HBM")
     return ap.parse_args()
+
+
+def with_routing(cfg, args):
+    """The workload with the command line's skew and capacity."""
+    import dataclasses
+    import math
+    cap = 0
+    if args.capacity_factor > 0:
+        cap = math.ceil(args.capacity_factor * cfg.tokens * cfg.top_k / cfg.experts)
+    return dataclasses.replace(cfg, skew=args.skew, capacity=cap)
+
+
+# Kernel names of each piece of the pages' pieces suite (route, sort_permute,
+# experts_grouped_swiglu, unpermute_combine); the rest of a train step is
+# the backward.
+PIECES = {
+    "route": ("tc_router", "router_fused", "topk_softmax", "simt_logits"),
+    "sort_permute": ("perm_hist", "perm_colscan", "perm_finalize", "perm_scatter", "zero_fill"),
+    "experts": ("scatter_rows", "tc_gateup", "tc_gateup_sh", "tc_down", "tc_down_sh",
+                "simt_gateup", "simt_gateup_sh", "simt_down", "simt_down_sh"),
+    "combine": ("combine", "loss_reduce"),
+}
+
+
+def pieces_of(fwd_rec, train_rec, steps):
+    """ms per step of each piece: the forward's pieces from a forward-only
+    record, the backward as the train step's remainder."""
+    def total(rec, names=None):
+        return sum(t for n, (_, t) in rec.items() if names is None or n in names) / steps
+    out = {k: total(fwd_rec, v) for k, v in PIECES.items()}
+    out["forward_total"] = total(fwd_rec)
+    out["backward"] = total(train_rec) - out["forward_total"]
+    out["train_total"] = total(train_rec)
+    return out
 
 
 # ---------------------------------------------------------------------------
 # algorithmic work per step
 # ---------------------------------------------------------------------------
-def step_flops(cfg):
+def step_flops(cfg, kept_frac=1.0):
     """Algorithmic FLOPs of one forward and one train step (router, routed
-    and shared SwiGLU experts; the backward is twice the forward)."""
+    and shared SwiGLU experts; the backward is twice the forward).  With
+    capacity routing the routed experts count the kept pairs only."""
     T, d, h, E, k, hs = cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k, cfg.shared_hidden
-    fwd = T * (2 * d * E + k * 6 * d * h + 6 * d * hs)
+    fwd = T * (2 * d * E + kept_frac * k * 6 * d * h + 6 * d * hs)
     return fwd, 3 * fwd
 
 
@@ -170,8 +211,10 @@ def oracle_tokens_per_s(cfg, inputs, target_s=10.0, max_tokens=None):
     S = min(cfg.tokens, 1024)
     cap = cfg.tokens if max_tokens is None else min(cfg.tokens, max_tokens)
     while True:
+        # capacity scales with the sample: the same share of each expert kept
+        c_s = -(-cfg.capacity * S // cfg.tokens) if cfg.capacity else None
         t0 = time.perf_counter()
-        oracle.train_step(inputs["x"][:S], p, cfg.top_k, inputs["upstream"][:S])
+        oracle.train_step(inputs["x"][:S], p, cfg.top_k, inputs["upstream"][:S], capacity=c_s)
         dt = time.perf_counter() - t0
         if dt >= target_s * 0.5 or S >= cap:
             return S / dt, S, dt
@@ -188,12 +231,13 @@ def reference_arm(args, cfg):
     inputs = make_inputs(cfg)
     p = params_of(inputs)
     S = min(cfg.tokens, 1024)
+    c_s = -(-cfg.capacity * S // cfg.tokens) if cfg.capacity else None  # same kept share
     for _ in range(args.warmup):
-        oracle.train_step(inputs["x"][:S], p, cfg.top_k, inputs["upstream"][:S])
+        oracle.train_step(inputs["x"][:S], p, cfg.top_k, inputs["upstream"][:S], capacity=c_s)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.train_step(inputs["x"][:S], p, cfg.top_k, inputs["upstream"][:S])
+        oracle.train_step(inputs["x"][:S], p, cfg.top_k, inputs["upstream"][:S], capacity=c_s)
         times.append(time.perf_counter() - t0)
     ms = 1e3 * sum(times) / len(times)
     v = S / (ms / 1e3)
@@ -204,10 +248,115 @@ def reference_arm(args, cfg):
         "data": "synthetic",
         "config": {"workload": cfg.name, "tokens": cfg.tokens, "d_model": cfg.d_model,
                    "d_hidden": cfg.d_hidden, "experts": cfg.experts, "top_k": cfg.top_k,
-                   "shared_hidden": cfg.shared_hidden, "storage": cfg.dtype},
+                   "shared_hidden": cfg.shared_hidden, "storage": cfg.dtype,
+                   "routing": {"skew": cfg.skew, "capacity": cfg.capacity}},
         "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": f"train step on the first {S} of {cfg.tokens} tokens per step"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# maximum tokens of one train step (the pages' maxtok suite)
+# ---------------------------------------------------------------------------
+def layer_device_bytes(cfg, tokens):
+    """Device bytes of one train-step invocation at ``tokens``: the layer's
+    buffers and workspace as the library sizes them (counted on torch's meta
+    device, nothing allocated), the token inputs, the weights and their
+    gradients' inputs."""
+    import torch
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    L = MoELayer(tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k, cfg.shared_hidden,
+                 cfg.dtype, device="meta", train=True, capacity=cfg.capacity)
+    b = 0
+    for v in vars(L).values():
+        if isinstance(v, torch.Tensor):
+            b += v.nbytes
+        elif isinstance(v, dict):
+            b += sum(x.nbytes for x in v.values() if isinstance(x, torch.Tensor))
+    el = 2 if cfg.dtype == "bf16" else 4
+    d, h, E, hs = cfg.d_model, cfg.d_hidden, cfg.experts, cfg.shared_hidden
+    b += 2 * tokens * d * el                        # x and the upstream gradient
+    b += (d * E + 3 * E * d * h + 3 * d * hs) * el  # weights
+    return b
+
+
+def maxtok_sweep(args, cfg):
+    """Largest train-step token count that fits in the free HBM of this GPU,
+    by the library's own sizes (a doubling then bisection search on
+    ``layer_device_bytes``), bounded by the C ABI's index range; then one
+    real train step at that size is run and timed to show it fits."""
+    import dataclasses
+    import torch
+    from dropless_mixture_experts_gb300 import abi
+    from dropless_mixture_experts_gb300.layer import MoELayer
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    abi.load()
+    free, total = torch.cuda.mem_get_info()
+    budget = int(free * 0.92)  # room for the allocator's rounding and the context
+
+    def abi_ok(T):
+        return T <= (1 << 31) // 64 and T * cfg.top_k + cfg.experts * 256 < (1 << 31)
+
+    def fits(T):
+        return abi_ok(T) and layer_device_bytes(cfg, T) <= budget
+
+    lo = 1024
+    hi = lo
+    while fits(hi * 2):
+        hi *= 2
+    lo, hi = hi, hi * 2
+    while hi - lo > 1024:
+        mid = (lo + hi) // 2 // 1024 * 1024
+        lo, hi = (mid, hi) if fits(mid) else (lo, mid)
+    T = lo
+    binding = "memory" if abi_ok(hi) else "index range"
+
+    # one real step at that size, inputs drawn on the device (seeded)
+    td = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    d, h, E, hs = cfg.d_model, cfg.d_hidden, cfg.experts, cfg.shared_hidden
+    g = torch.Generator(device="cuda")
+
+    def normal(seed, shape, std):
+        g.manual_seed(seed)
+        return (torch.randn(shape, generator=g, device="cuda", dtype=torch.float32) * std).to(td)
+
+    p = {"w_router": normal(1, (d, E), d ** -0.5), "w_gate": normal(2, (E, d, h), d ** -0.5),
+         "w_up": normal(3, (E, d, h), d ** -0.5), "w_down": normal(4, (E, h, d), h ** -0.5),
+         "ws_gate": None, "ws_up": None, "ws_down": None}
+    if hs:
+        p.update(ws_gate=normal(5, (d, hs), d ** -0.5), ws_up=normal(6, (d, hs), d ** -0.5),
+                 ws_down=normal(7, (hs, d), hs ** -0.5))
+    x = normal(0, (T, d), 1.0)
+    G = normal(8, (T, d), 1.0)
+    layer = MoELayer(T, d, h, E, cfg.top_k, hs, cfg.dtype, train=True, capacity=cfg.capacity)
+    for _ in range(2):
+        layer.train_step(x, p, G)
+    torch.cuda.synchronize()
+    st, _ = layer.device_status()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(3)]
+    for a, b in evs:
+        a.record()
+        layer.train_step(x, p, G)
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    line = {
+        "metric": "max train-step tokens in HBM", "value": T, "unit": "tokens", "n_gpus": 1,
+        "higher_is_better": True, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (drawn on the device)",
+        "config": {"workload": cfg.name, "d_model": d, "d_hidden": h, "experts": E,
+                   "top_k": cfg.top_k, "shared_hidden": hs, "step": "train (value_and_grad)"},
+        "binding": binding, "device_bytes": layer_device_bytes(cfg, T),
+        # the pages' maxtok rows give peak MB per doubling of the tokens
+        "ladder_mb": {str(t): layer_device_bytes(cfg, t) / 2 ** 20
+                      for t in (131072 << i for i in range(12)) if t <= T},
+        "bytes_per_token": layer_device_bytes(cfg, T) / T, "free_bytes": free,
+        "total_bytes": total, "peak_allocated": torch.cuda.max_memory_allocated(),
+        "device_status": st, "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
     }
     print(json.dumps(line), flush=True)
 
@@ -219,9 +368,12 @@ def main():
     args = parse()
     from dropless_mixture_experts_gb300.synthetic import CONFIGS
 
-    cfg = CONFIGS[args.config]
+    cfg = with_routing(CONFIGS[args.config], args)
     if args.impl == "reference":
         reference_arm(args, cfg)
+        return
+    if args.sweep == "maxtok":
+        maxtok_sweep(args, cfg)
         return
 
     import numpy as np
@@ -252,7 +404,7 @@ def main():
     dev = {k: (None if v is None else v.to("cuda", non_blocking=True)) for k, v in host.items()}
     p = {k: dev[k] for k in params_of(inputs)}
     layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
-                     cfg.shared_hidden, cfg.dtype, train=True)
+                     cfg.shared_hidden, cfg.dtype, train=True, capacity=cfg.capacity)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -280,6 +432,13 @@ def main():
     st, _ = layer.device_status()
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
+    # routing statistics as the pages record them, and the pairs kept
+    per_expert = torch.bincount(layer.idx.reshape(-1).long(), minlength=cfg.experts).cpu()
+    P = cfg.tokens * cfg.top_k
+    kept = int(layer.counts.sum().item())
+    routing = {"skew": cfg.skew, "max_expert_frac": float(per_expert.max()) / P,
+               "empty_experts": int((per_expert == 0).sum()), "capacity": cfg.capacity,
+               "kept_pairs_frac": kept / P}
 
     clocks = ClockSampler(local)
     time.sleep(0.3)
@@ -321,14 +480,21 @@ def main():
     e2e = {"value": world * cfg.tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": 4}
 
-    # per-kernel device time and launch count of the step
-    abi.moe_profile_enable(True)
+    # per-kernel device time and launch count of the forward and of the step
     prof_steps = 3
+    abi.moe_profile_enable(True)
+    for _ in range(prof_steps):
+        flush.zero_()
+        fwd()
+    fwd_rec = abi.moe_profile_read()
+    abi.moe_profile_enable(False)
+    abi.moe_profile_enable(True)
     for _ in range(prof_steps):
         flush.zero_()
         train()
     rec = abi.moe_profile_read()
     abi.moe_profile_enable(False)
+    pieces = pieces_of(fwd_rec, rec, prof_steps)
     launches_per_step = sum(n for n, _ in rec.values()) / prof_steps
     work = kernel_work(cfg)
     peaks = {}
@@ -384,7 +550,7 @@ def main():
                 ent["frac_bf16"] = ent["tflops"] / float(peaks.get("bf16_tflops", 1900.0))
         kernels[k_] = ent
 
-    f_fwd, f_train = step_flops(cfg)
+    f_fwd, f_train = step_flops(cfg, kept / P)
     bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -402,13 +568,14 @@ def main():
             "config": {"workload": cfg.name, "tokens": cfg.tokens, "d_model": cfg.d_model,
                        "d_hidden": cfg.d_hidden, "experts": cfg.experts, "top_k": cfg.top_k,
                        "shared_hidden": cfg.shared_hidden, "step": "train (value_and_grad)",
+                       "routing": routing,
                        "l2": "flushed between timed steps (256 MiB write)",
                        "parallelism": f"independent batch per GPU x{world}"},
             "fwd_tokens_per_s": fwd_value, "fwd_ms": fms,
             "pct_bf16_peak": {"train": f_train / (ms / 1e3) / 1e12 / bf16_peak,
                               "fwd": f_fwd / (fms / 1e3) / 1e12 / bf16_peak},
             "clocks": clk, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
-            "roofline": roofline, "cpu_baseline": cpu, "kernels": kernels,
+            "roofline": roofline, "cpu_baseline": cpu, "pieces_ms": pieces, "kernels": kernels,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
