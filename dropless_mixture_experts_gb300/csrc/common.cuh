@@ -70,7 +70,9 @@ struct Layout {
   size_t dg_part, dA, gH, dxsort, dxs, dAs, gHs, dys, dsel, dwr_part;
   size_t dl;      // dense router-logit gradient [T, E] (bf16 path)
   size_t wrt;     // W_r^T [E, d]
-  size_t dwpart;  // per-split partials of the weight-gradient GEMMs
+  size_t dwpart;  // per-split / per-chunk partials of the weight-gradient GEMMs
+  size_t dw_tick;    // the routed weight gradients' per-tile chunk tickets [dw_tick_n]
+  int64_t dw_tick_n;
   size_t total;
   int64_t P, PPcap, MTcap, NWc;
   int elem;  // bytes per storage element
@@ -153,14 +155,23 @@ inline Layout make_layout(const moe_dims& d, int mode) {
       const int s = split_bound(tiles);
       return (s > 1 || always) ? s * experts * M * ldp : 0;
     };
-    int64_t pf = need(E, h, dm, pick_bn((int)dm), false);
-    pf = std::max(pf, need(E, dm, 2 * h, pick_bn((int)h), false));
+    // routed weight gradients: per-chunk partials; the device-side schedule
+    // takes at most E + grid / tiles_per_expert + 1 chunks (grid <= 256 SMs)
+    auto chunked = [&](int64_t M, int64_t N, int bn) -> int64_t {
+      const int64_t tpe = ((M + 127) / 128) * (N / bn);
+      return (E + 256 / tpe + 1) * M * N;
+    };
+    int64_t pf = chunked(h, dm, pick_bn((int)dm));
+    pf = std::max(pf, chunked(dm, 2 * h, pick_bn((int)h)));
     if (hs > 0) {
       pf = std::max(pf, need(1, hs, dm, pick_bn((int)dm), false));
       pf = std::max(pf, need(1, dm, 2 * hs, pick_bn((int)hs), false));
     }
     pf = std::max(pf, (int64_t)router_dw_split_bound((dm + 127) / 128) * dm * 64);
     L.dwpart = take(sizeof(float) * pf);
+    L.dw_tick_n = std::max(E * ((h + 127) / 128) * (dm / pick_bn((int)dm)),
+                           E * ((dm + 127) / 128) * (2 * h / pick_bn((int)h)));
+    L.dw_tick = take(sizeof(int) * L.dw_tick_n);
   }
   L.total = o;
   return L;

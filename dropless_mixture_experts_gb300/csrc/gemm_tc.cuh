@@ -39,6 +39,10 @@ enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4, E_ROUTER = 5 };
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per block (227 KB)
+// Gate/up epilogue: the staged 32x32 tiles leave through the load/store
+// units (coalesced 16-byte copies, four lanes per row) instead of TMA stores,
+// which keeps the TMA engine for the operand loads.
+constexpr bool kGuStoreLsu = true;
 
 // Tensor maps of one launch: the two operands (B may come from two maps,
 // split along N or K) and the epilogue's bf16 outputs / inputs.
@@ -62,6 +66,10 @@ struct Params {
   int splits = 1;                   // DW kinds: K splits
   float* part = nullptr;            // DW kinds: per-split partials [splits][E][M][ldp]
   int ldp = 0;                      //   (reduced in a fixed order by a second kernel)
+                                    // routed DW kinds: per-chunk partials [chunk][M][ldp]
+  int* dw_tick = nullptr;           // routed DW kinds: per output tile, the chunks done;
+                                    //   routed DZ zeroes them (dw_tick_n) for the DW launches
+  int dw_tick_n = 0;
   int experts = 1;
   int kb_total = 0;                 // row kinds: K / 64
   int kb_split = 0;                 // dual-K B (dx): K blocks taken from the first map
@@ -77,6 +85,10 @@ struct Params {
   float* dg_part = nullptr;         // DZ: [pairs, dg_ld], entry 2*column-tile + half
   int dg_ld = 0;
   int ld_out = 0;
+  int64_t rows_out = 0;             // GU: rows of H / a_g / a_u (load/store-unit stores)
+  void* dst0 = nullptr;             // GU: H, a_g, a_u [rows_out, ld_out] bf16
+  void* dst1 = nullptr;
+  void* dst2 = nullptr;
   int hsplit = 0;
   int* status = nullptr;
 };
@@ -96,7 +108,9 @@ struct Cfg {
   static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048
                                    : EK == E_DZ ? 5 * 2048
                                    : (EK == E_DOWN || EK == E_DX) ? 2048 : 0;
-  static constexpr int FIXED = kEpiWarps * EPI_BYTES + 1024 + 256;
+  // routed DW kinds keep their chunk schedule (E + 1 ints) after the barriers
+  static constexpr int SCHED_BYTES = (DW && ROUTED) ? 4 * (kMaxExperts + 1) + 16 : 0;
+  static constexpr int FIXED = kEpiWarps * EPI_BYTES + 1024 + 256 + SCHED_BYTES;
   static constexpr int STAGES = (kSmemLimit - FIXED) / STAGE_BYTES > 8
                                     ? 8
                                     : (kSmemLimit - FIXED) / STAGE_BYTES;
@@ -113,14 +127,63 @@ struct Cfg {
 
 struct Tile {
   int e, row0, nvalid, m0, n0, kb0, kb1, nt;
-  int s;  // DW kinds: K split
+  int s;   // DW kinds: K split (routed: the global chunk index)
+  int ns;  // routed DW kinds: chunks of this expert (1: the tile writes the final gradient)
 };
+
+// Routed weight-gradient GEMMs reduce over each expert's rows, so a hot
+// expert's tiles carry a long K range while a cold expert's are short.  The
+// K range of expert e (nkb_e 64-row blocks) is cut into S_e chunks so that
+// no work unit holds more than twice the average work of a CTA:
+//   kb_target = max(4, 2 * ceil(sum_e nkb_e * tiles_per_expert / grid)),
+//   S_e = min(kMaxChunks, ceil(nkb_e / kb_target)), at least 1.
+// Uniform routing keeps S_e = 1 (no partials) unless its tiles fill less
+// than half the GPU; a hot expert is cut.  choff is the prefix of S_e
+// (E + 1 entries); chunk g belongs to the expert e with choff[e] <= g <
+// choff[e + 1].
+constexpr int kMaxChunks = 64;
+
+// One warp: lane l takes experts l, l + 32, ... (E <= 256).
+__device__ inline void dw_chunk_schedule(const int* counts, int E, int tiles_per_expert,
+                                         int grid, int* choff) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = kMaxExperts / 32;
+  int nkb[kPer];
+  int64_t total = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    nkb[i] = e < E ? (__ldg(counts + e) + 63) / 64 : 0;
+    total += nkb[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  int64_t target = 2 * ((total * tiles_per_expert + grid - 1) / grid);
+  if (target < 4) target = 4;
+  int base = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    int ns = (int)((nkb[i] + target - 1) / target);
+    ns = e >= E ? 0 : ns < 1 ? 1 : ns > kMaxChunks ? kMaxChunks : ns;
+    int incl = ns;  // inclusive scan over the 32 lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (e < E) choff[e] = base + incl - ns;
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) choff[E] = base;
+}
 
 // Tile t of the persistent schedule.  META=false skips the per-tile
 // metadata loads of the routed row kinds (the MMA issuer only needs the K
 // range, which is the same for every tile of those kinds).
 template <class C, bool META = true>
-__device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles, Tile& tl) {
+__device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles, Tile& tl,
+                                         const int* choff = nullptr) {
   if constexpr (!C::DW) {
     const int mt = t / p.n_nt;
     tl.nt = t % p.n_nt;
@@ -149,21 +212,36 @@ __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles,
     int r = t / p.n_nt;
     const int mt = r % p.n_mt;
     r /= p.n_mt;
-    const int s = r % p.splits;
-    tl.s = s;
-    tl.e = r / p.splits;
-    if (tl.e >= p.experts) return false;
+    int s, ns;
     int64_t ne;
     if constexpr (C::ROUTED) {
+      // r is the global chunk: its expert by bisection of the schedule
+      if (r >= choff[p.experts]) return false;
+      int lo = 0, hi = p.experts;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (choff[mid] <= r) lo = mid;
+        else hi = mid;
+      }
+      tl.e = lo;
+      s = r - choff[lo];
+      ns = choff[lo + 1] - choff[lo];
+      tl.s = r;
       ne = p.counts[tl.e];
       tl.row0 = p.poff[tl.e];
     } else {
+      s = r % p.splits;
+      ns = p.splits;
+      tl.s = s;
+      tl.e = r / p.splits;
+      if (tl.e >= p.experts) return false;
       ne = p.rows;
       tl.row0 = 0;
     }
+    tl.ns = ns;
     const int nkb = (int)((ne + C::BK - 1) / C::BK);
-    tl.kb0 = (int)((int64_t)s * nkb / p.splits);
-    tl.kb1 = (int)((int64_t)(s + 1) * nkb / p.splits);
+    tl.kb0 = (int)((int64_t)s * nkb / ns);
+    tl.kb1 = (int)((int64_t)(s + 1) * nkb / ns);
     tl.nvalid = 0;
     tl.m0 = mt * C::BM;
     tl.n0 = tl.nt * C::BN;
@@ -177,8 +255,10 @@ struct Shared {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t ebar[kEpiWarps];  // per epilogue warp: its staged input tiles
+  uint64_t epi_bar;          // the epilogue warps' own barrier (routed DW chunk fix-up)
   uint32_t tmem_base;
   volatile int abort;
+  volatile int fixup;        // routed DW: this CTA finishes the tile's chunk sum
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Shared* sh,
@@ -252,6 +332,66 @@ __device__ __forceinline__ void router_topk(const float (&lg)[64], int E, int k,
   }
 }
 
+// The epilogue warps' own barrier: one arrival per warp, a bounded wait.
+__device__ __forceinline__ bool epi_sync(Shared* sh, uint32_t& phase, int* status) {
+  if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&sh->epi_bar);
+  const bool ok = wait_or_abort(&sh->epi_bar, phase, sh, status, 600);
+  phase ^= 1;
+  return ok;
+}
+
+// Routed DW tile of an expert cut into ns > 1 K chunks: after storing its
+// partial, the CTA takes a ticket; the one that finishes the tile's last
+// chunk (any order) sums the ns partials in chunk order into the gradient
+// and resets the ticket.  Returns false when a wait ran out.
+template <class C>
+__device__ bool dw_chunk_fixup(const Params& p, const Tile& tl, const int* choff, Shared* sh,
+                               int row, int half, uint32_t& phase) {
+  __threadfence();  // this thread's partial stores before the ticket
+  if (!epi_sync(sh, phase, p.status)) return false;
+  if (threadIdx.x == 64) {
+    const int slot = (tl.e * p.n_mt + tl.m0 / C::BM) * p.n_nt + tl.nt;
+    const int done = atomicAdd(p.dw_tick + slot, 1) + 1;
+    const bool last = done == tl.ns;
+    if (last) p.dw_tick[slot] = 0;  // ready for the next launch
+    __threadfence();
+    sh->fixup = last ? 1 : 0;
+  }
+  if (!epi_sync(sh, phase, p.status)) return false;
+  if (!sh->fixup) return true;
+  const int om = tl.m0 + row;
+  if (om >= p.M) return true;
+  float* base = p.facc;
+  int ncol = tl.n0, ld = p.N;
+  if (p.hsplit > 0) {
+    ld = p.hsplit;
+    if (tl.n0 >= p.hsplit) {
+      base = p.facc2;
+      ncol = tl.n0 - p.hsplit;
+    }
+  }
+  float* dst = base + ((int64_t)tl.e * p.M + om) * ld + ncol;
+  const int g0 = choff[tl.e];
+  const int64_t cstride = (int64_t)p.M * p.ldp;
+  const float* src = p.part + ((int64_t)g0 * p.M + om) * p.ldp + tl.n0;
+#pragma unroll 1
+  for (int c = half; c < C::BN / 32; c += 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < tl.ns; ++s) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + s * cstride + 32 * c + 4 * i));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      *reinterpret_cast<float4*>(dst + 32 * c + 4 * i) = acc;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -274,6 +414,22 @@ __device__ __forceinline__ void stage_read_row(const uint8_t* tile, int r, float
   }
 }
 
+// A staged 32x32 bf16 tile (64-byte swizzle) to rows y0.. / columns x.. of a
+// row-major [rows, ld] bf16 array: lane l copies 16 bytes of rows l/4,
+// l/4 + 8, ... (four lanes per 64-byte row piece), rows past `rows` skipped.
+__device__ __forceinline__ void staged_copy_out(const uint8_t* tile, void* dst, int y0, int x,
+                                                int ld, int64_t rows, int lane) {
+  const int q = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = (lane >> 2) + 8 * i;
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + tc::sw64_off(r, q));
+    if ((int64_t)y0 + r < rows)
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst) +
+                                ((int64_t)y0 + r) * ld + x + 8 * q) = v;
+  }
+}
+
 __device__ __forceinline__ void stage_write_row(uint8_t* tile, int r, const float (&v)[32]) {
 #pragma unroll
   for (int k = 0; k < 4; ++k)
@@ -290,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;
   Shared* sh = reinterpret_cast<Shared*>(epi + kEpiWarps * C::EPI_BYTES);
+  int* choff = reinterpret_cast<int*>(sh + 1);  // routed DW kinds: the chunk schedule
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -302,8 +459,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_init(&sh->tempty[a], kEpiWarps);
     }
     for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&sh->ebar[w], 1);
+    tc::mbar_init(&sh->epi_bar, kEpiWarps);
     sh->abort = 0;
     tc::fence_barrier_init();
+  }
+  if constexpr (C::DW && C::ROUTED) {
+    if (warp == 2)  // an epilogue warp (idle until the first tile is ready)
+      dw_chunk_schedule(p.counts, p.experts, p.n_mt * p.n_nt, gridDim.x, choff);
+  }
+  if constexpr (C::EK == E_DZ && C::ROUTED) {
+    // the chunk tickets of the weight-gradient launches that follow start at 0
+    if (blockIdx.x == 0 && p.dw_tick)
+      for (int i = threadIdx.x; i < p.dw_tick_n; i += blockDim.x) p.dw_tick[i] = 0;
   }
   if (warp == 0 && lane == 0) {
     tc::tma_prefetch_desc(&m.a);
@@ -329,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       Tile tl;
-      for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl); t += gridDim.x) {
+      for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl, choff); t += gridDim.x) {
         int brow0 = 0;
         if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
         if constexpr (C::DW) brow0 = tl.row0;
@@ -376,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, aphase = 0;
     Tile tl;
-    for (int t = blockIdx.x; !aborted && get_tile<C, false>(p, t, nrow_tiles, tl);
+    for (int t = blockIdx.x; !aborted && get_tile<C, false>(p, t, nrow_tiles, tl, choff);
          t += gridDim.x) {
       if (!wait_or_abort(&sh->tempty[acc], aphase ^ 1, sh, p.status, 200)) {
         aborted = true;
@@ -430,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* ebar = &sh->ebar[ew];
     uint32_t ephase = 0;
     int acc = 0;
-    uint32_t aphase = 0;
+    uint32_t aphase = 0, epi_phase = 0;
     Tile tl, tn;
     int t = blockIdx.x;
-    bool have = get_tile<C>(p, t, nrow_tiles, tl);
+    bool have = get_tile<C>(p, t, nrow_tiles, tl, choff);
     // DZ: saved a_g / a_u of this warp's first chunk, loaded ahead of the MMA
     if constexpr (C::EK == E_DZ) {
       if (have && lane == 0) {
@@ -444,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     while (have && !aborted) {
       // the next tile's metadata is read while this one is processed
-      const bool have_next = get_tile<C>(p, t + gridDim.x, nrow_tiles, tn);
+      const bool have_next = get_tile<C>(p, t + gridDim.x, nrow_tiles, tn, choff);
       // per-row metadata of this tile (routed kinds): issued before the wait
       int32_t pr = -1;
       float gt = 1.f;
@@ -481,23 +648,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             uv[i] = bf16r(__uint_as_float(u[i]));
             hv[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
           }
-          if (lane == 0) tc::bulk_wait_read0();  // staging free again
-          __syncwarp();
-          stage_write_row(stg, lane, hv);
-          if (p.save) {
-            stage_write_row(stg + 2048, lane, gv);
-            stage_write_row(stg + 4096, lane, uv);
-          }
-          tc::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            const int x = tl.n0 + 32 * c;
-            tc::tma_store_2d(&m.o0, stg, x, yrow);
+          if constexpr (kGuStoreLsu) {
+            __syncwarp();  // the previous chunk's copies have read the staging
+            stage_write_row(stg, lane, hv);
             if (p.save) {
-              tc::tma_store_2d(&m.o1, stg + 2048, x, yrow);
-              tc::tma_store_2d(&m.o2, stg + 4096, x, yrow);
+              stage_write_row(stg + 2048, lane, gv);
+              stage_write_row(stg + 4096, lane, uv);
             }
-            tc::bulk_commit();
+            __syncwarp();
+            const int x = tl.n0 + 32 * c;
+            staged_copy_out(stg, p.dst0, yrow, x, p.ld_out, p.rows_out, lane);
+            if (p.save) {
+              staged_copy_out(stg + 2048, p.dst1, yrow, x, p.ld_out, p.rows_out, lane);
+              staged_copy_out(stg + 4096, p.dst2, yrow, x, p.ld_out, p.rows_out, lane);
+            }
+          } else {
+            if (lane == 0) tc::bulk_wait_read0();  // staging free again
+            __syncwarp();
+            stage_write_row(stg, lane, hv);
+            if (p.save) {
+              stage_write_row(stg + 2048, lane, gv);
+              stage_write_row(stg + 4096, lane, uv);
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int x = tl.n0 + 32 * c;
+              tc::tma_store_2d(&m.o0, stg, x, yrow);
+              if (p.save) {
+                tc::tma_store_2d(&m.o1, stg + 2048, x, yrow);
+                tc::tma_store_2d(&m.o2, stg + 4096, x, yrow);
+              }
+              tc::bulk_commit();
+            }
           }
         }
       } else if constexpr (C::EK == E_DOWN || C::EK == E_DX) {
@@ -638,9 +821,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one split's partial (reduced later in split order) or the final
         // gradient; every element of the tile is written once (zeros when
         // this split's K range is empty)
-        float* dst = p.part ? p.part + ((int64_t)tl.s * p.experts * p.M + (int64_t)tl.e * p.M + om) *
-                                           p.ldp + tl.n0
-                            : base + ((int64_t)tl.e * p.M + om) * ld + ncol;
+        float* dst;
+        if constexpr (C::ROUTED) {  // a chunk's partial, or the final gradient for one chunk
+          dst = tl.ns > 1 ? p.part + ((int64_t)tl.s * p.M + om) * p.ldp + tl.n0
+                          : base + ((int64_t)tl.e * p.M + om) * ld + ncol;
+        } else {
+          dst = p.part ? p.part + ((int64_t)tl.s * p.experts * p.M + (int64_t)tl.e * p.M + om) *
+                                      p.ldp + tl.n0
+                       : base + ((int64_t)tl.e * p.M + om) * ld + ncol;
+        }
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t v[32];
@@ -664,6 +853,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sh->tempty[acc]);
+      if constexpr (C::DW && C::ROUTED) {
+        if (tl.ns > 1 && !dw_chunk_fixup<C>(p, tl, choff, sh, row, half, epi_phase)) {
+          aborted = true;
+          break;
+        }
+      }
       if (++acc == 2) {
         acc = 0;
         aphase ^= 1;

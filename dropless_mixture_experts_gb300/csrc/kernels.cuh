@@ -23,6 +23,7 @@ void clear_status(int* status, cudaStream_t s);
 void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, int hsplit,
                          float* out0, float* out1, cudaStream_t s);
 
+
 // routing and permutation (route_permute.cu)
 void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* idx,
                          float* gates, cudaStream_t s);

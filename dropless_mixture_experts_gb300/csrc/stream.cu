@@ -209,6 +209,8 @@ __global__ void __launch_bounds__(32) loss_reduce_kernel(const float* __restrict
 // couples it to the kept slots); a rejected index (e outside [0, E)) has
 // neither.  The first KM slots' indices and logit gradients are loaded one
 // item ahead.
+constexpr int kNoRow = 1 << 16;  // router_dx: the slot's pair has no row (E <= 256)
+
 template <typename T, int KM>
 __global__ void __launch_bounds__(kThreads)
     router_dx_kernel(const int32_t* __restrict__ idx, const float* __restrict__ dsel,
@@ -236,16 +238,17 @@ __global__ void __launch_bounds__(kThreads)
   for (; i < n; i += stride) {
     const int64_t t = i / cpt;
     const int64_t col = (i % cpt) * VE;
-    int ex[KM], rw[KM];
+    int ex[KM];
     float ds[KM];
-    uint4 v[KM];
+    uint4 v[KM];  // zero for a slot without a row
     const uint4 us = dxs ? ldg16(dxs + t * d + col) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int j = 0; j < KM; ++j) {
-      rw[j] = j < k ? nr[j] : -1;                           // -1: no row
-      ex[j] = j < k && ne[j] >= 0 && ne[j] < E ? ne[j] : -1;  // -1: no router term
+      // ex: the expert, with kNoRow set for a slot without a row; -1 for no
+      // slot or a rejected index (nothing to add)
+      ex[j] = j < k && (unsigned)ne[j] < (unsigned)E ? ne[j] | (nr[j] < 0 ? kNoRow : 0) : -1;
       ds[j] = nd[j];
-      if (rw[j] >= 0) v[j] = ldg16(dxsort + (int64_t)rw[j] * d + col);
+      if (ex[j] >= 0 && !(ex[j] & kNoRow)) v[j] = ldg16(dxsort + (int64_t)nr[j] * d + col);
     }
     if (i + stride < n) index_ahead(i + stride);
     float acc[VE];
@@ -255,37 +258,33 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int q = 0; q < VE; ++q) acc[q] = 0.f;
     }
-    // slot j adds its row (when it has one), then its router term
+    // slot j adds its row (when it has one) and its router term
     auto add_slot = [&](int j) {
+      if (ex[j] < 0) return;
       float fv[VE], fw[VE];
-      if (rw[j] >= 0) {
-        cvt16<T>(v[j], fv);
-      } else {
+      if (ex[j] & kNoRow) {
 #pragma unroll
         for (int q = 0; q < VE; ++q) fv[q] = 0.f;
+      } else {
+        cvt16<T>(v[j], fv);
       }
-      if (ex[j] >= 0) {
-        cvt16<T>(ldg16(wt + (int64_t)ex[j] * d + col), fw);
+      cvt16<T>(ldg16(wt + (int64_t)(ex[j] & ~kNoRow) * d + col), fw);
 #pragma unroll
-        for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds[j], fw[q], fv[q]);
-      } else if (rw[j] >= 0) {
-#pragma unroll
-        for (int q = 0; q < VE; ++q) acc[q] += fv[q];
-      }
+      for (int q = 0; q < VE; ++q) acc[q] += fmaf(ds[j], fw[q], fv[q]);
     };
 #pragma unroll
     for (int j = 0; j < KM; ++j) add_slot(j);
     for (int j0 = KM; j0 < k; j0 += KM) {  // k > KM: further slots, in order
 #pragma unroll
       for (int j = 0; j < KM; ++j) {
-        rw[j] = ex[j] = -1;
+        ex[j] = -1;
         if (j0 + j < k) {
           const int64_t p = t * k + j0 + j;
           const int e = __ldg(idx + p);
-          rw[j] = __ldg(pairrow + p);
-          ex[j] = e >= 0 && e < E ? e : -1;
+          const int64_t r = __ldg(pairrow + p);
+          ex[j] = (unsigned)e < (unsigned)E ? e | (r < 0 ? kNoRow : 0) : -1;
           ds[j] = __ldg(dsel + p);
-          if (rw[j] >= 0) v[j] = ldg16(dxsort + (int64_t)rw[j] * d + col);
+          if (r >= 0) v[j] = ldg16(dxsort + r * d + col);
         }
       }
 #pragma unroll

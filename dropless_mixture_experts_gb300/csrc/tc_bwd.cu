@@ -46,6 +46,8 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.gates = p.gates;
     q.dg_part = at<float>(ws, L.dg_part);
     q.dg_ld = 2 * h / 64;
+    q.dw_tick = at<int>(ws, L.dw_tick);  // zeroed here for the weight gradients
+    q.dw_tick_n = (int)L.dw_tick_n;
     launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_dz", s);
   } else {
     if (!make_map(&mp.a, p.dy, d.tokens, dm, 64, 128)) return false;
@@ -120,6 +122,17 @@ void reduce_splits(const Params& q, float* out0, float* out1, cudaStream_t s) {
                       out1, s);
 }
 
+// Routed DW launches: K chunks per expert from the device-side schedule
+// (balanced against the row counts; the last chunk of a tile to finish sums
+// the chunks' partials); the work units are bounded by
+// (E + grid / tiles_per_expert + 1) chunks.
+int64_t set_chunks(Params& q, const Layout& L, void* ws) {
+  q.part = at<float>(ws, L.dwpart);
+  q.dw_tick = at<int>(ws, L.dw_tick);
+  const int64_t tpe = (int64_t)q.n_mt * q.n_nt;
+  return (q.experts + sm_count() / tpe + 1) * tpe;
+}
+
 // dW_down[e] = sum over the expert's rows of gH_r^T dy_r: A = gH (MN-major:
 // rows are K), B = sorted dy (MN-major)
 template <int BN>
@@ -136,8 +149,6 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   q.n_mt = (h + 127) / 128;
   q.n_nt = dm / BN;
   q.experts = E;
-  const int64_t rows_per_e = routed ? L.P / E : d.tokens;
-  set_splits(q, L, ws, (rows_per_e + 63) / 64, false);
   q.ldp = dm;
   float* out = routed ? p.dw_down : p.dws_down;
   q.facc = out;
@@ -147,9 +158,11 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(
-        mp, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_down", s);
+    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(mp, q, set_chunks(q, L, ws),
+                                                        "tc_dw_down", s);
+    return true;
   } else {
+    set_splits(q, L, ws, (d.tokens + 63) / 64, false);
     if (!make_map(&mp.a, at<void>(ws, L.gHs), d.tokens, h, 64, 64)) return false;
     if (!make_map(&mp.b0, p.dy, d.tokens, dm, 64, 64)) return false;
     mp.b1 = mp.b0;
@@ -178,8 +191,6 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
   q.n_mt = (dm + 127) / 128;
   q.n_nt = 2 * h / BN;
   q.experts = E;
-  const int64_t rows_per_e = routed ? L.P / E : d.tokens;
-  set_splits(q, L, ws, (rows_per_e + 63) / 64, false);
   q.ldp = 2 * h;
   float* g = routed ? p.dw_gate : p.dws_gate;
   float* u = routed ? p.dw_up : p.dws_up;
@@ -191,9 +202,11 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(
-        mp, q, (int64_t)E * q.n_mt * q.n_nt * q.splits, "tc_dw_gateup", s);
+    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(mp, q, set_chunks(q, L, ws),
+                                                        "tc_dw_gateup", s);
+    return true;
   } else {
+    set_splits(q, L, ws, (d.tokens + 63) / 64, false);
     if (!make_map(&mp.a, p.x, d.tokens, dm, 64, 64)) return false;
     if (!make_map(&mp.b0, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 64)) return false;
     mp.b1 = mp.b0;

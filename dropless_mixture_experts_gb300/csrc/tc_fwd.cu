@@ -27,6 +27,10 @@ bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, vo
   void* H = routed ? p.h_buf : p.hs_buf;
   void* AG = routed ? p.a_gate : p.as_gate;
   void* AU = routed ? p.a_up : p.as_up;
+  q.rows_out = rows;
+  q.dst0 = H;
+  q.dst1 = AG;
+  q.dst2 = AU;
   if (!make_map_sw64(&mp.o0, H, rows, h)) return false;
   mp.o1 = mp.o2 = mp.o0;
   if (save && (!make_map_sw64(&mp.o1, AG, rows, h) || !make_map_sw64(&mp.o2, AU, rows, h)))
