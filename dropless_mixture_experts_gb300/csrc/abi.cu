@@ -134,7 +134,6 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
   MOE_TRY(shape_supported(dims));
   MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
   const Layout L = make_layout(*dims, MOE_FWD_ONLY);
-  clear_status(at<int>(workspace, L.status), stream);
   launch_permute(*dims, L, topk_idx, counts, offsets, perm, inv_perm, workspace, stream);
   return cuda_status();
 }

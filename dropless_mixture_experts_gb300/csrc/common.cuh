@@ -62,7 +62,7 @@ __device__ __forceinline__ void report_error(int* status, int code, int detail) 
 // ---- workspace layout -------------------------------------------------------
 struct Layout {
   size_t status, warp_counts, warp_base, counts, poff, rowpair, tiles, ntiles,
-      loss_part, logits;
+      loss_part, loss_tick, logits;
   size_t xs;       // expert-sorted copy of the token rows [padded rows, d]
   size_t pairrow;  // pair -> padded row [P]
   size_t osort;    // gate-weighted expert output per sorted row [padded rows, d]
@@ -130,6 +130,7 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.tiles = take(sizeof(int4) * L.MTcap);
   L.ntiles = take(sizeof(int) * 4);
   L.loss_part = take(sizeof(float) * kLossBlocks);
+  L.loss_tick = take(sizeof(int));  // the combine's blocks done (reset by its last block)
   L.logits = take(sizeof(float) * T * E);
   L.xs = take((size_t)L.elem * L.PPcap * dm);
   L.pairrow = take(sizeof(int) * L.P);

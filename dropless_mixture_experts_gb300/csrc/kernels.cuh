@@ -18,7 +18,6 @@ void prof_end(cudaStream_t s);
 // utility kernels (misc.cu)
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s);
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s);
-void clear_status(int* status, cudaStream_t s);
 // fixed-order sum of the K-split partials of a weight-gradient GEMM
 void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, int hsplit,
                          float* out0, float* out1, cudaStream_t s);

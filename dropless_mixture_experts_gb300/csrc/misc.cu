@@ -64,6 +64,6 @@ void launch_split_reduce(const float* part, int S, int64_t EM, int ldp, int N, i
 
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s) { zero_fill<int32_t>(p, n, s); }
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s) { zero_fill<float>(p, n, s); }
-void clear_status(int* status, cudaStream_t s) { zero_fill<int>(status, 2, s); }
+
 
 }  // namespace moe

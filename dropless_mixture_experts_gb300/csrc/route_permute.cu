@@ -332,37 +332,62 @@ __global__ void __launch_bounds__(1024) perm_colscan_kernel(const int* __restric
   if (tid == 1023) counts_ws[e] = part[1023];
 }
 
-// Offsets, padded offsets, the tile list and the padding rows (one block).
-// With a capacity the counts become the kept counts (in the workspace too:
-// the weight-gradient GEMMs take their K ranges from there), and perm past
-// the kept rows reads -1.
-__global__ void __launch_bounds__(1024) perm_finalize_kernel(int* __restrict__ counts_ws, int E,
-                                                             int capacity, int64_t P,
-                                                             int32_t* counts_out,
-                                                             int32_t* offsets_out, int* poff,
-                                                             int4* tiles, int* ntiles,
-                                                             int32_t* rowpair, int32_t* perm) {
-  __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1], s_toff[kMaxExperts + 1];
+// Offsets, padded offsets, the tile list and the padding rows (one block of
+// 1024 threads).  With a capacity the counts become the kept counts (in the
+// workspace too: the weight-gradient GEMMs take their K ranges from there),
+// and perm past the kept rows reads -1.  It also starts the invocation's
+// device status (an index the histogram pass rejected is rejected again by
+// the scatter pass) and the combine's block ticket.  s_off / s_poff receive
+// the offsets the scatter pass uses.
+__device__ void finalize_block(int* __restrict__ counts_ws, int E, int capacity, int64_t P,
+                               int32_t* counts_out, int32_t* offsets_out, int* poff, int4* tiles,
+                               int* ntiles, int32_t* rowpair, int32_t* perm, int* status,
+                               int* loss_tick, int* s_off, int* s_poff) {
+  __shared__ int s_toff[kMaxExperts + 1];
   __shared__ int s_cnt[kMaxExperts];
-  const int tid = threadIdx.x;
-  if (tid == 0) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < E; e += blockDim.x) {
+    const int c = counts_ws[e];
+    s_cnt[e] = capacity > 0 && c > capacity ? capacity : c;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scans of the counts, padded rows and tiles, 32 experts a round
     int o = 0, po = 0, to = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = o;
-      s_poff[e] = po;
-      s_toff[e] = to;
-      const int c = capacity > 0 && counts_ws[e] > capacity ? capacity : counts_ws[e];
-      s_cnt[e] = c;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      const int c = e < E ? s_cnt[e] : 0;
       const int nt = (c + kRowPad - 1) / kRowPad;
-      o += c;
-      po += nt * kRowPad;
-      to += nt;
+      int ic = c, ip = nt * kRowPad, it = nt;  // inclusive scans over the lanes
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int vc = __shfl_up_sync(0xffffffffu, ic, d);
+        const int vp = __shfl_up_sync(0xffffffffu, ip, d);
+        const int vt = __shfl_up_sync(0xffffffffu, it, d);
+        if (lane >= d) {
+          ic += vc;
+          ip += vp;
+          it += vt;
+        }
+      }
+      if (e < E) {
+        s_off[e] = o + ic - c;
+        s_poff[e] = po + ip - nt * kRowPad;
+        s_toff[e] = to + it - nt;
+      }
+      o += __shfl_sync(0xffffffffu, ic, 31);
+      po += __shfl_sync(0xffffffffu, ip, 31);
+      to += __shfl_sync(0xffffffffu, it, 31);
     }
-    s_off[E] = o;
-    s_poff[E] = po;
-    s_toff[E] = to;
-    ntiles[0] = to;
-    ntiles[1] = po;
+    if (lane == 0) {
+      s_off[E] = o;
+      s_poff[E] = po;
+      s_toff[E] = to;
+      ntiles[0] = to;
+      ntiles[1] = po;
+      status[0] = 0;
+      status[1] = 0;
+      *loss_tick = 0;
+    }
   }
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) {
@@ -374,17 +399,28 @@ __global__ void __launch_bounds__(1024) perm_finalize_kernel(int* __restrict__ c
     }
   }
   for (int64_t r = s_off[E] + tid; r < P; r += blockDim.x) perm[r] = -1;  // past the kept rows
-  for (int e = 0; e < E; ++e) {
+  // one warp per expert: its tiles, and the padding rows of its last tile
+  for (int e = warp; e < E; e += blockDim.x >> 5) {
     const int c = s_cnt[e];
     const int nt = s_toff[e + 1] - s_toff[e];
-    for (int j = tid; j < nt; j += blockDim.x) {
+    for (int j = lane; j < nt; j += 32) {
       const int valid = min(kRowPad, c - j * kRowPad);
       tiles[s_toff[e] + j] = make_int4(e, s_poff[e] + j * kRowPad, valid, 0);
     }
-    // padding rows of this expert's last tile: no pair
-    const int pad_lo = s_poff[e] + c, pad_hi = s_poff[e + 1];
-    for (int r = pad_lo + tid; r < pad_hi; r += blockDim.x) rowpair[r] = -1;
+    for (int r = s_poff[e] + c + lane; r < s_poff[e + 1]; r += 32) rowpair[r] = -1;
   }
+}
+
+__global__ void __launch_bounds__(1024) perm_finalize_kernel(int* __restrict__ counts_ws, int E,
+                                                             int capacity, int64_t P,
+                                                             int32_t* counts_out,
+                                                             int32_t* offsets_out, int* poff,
+                                                             int4* tiles, int* ntiles,
+                                                             int32_t* rowpair, int32_t* perm,
+                                                             int* status, int* loss_tick) {
+  __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1];
+  finalize_block(counts_ws, E, capacity, P, counts_out, offsets_out, poff, tiles, ntiles, rowpair,
+                 perm, status, loss_tick, s_off, s_poff);
 }
 
 __global__ void __launch_bounds__(256) perm_scatter_kernel(
@@ -432,7 +468,7 @@ void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int3
   MOE_LAUNCH("perm_finalize", s,
              perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, d.capacity, L.P, counts,
                                                      offsets, poff, tiles, ntiles, rowpair,
-                                                     perm));
+                                                     perm, status, at<int>(ws, L.loss_tick)));
   if (NW > 0)
     MOE_LAUNCH("perm_scatter", s,
                perm_scatter_kernel<<<blocks, 256, 0, s>>>(idx, L.P, E, k, NW, warp_base, offsets,

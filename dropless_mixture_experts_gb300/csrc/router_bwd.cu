@@ -15,13 +15,27 @@ namespace {
 // lanes (the power of two >= k) takes one token, lane j of the group its
 // slot j.  With dl given, the token's dense bf16 row of the logit gradient
 // (zero off the selection; E a multiple of 8) is written as well.
+// The blocks past the tokens' write W_r^T [E, d] from W_r [d, E] (storage
+// type unchanged) for the router input gradient.
+template <typename T>
 __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restrict__ gates,
                                                           const float* __restrict__ dg_part,
                                                           int dg_ld, int dg_n, int64_t Tn, int k,
                                                           int G, float* __restrict__ dsel,
                                                           const int32_t* __restrict__ idx, int E,
                                                           const int32_t* __restrict__ pairrow,
-                                                          __nv_bfloat16* __restrict__ dl) {
+                                                          __nv_bfloat16* __restrict__ dl,
+                                                          unsigned dsel_blocks,
+                                                          const T* __restrict__ w, int d,
+                                                          T* __restrict__ wt) {
+  if (blockIdx.x >= dsel_blocks) {
+    const int64_t n = (int64_t)d * E;
+    const int64_t stride = (int64_t)(gridDim.x - dsel_blocks) * blockDim.x;
+    for (int64_t i = (blockIdx.x - dsel_blocks) * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += stride)
+      wt[(i % E) * d + i / E] = w[i];
+    return;
+  }
   const int j = threadIdx.x & (G - 1);
   const int64_t t = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / G;
   const bool live = t < Tn;  // every lane stays for the shuffles
@@ -49,18 +63,6 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
       const int e = idx[p];
       if (e >= 0 && e < E) dl[t * E + e] = __float2bfloat16_rn(v);  // a rejected index is skipped
     }
-  }
-}
-
-// W_r^T [E, d] from W_r [d, E] (storage type unchanged)
-template <typename T>
-__global__ void __launch_bounds__(256) transpose_router_kernel(const T* __restrict__ w, int d,
-                                                               int E, T* __restrict__ wt) {
-  const int64_t n = (int64_t)d * E;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / E, e = i % E;
-    wt[e * d + r] = w[i];
   }
 }
 
@@ -153,16 +155,16 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
 
   int G = 1;
   while (G < k) G *= 2;
+  T* wt = at<T>(ws, L.wrt);
+  const unsigned dsel_blocks = (unsigned)((d.tokens * G + 255) / 256);
+  int64_t tr_blocks = ((int64_t)dm * E + 255) / 256;
+  if (tr_blocks > sms) tr_blocks = sms;
   MOE_LAUNCH("router_dsel", s,
-             router_dsel_kernel<<<(unsigned)((d.tokens * G + 255) / 256), 256, 0, s>>>(
+             router_dsel_kernel<T><<<dsel_blocks + (unsigned)tr_blocks, 256, 0, s>>>(
                  p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, G, dsel,
                  p.topk_idx, E, at<const int32_t>(ws, L.pairrow),
-                 tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr));
-
-  T* wt = at<T>(ws, L.wrt);
-  MOE_LAUNCH("router_transpose", s,
-             transpose_router_kernel<T><<<(unsigned)((dm * E + 255) / 256), 256, 0, s>>>(
-                 reinterpret_cast<const T*>(p.w_router), dm, E, wt));
+                 tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr, dsel_blocks,
+                 reinterpret_cast<const T*>(p.w_router), dm, wt));
 
   launch_router_dx(d, L, p, dsel, wt, ws, s);
 

@@ -111,7 +111,8 @@ template <typename T, int KM>
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(const T* __restrict__ osort, const int32_t* __restrict__ pairrow,
                    const T* __restrict__ ys, T* __restrict__ y, const T* __restrict__ G,
-                   int64_t Tn, int d, int k, float* __restrict__ loss_part) {
+                   int64_t Tn, int d, int k, float* __restrict__ loss_part,
+                   int* __restrict__ loss_tick, float* __restrict__ loss) {
   constexpr int VE = 16 / sizeof(T);
   __shared__ float red[kThreads / 32];
   const int cpt = d / VE;
@@ -184,22 +185,27 @@ __global__ void __launch_bounds__(kThreads)
   for (int o = 16; o > 0; o >>= 1) lacc += __shfl_xor_sync(0xffffffffu, lacc, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = lacc;
   __syncthreads();
+  __shared__ int last;
   if (threadIdx.x == 0) {
     float s = 0.f;
     for (int w = 0; w < kThreads / 32; ++w) s += red[w];
     loss_part[blockIdx.x] = s;
+    __threadfence();  // the partial before the ticket
+    last = atomicAdd(loss_tick, 1) == (int)gridDim.x - 1;
   }
-}
-
-__global__ void __launch_bounds__(32) loss_reduce_kernel(const float* __restrict__ part, int n,
-                                                         float* loss) {
-  // fixed-order reduction: lane l sums part[l], part[l+32], ...; then a
-  // fixed butterfly
+  __syncthreads();
+  if (!last || threadIdx.x >= 32 || !loss) return;
+  // the last block: fixed-order reduction of the partials (lane l sums
+  // part[l], part[l + 32], ...; then a fixed butterfly)
+  __threadfence();
   float s = 0.f;
-  for (int i = threadIdx.x; i < n; i += 32) s += part[i];
+  for (int i = threadIdx.x; i < (int)gridDim.x; i += 32) s += __ldcg(loss_part + i);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (threadIdx.x == 0) *loss = s;
+  if (threadIdx.x == 0) {
+    *loss = s;
+    *loss_tick = 0;  // ready for the next call
+  }
 }
 
 // ---- router backward: input gradient ------------------------------------------
@@ -309,7 +315,7 @@ void combine_t(const moe_dims& d, const Layout& L, void* y, const void* G, float
                kernel<<<blocks, kThreads, 0, s>>>(
                    at<const T>(ws, L.osort), at<const int32_t>(ws, L.pairrow), ys,
                    reinterpret_cast<T*>(y), reinterpret_cast<const T*>(G), d.tokens, d.d_model,
-                   d.top_k, part));
+                   d.top_k, part, at<int>(ws, L.loss_tick), loss));
   };
   switch (slots_ahead(d.top_k)) {
     case 1: launch(combine_kernel<T, 1>); break;
@@ -317,8 +323,7 @@ void combine_t(const moe_dims& d, const Layout& L, void* y, const void* G, float
     case 4: launch(combine_kernel<T, 4>); break;
     default: launch(combine_kernel<T, 8>); break;
   }
-  if (G && loss)
-    MOE_LAUNCH("loss_reduce", s, loss_reduce_kernel<<<1, 32, 0, s>>>(part, (int)blocks, loss));
+
 }
 
 template <typename T>
