@@ -129,6 +129,37 @@ class MoELayer:
         self.backward(x, p, dy)
         return self.loss, self.dx, self.grads
 
+    def train_step_from_host(self, x_host, p, dy_host, loss_host=None):
+        """The train step on a batch in pinned host memory: x is copied to the
+        device on the current stream, the upstream gradient on a side stream
+        while the forward pass runs (only the combine needs it), and the value
+        is copied back into ``loss_host`` (pinned, optional).  Returns the
+        same device buffers as ``train_step``; the copies land in the layer's
+        own input buffers."""
+        if self.mode != abi.MOE_SAVE_FOR_BWD:
+            raise RuntimeError("layer was built with train=False")
+        if getattr(self, "x_dev", None) is None:
+            self.x_dev = torch.empty(self.T, self.d, dtype=self.tdtype, device=self.device)
+            self.dy_dev = torch.empty(self.T, self.d, dtype=self.tdtype, device=self.device)
+            self.side = torch.cuda.Stream(self.device)
+            self.dy_ready = torch.cuda.Event()
+        main = torch.cuda.current_stream(self.device)
+        self.x_dev.copy_(x_host, non_blocking=True)
+        self.side.wait_stream(main)  # the previous step has finished with dy_dev
+        with torch.cuda.stream(self.side):
+            self.dy_dev.copy_(dy_host, non_blocking=True)
+            self.dy_ready.record(self.side)
+        x = self.x_dev
+        self.route(x, p["w_router"], None, p.get("router_bias"))
+        self.permute()
+        self.grouped_ffn_fwd(x, p, abi.MOE_SAVE_FOR_BWD)
+        main.wait_event(self.dy_ready)
+        self.combine(x, p, abi.MOE_SAVE_FOR_BWD, upstream=self.dy_dev)
+        self.backward(x, p, self.dy_dev)
+        if loss_host is not None:
+            loss_host.copy_(self.loss, non_blocking=True)
+        return self.loss, self.dx, self.grads
+
     def device_status(self):
         """(status, detail) recorded by the kernels; synchronises the stream."""
         return abi.moe_read_device_status(self.ws_ptr, self.ws_bytes, self._stream())

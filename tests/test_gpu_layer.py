@@ -176,3 +176,28 @@ def test_rejected_expert_index_is_skipped_through_the_train_step(dtype):
     keep[[5, 17]] = False
     assert torch.equal(runs[0][1][keep], runs[1][1][keep])
     assert torch.equal(runs[0][2][keep], runs[1][2][keep])
+
+
+def test_train_step_from_host_matches_device_inputs():
+    # the host-input step (upstream copied on a side stream behind the
+    # forward) gives the device-input step's results bit for bit
+    cfg = MoEConfig(777, 128, 128, 8, 3, 128, "bf16", "host_inputs")
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, "bf16")
+    p = {k: dev[k] for k in params_of(inp)}
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                     cfg.shared_hidden, "bf16", train=True)
+    loss, dx, g = layer.train_step(dev["x"], p, dev["upstream"])
+    torch.cuda.synchronize()
+    ref = (loss.clone(), dx.clone(), {k: v.clone() for k, v in g.items() if v is not None})
+    xh = dev["x"].cpu().pin_memory()
+    gh = dev["upstream"].cpu().pin_memory()
+    lh = torch.empty(1, dtype=torch.float32).pin_memory()
+    for _ in range(2):  # the second call reuses the layer's input buffers
+        loss2, dx2, g2 = layer.train_step_from_host(xh, p, gh, lh)
+        torch.cuda.synchronize()
+        assert torch.equal(loss2, ref[0]) and float(lh[0]) == float(ref[0][0])
+        assert torch.equal(dx2, ref[1])
+        for k, v in ref[2].items():
+            assert torch.equal(g2[k], v), k
