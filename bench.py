@@ -94,29 +94,64 @@ def step_flops(cfg, kept_frac=1.0):
     return fwd, 3 * fwd
 
 
-def kernel_work(cfg):
-    """Algorithmic work per step of each kernel name: ("flop", n) for the
-    contractions (2*M*N*K over real rows; the routed experts' launches, and
-    the shared expert's with suffix _sh), ("byte", n) for the row streams
-    (each row read or written once)."""
+def kernel_work(cfg, kept=None):
+    """Algorithmic work per step of each kernel name: {"flop": f, "byte": b}.
+    f = 2*M*N*K over real rows (routed launches count the kept pairs; the
+    shared expert's launches carry the suffix _sh); b = every operand and
+    result read or written once (real rows only, no padding rows, no
+    split-K partials; weights once per launch).  The train step saves the
+    pre-activations, so gate/up counts three [rows, h] outputs."""
     T, d, h, E, k, hs = cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k, cfg.shared_hidden
-    P = T * k
+    P = T * k if kept is None else kept
     el = 2 if cfg.dtype == "bf16" else 4
-    w = {"logits": ("flop", 2 * T * d * E), "router": ("flop", 2 * T * d * E),
-         "router_dw": ("flop", 2 * T * d * E)}
-    for name, n in (("gateup", 2), ("down", 1), ("dz", 1), ("dx", 2), ("dw_down", 1),
-                    ("dw_gateup", 2)):
-        w[name] = ("flop", 2 * P * d * h * n)
-        if hs:
-            w[name + "_sh"] = ("flop", 2 * T * d * hs * n)
+    w = {}
+    router_b = T * d * el + d * E * el
+    w["router"] = {"flop": 2 * T * d * E, "byte": router_b + T * k * 8}
+    w["logits"] = {"flop": 2 * T * d * E, "byte": router_b + T * E * 4}
+    # x and the dense bf16 logit gradient in, the f32 [d, E] gradient out
+    w["router_dw"] = {"flop": 2 * T * d * E, "byte": T * d * el + T * E * el + d * E * 4}
+
+    def ffn(tag, M, hh, n_w):
+        # M rows through one SwiGLU expert stack of hidden hh (n_w weight sets)
+        wb = d * hh * el * n_w  # one [d, hh] matrix per weight set
+        w["gateup" + tag] = {"flop": 4 * M * d * hh,
+                             "byte": M * d * el + 2 * wb + 3 * M * hh * el}
+        w["down" + tag] = {"flop": 2 * M * d * hh, "byte": M * hh * el + wb + M * d * el}
+        # dy rows and the saved a_g, a_u in; dA [M, 2hh] and gate*H out
+        w["dz" + tag] = {"flop": 2 * M * d * hh,
+                         "byte": M * d * el + wb + 2 * M * hh * el + 3 * M * hh * el}
+        w["dx" + tag] = {"flop": 4 * M * d * hh, "byte": 2 * M * hh * el + 2 * wb + M * d * el}
+        w["dw_down" + tag] = {"flop": 2 * M * d * hh,
+                              "byte": M * hh * el + M * d * el + d * hh * 4 * n_w}
+        w["dw_gateup" + tag] = {"flop": 4 * M * d * hh,
+                                "byte": M * d * el + 2 * M * hh * el + 2 * d * hh * 4 * n_w}
+
+    ffn("", P, h, E)
+    if hs:
+        ffn("_sh", T, hs, 1)
     shared_rows = T if hs else 0
     # x -> xs and dy -> dys: each token row read once, written to its k rows
-    w["scatter_rows"] = ("byte", 2 * (T + P) * d * el)
+    w["scatter_rows"] = {"flop": 0, "byte": 2 * (T + P) * d * el}
     # pair rows + shared rows + upstream read, y written
-    w["combine"] = ("byte", (P + shared_rows + T + T) * d * el)
+    w["combine"] = {"flop": 0, "byte": (P + shared_rows + T + T) * d * el}
     # pair rows + shared rows read, dx written
-    w["router_dx"] = ("byte", (P + shared_rows + T) * d * el)
+    w["router_dx"] = {"flop": 0, "byte": (P + shared_rows + T) * d * el}
     return w
+
+
+def kernel_bound(name, wk, peaks):
+    """The roofline a kernel sits under: the larger of its time at the
+    compute peak (bf16 tensor, or FP32 FFMA for the SIMT kernels) and its
+    time at the HBM peak.  Returns (bound, compute peak TFLOP/s, hbm GB/s)."""
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    if name.startswith("simt_"):
+        # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock
+        comp, cb = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12, "alu"
+    else:
+        comp, cb = float(peaks.get("bf16_tflops", 1900.0)), "tensor"
+    t_c = wk["flop"] / (comp * 1e12)
+    t_m = wk["byte"] / (hbm * 1e9)
+    return (cb if t_c >= t_m else "hbm"), comp, hbm
 
 
 def src_hash():
@@ -497,33 +532,25 @@ def main():
     abi.moe_profile_enable(False)
     pieces = pieces_of(fwd_rec, rec, prof_steps)
     launches_per_step = sum(n for n, _ in rec.values()) / prof_steps
-    work = kernel_work(cfg)
+    work = kernel_work(cfg, kept)
     peaks = {}
     try:
         peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
     except Exception:
         pass
-    # the dominant kernel with a known algorithmic amount of work
+    # the dominant kernel with a known algorithmic amount of work, under
+    # whichever of its compute and HBM rooflines is the binding one
     def work_of(name):
         return work.get(name.split("_", 1)[1] if name.startswith(("tc_", "simt_")) else name)
     known = [kv for kv in rec.items() if work_of(kv[0])]
     tname, (tn, tms) = max(known, key=lambda kv: kv[1][1])
-    unit, amount = work_of(tname)
-    amount *= prof_steps
-    alu = tname.startswith("simt_")
-    if unit == "byte":
-        achieved = amount / (tms / 1e3) / 1e9 if tms > 0 else 0.0
-        peak = float(peaks.get("hbm_gbs", 6800.0))
-        bound, runit = "hbm", "GB/s"
-    elif alu:
-        achieved = amount / (tms / 1e3) / 1e12 if tms > 0 else 0.0
-        # FP32 FFMA: 152 SMs x 128 lanes x 2 flop x max SM clock
-        peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
-        bound, runit = "alu", "TFLOP/s"
+    wk = work_of(tname)
+    bound, comp_peak, hbm_peak = kernel_bound(tname, wk, peaks)
+    secs = tms / prof_steps / 1e3
+    if bound == "hbm":
+        achieved, peak, runit = wk["byte"] / secs / 1e9 if secs > 0 else 0.0, hbm_peak, "GB/s"
     else:
-        achieved = amount / (tms / 1e3) / 1e12 if tms > 0 else 0.0
-        peak = float(peaks.get("bf16_tflops", 1900.0))
-        bound, runit = "tensor", "TFLOP/s"
+        achieved, peak, runit = wk["flop"] / secs / 1e12 if secs > 0 else 0.0, comp_peak, "TFLOP/s"
     traffic = None
     try:
         tr = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
@@ -535,6 +562,7 @@ def main():
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": runit,
                 "frac": achieved / peak if peak else None, "traffic": traffic,
                 "kernel": tname, "launch_ms": tms / tn,
+                "algorithmic": {"flop": wk["flop"], "byte": wk["byte"]},
                 "peak_source": {"tensor": "measured bf16 burst", "hbm": "measured HBM copy",
                                 "alu": "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"}[bound]}
     kernels = {}
@@ -542,13 +570,14 @@ def main():
         ent = {"launches_per_step": n / prof_steps, "ms_per_step": t / prof_steps}
         wk = work_of(k_)
         if wk and t > 0:
-            u, a = wk
-            if u == "byte":
-                ent["gbs"] = a / (t / prof_steps / 1e3) / 1e9
-                ent["frac_hbm"] = ent["gbs"] / float(peaks.get("hbm_gbs", 6800.0))
-            elif not k_.startswith("simt_"):
-                ent["tflops"] = a / (t / prof_steps / 1e3) / 1e12
-                ent["frac_bf16"] = ent["tflops"] / float(peaks.get("bf16_tflops", 1900.0))
+            secs = t / prof_steps / 1e3
+            bnd, comp_peak, hbm_peak = kernel_bound(k_, wk, peaks)
+            ent["bound"] = bnd
+            if wk["flop"]:
+                ent["tflops"] = wk["flop"] / secs / 1e12
+                ent["frac_" + ("alu" if k_.startswith("simt_") else "bf16")] = ent["tflops"] / comp_peak
+            ent["gbs"] = wk["byte"] / secs / 1e9
+            ent["frac_hbm"] = ent["gbs"] / hbm_peak
         kernels[k_] = ent
 
     f_fwd, f_train = step_flops(cfg, kept / P)

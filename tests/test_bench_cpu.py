@@ -1,0 +1,39 @@
+"""Host-side accounting of bench.py: the per-kernel algorithmic work adds
+up to the layer's FLOP count, and each kernel's roofline is the binding one."""
+
+import bench
+from dropless_mixture_experts_gb300.synthetic import CONFIGS
+
+PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2070.0}
+
+
+def test_kernel_flops_add_up_to_the_train_step():
+    for name, cfg in CONFIGS.items():
+        w = bench.kernel_work(cfg)
+        gemm = sum(v["flop"] for k, v in w.items() if k not in ("router", "logits", "router_dw"))
+        # the router's three contractions: x W_r, x^T dl, and dl W_r^T (inside router_dx)
+        router = 3 * w["router"]["flop"]
+        _, train = bench.step_flops(cfg)
+        assert gemm + router == train, name
+
+
+def test_capacity_counts_kept_pairs_only():
+    cfg = CONFIGS["e8k2_bf16_32k"]
+    full = bench.kernel_work(cfg)
+    half = bench.kernel_work(cfg, kept=cfg.tokens * cfg.top_k // 2)
+    assert half["gateup"]["flop"] * 2 == full["gateup"]["flop"]
+    assert half["router"] == full["router"]
+
+
+def test_binding_roofline():
+    w = bench.kernel_work(CONFIGS["e8k2_bf16_32k"])
+    # h = 1024: the saved-activation traffic of dZ outweighs its FLOPs
+    assert bench.kernel_bound("tc_dz", w["dz"], PEAKS)[0] == "hbm"
+    assert bench.kernel_bound("tc_gateup", w["gateup"], PEAKS)[0] == "tensor"
+    assert bench.kernel_bound("tc_router", w["router"], PEAKS)[0] == "hbm"
+    assert bench.kernel_bound("combine", w["combine"], PEAKS)[0] == "hbm"
+    assert bench.kernel_bound("simt_gateup", w["gateup"], PEAKS)[0] == "alu"
+    # fine-grained experts (h = 128): every routed GEMM is HBM-bound
+    wd = bench.kernel_work(CONFIGS["decoder_bf16_128k"])
+    for k in ("gateup", "down", "dz", "dx", "dw_down", "dw_gateup"):
+        assert bench.kernel_bound("tc_" + k, wd[k], PEAKS)[0] == "hbm", k
