@@ -117,9 +117,11 @@ def kernel_work(cfg, kept=None):
         w["gateup" + tag] = {"flop": 4 * M * d * hh,
                              "byte": M * d * el + 2 * wb + 3 * M * hh * el}
         w["down" + tag] = {"flop": 2 * M * d * hh, "byte": M * hh * el + wb + M * d * el}
-        # dy rows and the saved a_g, a_u in; dA [M, 2hh] and gate*H out
+        # the (gate-scaled) dy rows and the saved a_g, a_u in; dA [M, 2hh]
+        # out (the float32 path also writes gate*H for its W_down gradient)
+        n_out = 3 if cfg.dtype == "f32" else 2
         w["dz" + tag] = {"flop": 2 * M * d * hh,
-                         "byte": M * d * el + wb + 2 * M * hh * el + 3 * M * hh * el}
+                         "byte": M * d * el + wb + 2 * M * hh * el + n_out * M * hh * el}
         w["dx" + tag] = {"flop": 4 * M * d * hh, "byte": 2 * M * hh * el + 2 * wb + M * d * el}
         w["dw_down" + tag] = {"flop": 2 * M * d * hh,
                               "byte": M * hh * el + M * d * el + d * hh * 4 * n_w}

@@ -64,7 +64,7 @@ _SIGS = {
     "moe_permute": ([_D, _P, _P, _P, _P, _P, _P, _S, _P], ctypes.c_int),
     "moe_grouped_ffn_fwd": ([_D, ctypes.c_int] + [_P] * 9 + [_S, _P], ctypes.c_int),
     "moe_combine": ([_D, ctypes.c_int] + [_P] * 11 + [_S, _P], ctypes.c_int),
-    "moe_backward": ([_D] + [_P] * 24 + [_S, _P], ctypes.c_int),
+    "moe_backward": ([_D] + [_P] * 26 + [_S, _P], ctypes.c_int),
     "moe_read_device_status": ([_P, _S, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "moe_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "moe_permute_noalloc": ([_D, _P, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -161,12 +161,12 @@ def moe_combine(dims, mode, x, ws_gate, ws_up, ws_down, y, hs_buf, as_gate_saved
 
 
 def moe_backward(dims, dy, x, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, topk_idx,
-                 gates, a_gate_saved, a_up_saved, as_gate_saved, as_up_saved, dx, dw_router,
-                 dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, ws, ws_bytes, stream,
-                 check=True):
+                 gates, a_gate_saved, a_up_saved, h_saved, as_gate_saved, as_up_saved, hs_saved,
+                 dx, dw_router, dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, ws, ws_bytes,
+                 stream, check=True):
     args = [dy, x, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, topk_idx, gates,
-            a_gate_saved, a_up_saved, as_gate_saved, as_up_saved, dx, dw_router, dw_gate, dw_up,
-            dw_down, dws_gate, dws_up, dws_down, ws]
+            a_gate_saved, a_up_saved, h_saved, as_gate_saved, as_up_saved, hs_saved, dx,
+            dw_router, dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down, ws]
     s = load().moe_backward(ctypes.byref(dims), *[_p(a) for a in args], ws_bytes, _p(stream))
     if check:
         _check(s, "moe_backward")

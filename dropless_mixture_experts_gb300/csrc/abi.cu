@@ -213,8 +213,9 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
                         const void* w_gate, const void* w_up, const void* w_down,
                         const void* ws_gate, const void* ws_up, const void* ws_down,
                         const int32_t* topk_idx, const float* gates, const void* a_gate_saved,
-                        const void* a_up_saved, const void* as_gate_saved, const void* as_up_saved,
-                        void* dx, float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
+                        const void* a_up_saved, const void* h_saved, const void* as_gate_saved,
+                        const void* as_up_saved, const void* hs_saved, void* dx,
+                        float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
                         float* dws_gate, float* dws_up, float* dws_down, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
   if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
@@ -224,13 +225,13 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
     return MOE_ERR_INVALID_ARG;
   if (dims->tokens > 0) {
     if (!dy || !x || !w_gate || !w_up || !w_down || !topk_idx || !gates || !a_gate_saved ||
-        !a_up_saved || !dx)
+        !a_up_saved || !h_saved || !dx)
       return MOE_ERR_INVALID_ARG;
-    if (shared && (!as_gate_saved || !as_up_saved)) return MOE_ERR_INVALID_ARG;
+    if (shared && (!as_gate_saved || !as_up_saved || !hs_saved)) return MOE_ERR_INVALID_ARG;
   }
   if (!aligned16({dy, x, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down, a_gate_saved,
-                  a_up_saved, as_gate_saved, as_up_saved, dx, dw_router, dw_gate, dw_up, dw_down,
-                  dws_gate, dws_up, dws_down}))
+                  a_up_saved, h_saved, as_gate_saved, as_up_saved, hs_saved, dx, dw_router,
+                  dw_gate, dw_up, dw_down, dws_gate, dws_up, dws_down}))
     return MOE_ERR_INVALID_ARG;
   MOE_TRY(shape_supported(dims));
   // the router backward keeps W_r^T and one dW_r column block in shared memory
@@ -267,6 +268,8 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
   p.a_up = const_cast<void*>(a_up_saved);
   p.as_gate = const_cast<void*>(as_gate_saved);
   p.as_up = const_cast<void*>(as_up_saved);
+  p.h_buf = const_cast<void*>(h_saved);
+  p.hs_buf = const_cast<void*>(hs_saved);
   p.dx = dx;
   p.dw_router = dw_router;
   p.dw_gate = dw_gate;

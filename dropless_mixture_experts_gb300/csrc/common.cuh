@@ -67,7 +67,8 @@ struct Layout {
   size_t pairrow;  // pair -> padded row [P]
   size_t osort;    // gate-weighted expert output per sorted row [padded rows, d]
   size_t ys;       // shared-expert output [T, d]
-  size_t dg_part, dA, gH, dxsort, dxs, dAs, gHs, dys, dsel, dwr_part;
+  size_t dg_part, dA, dxsort, dxs, dAs, dys, dsel, dwr_part;
+  size_t gH, gHs;  // gate * H for the W_down gradients (float32 path only)
   size_t dl;      // dense router-logit gradient [T, E] (bf16 path)
   size_t wrt;     // W_r^T [E, d]
   size_t dwpart;  // per-split / per-chunk partials of the weight-gradient GEMMs
@@ -139,11 +140,13 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   if (mode == MOE_SAVE_FOR_BWD) {
     L.dg_part = take(sizeof(float) * L.P * 2 * (h / 64));
     L.dA = take((size_t)L.elem * L.PPcap * 2 * h);
-    L.gH = take((size_t)L.elem * L.PPcap * h);
+    // the bf16 path's W_down gradients read the forward's saved H instead
+    const bool gh = d.dtype != MOE_BF16;
+    L.gH = take(gh ? (size_t)L.elem * L.PPcap * h : 0);
     L.dxsort = take((size_t)L.elem * L.PPcap * dm);
     L.dxs = take((size_t)L.elem * (hs > 0 ? T : 0) * dm);
     L.dAs = take((size_t)L.elem * T * 2 * hs);
-    L.gHs = take((size_t)L.elem * T * hs);
+    L.gHs = take(gh ? (size_t)L.elem * T * hs : 0);
     L.dys = take((size_t)L.elem * L.PPcap * dm);
     L.dsel = take(sizeof(float) * T * d.top_k);
     L.dwr_part = take(sizeof(float) * kRouterBwdRanges * dm * E);

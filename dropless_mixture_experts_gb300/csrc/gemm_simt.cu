@@ -7,8 +7,9 @@
 //   GU      a_g = x_t W_gate[e], a_u = x_t W_up[e], H = silu(a_g) * a_u
 //           (gather of the token rows fused into the operand load)
 //   DOWN    gate * (H W_down[e]) per sorted row (the pair's share of y[t])
-//   DZ      Z = dy_t W_down[e]^T; dgate = <Z, H>; dA_g, dA_u by the SwiGLU
-//           chain rule; gH = gate * H kept for the W_down gradient
+//   DZ      Z = dy_t W_down[e]^T; gate * dgate = gate * <Z, H> (the router
+//           backward's q); dA_g, dA_u by the SwiGLU chain rule; gH = gate * H
+//           kept for the W_down gradient
 //   DX      dA_g W_gate[e]^T + dA_u W_up[e]^T per sorted row (share of dx[t])
 //   DWD     dW_down[e] = sum_r gH_r^T dy_t           (ragged K = expert rows)
 //   DWGU    dW_gate[e] | dW_up[e] = sum_r x_t^T [dA_g | dA_u]
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       // the 16 threads of one row are 16 consecutive lanes of a warp
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, o);
-      if (ROUTED && tx == 0 && valid) a.dg_part[(int64_t)a.rowpair[r] * a.dg_ld + ntile] = dgp;
+      if (ROUTED && tx == 0 && valid)
+        a.dg_part[(int64_t)a.rowpair[r] * a.dg_ld + ntile] = gt * dgp;
     } else {  // DWD / DWGU: plain stores of the expert's gradient tile
       const int64_t om = m0 + m;
       const int64_t eoff = (int64_t)e * a.n_mtiles * BM;  // expert offset in rows

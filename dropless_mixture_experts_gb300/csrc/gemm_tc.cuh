@@ -12,7 +12,7 @@
 //              splitting its columns: tcgen05.ld, then the fused SwiGLU,
 //              gate-weighted combine, SwiGLU backward or gradient stores.
 //              bf16 tiles the epilogue reads or writes (the SwiGLU outputs,
-//              the saved pre-activations, the backward's dA and gate*H) go
+//              the saved pre-activations, the backward's dA) go
 //              through a per-warp 32x32 staging tile in shared memory and
 //              move with TMA loads and stores.
 //
@@ -76,7 +76,7 @@ struct Params {
   int brow_stride = 0;              // rows of a B weight matrix per expert (0: activations)
   int M = 0, N = 0;                 // DW output dims / row-kind output columns
   // epilogue
-  const float* gates = nullptr;     // routed DOWN / DZ: pair gates; router: logit offsets [E]
+  const float* gates = nullptr;     // routed DOWN: pair gates; router: logit offsets [E]
   int save = 0;                     // GU: also store a_g, a_u
   void* out0 = nullptr;             // router: top-k indices [T, k]
   void* out1 = nullptr;             // router: gates [T, k]
@@ -106,7 +106,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per-warp staging: 2 KB per bf16 32x32 tile
   static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048
-                                   : EK == E_DZ ? 5 * 2048
+                                   : EK == E_DZ ? 4 * 2048
                                    : (EK == E_DOWN || EK == E_DX) ? 2048 : 0;
   // routed DW kinds keep their chunk schedule (E + 1 ints) after the barriers
   static constexpr int SCHED_BYTES = (DW && ROUTED) ? 4 * (kMaxExperts + 1) + 16 : 0;
@@ -618,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (C::ROUTED && (C::EK == E_DOWN || C::EK == E_DZ)) {
         if (row < tl.nvalid) {
           pr = p.rowpair[(int64_t)tl.row0 + row];
-          gt = p.gates[pr];
+          if constexpr (C::EK == E_DOWN) gt = p.gates[pr];
         } else {
           gt = 0.f;
         }
@@ -709,9 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else if constexpr (C::EK == E_DZ) {
-        // Z = dy W_down^T for this row; SwiGLU backward from the saved
-        // pre-activations (TMA-staged); gate-gradient partial <Z, H> over
-        // these columns; dA and gate*H tiles stored by TMA
+        // the routed rows of dy arrive scaled by their pair's gate, so the
+        // accumulator holds dH = g (dy W_down^T) (the shared expert: g = 1);
+        // SwiGLU backward from the saved pre-activations (TMA-staged); the
+        // partial <dH, H> = g dg over these columns; dA tiles stored by TMA
         const int h = p.ld_out;
         float dgp = 0.f;
 #pragma unroll 1
@@ -740,31 +741,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_2d(stg + 2048, &m.i1, ebar, nx, ny);
             }
           }
-          float dag[32], dau[32], gh[32];
+          float dag[32], dau[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float z = __uint_as_float(zv[i]);
+            const float dh = __uint_as_float(zv[i]);
             const float s = __fdividef(1.f, 1.f + __expf(-ag[i]));
             const float sl = ag[i] * s;
-            const float hv = bf16r(sl * au[i]);
-            dgp = fmaf(z, hv, dgp);
-            const float dh = gt * z;
+            const float hv = bf16r(sl * au[i]);  // H as the forward stored it
+            dgp = fmaf(dh, hv, dgp);
             dau[i] = dh * sl;
             dag[i] = dh * au[i] * s * (1.f + ag[i] * (1.f - s));
-            gh[i] = gt * hv;
           }
           if (lane == 0) tc::bulk_wait_read0();
           __syncwarp();
           stage_write_row(stg + 4096, lane, dag);
           stage_write_row(stg + 6144, lane, dau);
-          stage_write_row(stg + 8192, lane, gh);
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             const int x = tl.n0 + 32 * c;
             tc::tma_store_2d(&m.o0, stg + 4096, x, yrow);
             tc::tma_store_2d(&m.o0, stg + 6144, h + x, yrow);
-            tc::tma_store_2d(&m.o1, stg + 8192, x, yrow);
             tc::bulk_commit();
           }
         }

@@ -1,7 +1,9 @@
 // Router backward.  The gates are a softmax over the k selected logits, so
 // the logit gradient of slot j is g_j (dg_j - sum_i g_i dg_i), with dg_j the
-// gradient of the gate (the row-dot <dy_t W_down[e]^T, H_r> produced by the
-// grouped backward), and zero on the experts that were not selected
+// gradient of the gate (the row-dot <dy_t W_down[e]^T, H_r>).  The grouped
+// backward hands over q_j = g_j dg_j (its rows of dy come scaled by the
+// gate), so the logit gradient is q_j - g_j sum_i q_i, with no division by
+// a gate; zero on the experts that were not selected
 // (gpu_moe_h100.json: value_and_grad through the router).  Then
 // dW_r = x^T dlogits, and dx gains dlogits W_r^T (a row stream, stream.cu).
 #include "kernels.cuh"
@@ -9,9 +11,9 @@
 namespace moe {
 namespace {
 
-// dsel[t, j] = g_j (dg_j - sum_i g_i dg_i); dg_j is the sum (in column-tile
-// order) of the grouped backward's partials of pair t*k+j, and 0 for a pair
-// without a row (capacity-dropped or a rejected index).  A group of G
+// dsel[t, j] = q_j - g_j sum_i q_i; q_j = g_j dg_j is the sum (in
+// column-tile order) of the grouped backward's partials of pair t*k+j, and
+// 0 for a pair without a row (capacity-dropped or a rejected index).  A group of G
 // lanes (the power of two >= k) takes one token, lane j of the group its
 // slot j.  With dl given, the token's dense bf16 row of the logit gradient
 // (zero off the selection; E a multiple of 8) is written as well.
@@ -41,17 +43,17 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
   const bool live = t < Tn;  // every lane stays for the shuffles
   const bool own = live && j < k;
   const int64_t p = t * k + j;
-  float dg = 0.f, g = 0.f;
+  float qj = 0.f, g = 0.f;
   if (own) {
     if (pairrow[p] >= 0) {
       const float* src = dg_part + p * dg_ld;
-      for (int q = 0; q < dg_n; ++q) dg += src[q];
+      for (int q = 0; q < dg_n; ++q) qj += src[q];
     }
     g = gates[p];
   }
-  float sgd = g * dg;
-  for (int o = G / 2; o > 0; o >>= 1) sgd += __shfl_xor_sync(0xffffffffu, sgd, o);
-  const float v = g * (dg - sgd);
+  float sq = qj;
+  for (int o = G / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+  const float v = fmaf(-g, sq, qj);
   if (own) dsel[p] = v;
   if (dl) {
     if (live) {

@@ -70,17 +70,19 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
 }
 
 // ---- expert-sorted row copy ---------------------------------------------------
-// out[pairrow[t*k + j]] = src[t] for every slot j: each token row is read
-// once and written to its k sorted rows (reading in sorted order instead
-// would fetch a row k times once the rows outgrow the L2).  The padding rows
-// of each expert, [poff[e] + counts[e], poff[e+1]), are zeroed by the items
-// past the tokens' (the grouped GEMMs read them; zero rows give zero
-// contributions to every weight gradient).
+// out[pairrow[t*k + j]] = src[t] for every slot j (with gates: the row
+// scaled by the pair's gate, g_tj src[t], rounded to the storage type): each
+// token row is read once and written to its k sorted rows (reading in sorted
+// order instead would fetch a row k times once the rows outgrow the L2).
+// The padding rows of each expert, [poff[e] + counts[e], poff[e+1]), are
+// zeroed by the items past the tokens' (the grouped GEMMs read them; zero
+// rows give zero contributions to every weight gradient).
+template <typename T, bool SCALE>
 __global__ void __launch_bounds__(kThreads)
     scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ pairrow,
-                        uint4* __restrict__ out, int64_t Tn, int cpt, int k,
-                        const int32_t* __restrict__ poff, const int32_t* __restrict__ counts,
-                        int E) {
+                        const float* __restrict__ gates, uint4* __restrict__ out, int64_t Tn,
+                        int cpt, int k, const int32_t* __restrict__ poff,
+                        const int32_t* __restrict__ counts, int E) {
   const int64_t n = Tn * cpt;
   const int64_t per_e = (int64_t)(kRowPad - 1) * cpt;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -92,7 +94,18 @@ __global__ void __launch_bounds__(kThreads)
       const uint4 v = __ldg(src + i);
       for (int j = 0; j < k; ++j) {
         const int64_t r = __ldg(pairrow + t * k + j);
-        if (r >= 0) out[r * cpt + c] = v;  // a pair without a row (a rejected index) is skipped
+        if (r < 0) continue;  // a pair without a row (a rejected index) is skipped
+        if constexpr (SCALE) {
+          constexpr int VE = 16 / sizeof(T);
+          const float g = __ldg(gates + t * k + j);
+          float f[VE];
+          cvt16<T>(v, f);
+#pragma unroll
+          for (int q = 0; q < VE; ++q) f[q] *= g;
+          st16<T>(out + r * cpt + c, f);
+        } else {
+          out[r * cpt + c] = v;
+        }
       }
     } else {
       const int64_t q = i - n;
@@ -350,15 +363,20 @@ void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const f
 }  // namespace
 
 void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, void* out, void* ws,
-                         cudaStream_t s) {
+                         cudaStream_t s, const float* gates) {
   if (d.tokens == 0) return;
   const int cpt = (int)((int64_t)d.d_model * L.elem / 16);
   const int64_t items = d.tokens * cpt + (int64_t)d.experts * (kRowPad - 1) * cpt;
-  MOE_LAUNCH("scatter_rows", s,
-             scatter_rows_kernel<<<stream_grid(items, INT32_MAX), kThreads, 0, s>>>(
-                 reinterpret_cast<const uint4*>(src), at<const int32_t>(ws, L.pairrow),
-                 reinterpret_cast<uint4*>(out), d.tokens, cpt, d.top_k, at<const int32_t>(ws, L.poff),
-                 at<const int32_t>(ws, L.counts), d.experts));
+  auto launch = [&](auto kernel) {
+    MOE_LAUNCH("scatter_rows", s,
+               kernel<<<stream_grid(items, INT32_MAX), kThreads, 0, s>>>(
+                   reinterpret_cast<const uint4*>(src), at<const int32_t>(ws, L.pairrow), gates,
+                   reinterpret_cast<uint4*>(out), d.tokens, cpt, d.top_k,
+                   at<const int32_t>(ws, L.poff), at<const int32_t>(ws, L.counts), d.experts));
+  };
+  if (!gates) launch(scatter_rows_kernel<__nv_bfloat16, false>);
+  else if (d.dtype == MOE_BF16) launch(scatter_rows_kernel<__nv_bfloat16, true>);
+  else launch(scatter_rows_kernel<float, true>);
 }
 
 void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* upstream, float* loss,

@@ -1,10 +1,11 @@
 // Backward launches of the tensor-core GEMMs (bf16 storage).  The upstream
-// gradient rows are first gathered into expert-sorted order (one HBM pass);
-// the forward's sorted copy of x is reused.  Then
-//   DZ  Z = dy_t W_down[e]^T with the SwiGLU backward and the gate-gradient
-//       partials in the epilogue
+// gradient rows are first copied into expert-sorted order, each scaled by
+// its pair's gate (one HBM pass: row r of pair (t, j) holds g_tj dy_t); the
+// forward's sorted copy of x and its saved H are reused.  Then
+//   DZ  dH = (g dy_t) W_down[e]^T with the SwiGLU backward and the partials
+//       of g dg = <dH, H> in the epilogue
 //   DX  [dA_g | dA_u] [W_gate[e] | W_up[e]]^T per sorted row
-//   DW  dW_down[e] = gH^T dy_t and dW_gate[e] | dW_up[e] = x_t^T [dA_g | dA_u]
+//   DW  dW_down[e] = H^T (g dy_t) and dW_gate[e] | dW_up[e] = x_t^T [dA_g | dA_u]
 //       with K the expert's own rows (ragged), split over CTAs when the
 //       output has too few tiles to fill the GPU; splits write partials that
 //       a second kernel sums in split order (deterministic)
@@ -30,10 +31,9 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   q.kb_total = dm / 64;
   q.ld_out = h;
   if (!make_map_sw64(&mp.o0, at<void>(ws, routed ? L.dA : L.dAs), rows, 2 * h)) return false;
-  if (!make_map_sw64(&mp.o1, at<void>(ws, routed ? L.gH : L.gHs), rows, h)) return false;
   if (!make_map_sw64(&mp.i0, routed ? p.a_gate : p.as_gate, rows, h)) return false;
   if (!make_map_sw64(&mp.i1, routed ? p.a_up : p.as_up, rows, h)) return false;
-  mp.o2 = mp.o1;
+  mp.o1 = mp.o2 = mp.o0;
   if (routed) {
     if (!make_map(&mp.a, at<void>(ws, L.dys), L.PPcap, dm, 64, 128)) return false;
     if (!make_map(&mp.b0, p.w_down, (uint64_t)d.experts * h, dm, 64, BN)) return false;
@@ -43,7 +43,6 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = h;
-    q.gates = p.gates;
     q.dg_part = at<float>(ws, L.dg_part);
     q.dg_ld = 2 * h / 64;
     q.dw_tick = at<int>(ws, L.dw_tick);  // zeroed here for the weight gradients
@@ -133,8 +132,9 @@ int64_t set_chunks(Params& q, const Layout& L, void* ws) {
   return (q.experts + sm_count() / tpe + 1) * tpe;
 }
 
-// dW_down[e] = sum over the expert's rows of gH_r^T dy_r: A = gH (MN-major:
-// rows are K), B = sorted dy (MN-major)
+// dW_down[e] = sum over the expert's rows of H_r^T (g dy)_r: A = the
+// forward's saved H (MN-major: rows are K), B = the gate-scaled sorted dy
+// (MN-major); the shared expert: Hs^T dy
 template <int BN>
 bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
              cudaStream_t s) {
@@ -153,7 +153,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
   float* out = routed ? p.dw_down : p.dws_down;
   q.facc = out;
   if (routed) {
-    if (!make_map(&mp.a, at<void>(ws, L.gH), L.PPcap, h, 64, 64)) return false;
+    if (!make_map(&mp.a, p.h_buf, L.PPcap, h, 64, 64)) return false;
     if (!make_map(&mp.b0, at<void>(ws, L.dys), L.PPcap, dm, 64, 64)) return false;
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
@@ -163,7 +163,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     return true;
   } else {
     set_splits(q, L, ws, (d.tokens + 63) / 64, false);
-    if (!make_map(&mp.a, at<void>(ws, L.gHs), d.tokens, h, 64, 64)) return false;
+    if (!make_map(&mp.a, p.hs_buf, d.tokens, h, 64, 64)) return false;
     if (!make_map(&mp.b0, p.dy, d.tokens, dm, 64, 64)) return false;
     mp.b1 = mp.b0;
     q.rows = d.tokens;
@@ -238,7 +238,7 @@ int tc_dz_bn(int h) { return pick_bn(h); }
 
 bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                        cudaStream_t s) {
-  launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s);
+  launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s, p.gates);
   if (d.shared_hidden > 0 && !backward_one(d, L, p, ws, false, s)) return false;
   return backward_one(d, L, p, ws, true, s);
 }

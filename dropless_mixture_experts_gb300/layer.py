@@ -103,7 +103,8 @@ class MoELayer:
                          _ptr(p["w_up"]), _ptr(p["w_down"]), _ptr(p.get("ws_gate")),
                          _ptr(p.get("ws_up")), _ptr(p.get("ws_down")), _ptr(self.idx),
                          _ptr(self.gates), _ptr(self.a_gate), _ptr(self.a_up),
-                         _ptr(self.as_gate), _ptr(self.as_up), _ptr(self.dx),
+                         _ptr(self.h_buf), _ptr(self.as_gate), _ptr(self.as_up),
+                         _ptr(self.hs_buf), _ptr(self.dx),
                          _ptr(g["dw_router"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]),
                          _ptr(g["dw_down"]), _ptr(g["dws_gate"]), _ptr(g["dws_up"]),
                          _ptr(g["dws_down"]), self.ws_ptr, self.ws_bytes, self._stream())

@@ -173,24 +173,30 @@ moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Backward of the train step for L = sum(y * dy):
- *   inputs : dy [T, d], x, all weights, topk_idx, gates, and the saved
- *            pre-activations of a MOE_SAVE_FOR_BWD forward that used the
- *            same workspace (as_* NULL when hs == 0)
+ *   inputs : dy [T, d], x, all weights, topk_idx, gates, and what a
+ *            MOE_SAVE_FOR_BWD forward that used the same workspace left:
+ *            its pre-activations a_gate_saved / a_up_saved [padded_rows, h]
+ *            and h_saved [padded_rows, h] (the h_buf of moe_grouped_ffn_fwd),
+ *            and for the shared expert as_gate_saved / as_up_saved and
+ *            hs_saved [T, hs] (the hs_buf of moe_combine; all three NULL
+ *            when hs == 0)
  *   outputs: dx [T, d] (dtype); dw_router [d, E], dw_gate/dw_up [E, d, h],
  *            dw_down [E, h, d], dws_gate/dws_up [d, hs], dws_down [hs, d]
  *            (all f32; the dws_* NULL when hs == 0).  Outputs are
  *            overwritten, not accumulated.
  * The router gradient follows from the softmax over the selected logits;
- * experts that were not selected get no logit gradient. */
+ * experts that were not selected get no logit gradient.  The saved
+ * buffers are read only. */
 moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x,
                         const void* w_router, const void* w_gate, const void* w_up,
                         const void* w_down, const void* ws_gate, const void* ws_up,
                         const void* ws_down, const int32_t* topk_idx, const float* gates,
-                        const void* a_gate_saved, const void* a_up_saved,
-                        const void* as_gate_saved, const void* as_up_saved, void* dx,
-                        float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
-                        float* dws_gate, float* dws_up, float* dws_down, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream);
+                        const void* a_gate_saved, const void* a_up_saved, const void* h_saved,
+                        const void* as_gate_saved, const void* as_up_saved,
+                        const void* hs_saved, void* dx, float* dw_router, float* dw_gate,
+                        float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
+                        float* dws_down, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
 
 /* Synchronises `stream`, then returns the device-side status recorded in
  * the workspace since the last moe_permute (MOE_OK, MOE_ERR_TIMEOUT or

@@ -77,8 +77,8 @@ def test_workspace_errors(lib):
     assert abi.moe_permute(d, 256, 256, 256, 256, 256, 0x1010, need, None, check=False) == abi.MOE_ERR_WORKSPACE
     assert abi.moe_permute(d, 256, 256, 256, 256, 256, 0x1000, need - 1, None, check=False) == abi.MOE_ERR_WORKSPACE
     need_t = abi.moe_workspace_bytes(d, abi.MOE_SAVE_FOR_BWD)
-    ptrs = [256] * 24
-    s = abi.moe_backward(d, *ptrs[:15], *ptrs[15:23], 0x1000, need_t - 1, None, check=False)
+    ptrs = [256] * 25
+    s = abi.moe_backward(d, *ptrs, 0x1000, need_t - 1, None, check=False)
     assert s == abi.MOE_ERR_WORKSPACE
 
 
@@ -99,6 +99,16 @@ def test_null_pointers_rejected(lib):
     # a value without a place to put it
     assert abi.moe_combine(d, 0, None, None, None, None, 256, None, None, None, 256, None, 0x1000,
                            need, None, check=False) == abi.MOE_ERR_INVALID_ARG
+    # a backward without the forward's saved H (routed; and shared, hs > 0)
+    need_t = abi.moe_workspace_bytes(d, abi.MOE_SAVE_FOR_BWD)
+    ptrs = [256] * 25
+    ptrs[13] = None
+    assert abi.moe_backward(d, *ptrs, 0x1000, need_t, None, check=False) == abi.MOE_ERR_INVALID_ARG
+    ds = abi.make_dims(64, 128, 128, 8, 2, 64, abi.MOE_F32)
+    need_s = abi.moe_workspace_bytes(ds, abi.MOE_SAVE_FOR_BWD)
+    ptrs = [256] * 25
+    ptrs[16] = None
+    assert abi.moe_backward(ds, *ptrs, 0x1000, need_s, None, check=False) == abi.MOE_ERR_INVALID_ARG
 
 
 def test_misaligned_row_data_rejected(lib):
@@ -113,10 +123,11 @@ def test_misaligned_row_data_rejected(lib):
                                    need, None, check=False) == abi.MOE_ERR_INVALID_ARG
     assert abi.moe_combine(d, 0, None, None, None, None, 0x2004, None, None, None, None, None,
                            0x1000, need, None, check=False) == abi.MOE_ERR_INVALID_ARG
-    ptrs = [256] * 23
-    ptrs[15] = 0x3002  # dx
-    assert abi.moe_backward(d, *ptrs[:15], *ptrs[15:23], 0x1000, need_t, None,
-                            check=False) == abi.MOE_ERR_INVALID_ARG
+    for pos in (13, 17):  # the saved H, dx
+        ptrs = [256] * 25
+        ptrs[pos] = 0x3002
+        assert abi.moe_backward(d, *ptrs, 0x1000, need_t, None,
+                                check=False) == abi.MOE_ERR_INVALID_ARG
 
 
 def test_capacity_routing_is_refused_by_the_allocation_free_sort(lib):
