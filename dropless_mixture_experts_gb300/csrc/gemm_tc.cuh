@@ -93,16 +93,21 @@ struct Params {
   int* status = nullptr;
 };
 
-template <int AK_, int BKIND_, int EK_, int BN_, bool ROUTED_>
+// PAIR: a two-CTA cluster computes one 256 x BN tile with tcgen05's
+// cta_group::2 MMA: each CTA loads its own 128 rows of A and half of B's
+// columns (half the operand bytes per SM per FLOP of a single-CTA tile),
+// the even CTA issues the MMAs, each CTA's epilogue drains its own rows.
+template <int AK_, int BKIND_, int EK_, int BN_, bool ROUTED_, bool PAIR_ = false>
 struct Cfg {
   static constexpr int AK = AK_, BKIND = BKIND_, EK = EK_, BN = BN_;
   static constexpr bool ROUTED = ROUTED_;
+  static constexpr bool PAIR = PAIR_;
   static constexpr bool DW = EK == E_DW;
   static constexpr bool DUALN = EK == E_GU;
   static constexpr bool DUALK = EK == E_DX;
   static constexpr int BM = 128, BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per-warp staging: 2 KB per bf16 32x32 tile
   static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048
@@ -117,12 +122,13 @@ struct Cfg {
 
   static constexpr bool A_MN = AK == A_MN_TMA;
   static constexpr bool B_MN = BKIND == B_MN_TMA;
-  static constexpr uint32_t IDESC = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+  static constexpr uint32_t IDESC = tc::idesc_bf16(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + FIXED;
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(!DUALN || BN >= 128, "the gate/up tile holds 64-column halves");
   static_assert(STAGES >= 2, "shared memory");
+  static_assert(!PAIR || (DW && B_MN && BN >= 128), "pairs: weight-gradient kinds");
 };
 
 struct Tile {
@@ -183,7 +189,7 @@ __device__ inline void dw_chunk_schedule(const int* counts, int E, int tiles_per
 // range, which is the same for every tile of those kinds).
 template <class C, bool META = true>
 __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles, Tile& tl,
-                                         const int* choff = nullptr) {
+                                         const int* choff = nullptr, int rank = 0) {
   if constexpr (!C::DW) {
     const int mt = t / p.n_nt;
     tl.nt = t % p.n_nt;
@@ -210,8 +216,12 @@ __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles,
   } else {
     tl.nt = t % p.n_nt;
     int r = t / p.n_nt;
-    const int mt = r % p.n_mt;
-    r /= p.n_mt;
+    // output row units: 128-row tiles, or 256-row tiles of a CTA pair (this
+    // CTA takes the half of its rank)
+    const int n_mu = C::PAIR ? p.n_mt / 2 : p.n_mt;
+    const int mu = r % n_mu;
+    r /= n_mu;
+    const int mt = C::PAIR ? 2 * mu + rank : mu;
     int s, ns;
     int64_t ne;
     if constexpr (C::ROUTED) {
@@ -261,12 +271,19 @@ struct Shared {
   volatile int fixup;        // routed DW: this CTA finishes the tile's chunk sum
 };
 
+// CLUSTER: a barrier of a CTA pair (arrivals from the other CTA, or from
+// the pair's MMA completions): polled without suspending, cluster-scope
+// acquire.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Shared* sh,
                                               int* status, int where) {
-  if (tc::mbar_try_wait(bar, parity)) return true;
+  auto try_wait = [&] {
+    return CLUSTER ? tc::mbar_test_wait_cluster(bar, parity) : tc::mbar_try_wait(bar, parity);
+  };
+  if (try_wait()) return true;
   const uint64_t t0 = tc::globaltimer();
   while (true) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     if (sh->abort) return false;
     if (tc::globaltimer() - t0 > 2000000000ull) {
       sh->abort = 1;
@@ -448,15 +465,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared* sh = reinterpret_cast<Shared*>(epi + kEpiWarps * C::EPI_BYTES);
   int* choff = reinterpret_cast<int*>(sh + 1);  // routed DW kinds: the chunk schedule
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // work units: one per CTA, or one per CTA pair (both CTAs walk the same units)
+  const int rank = C::PAIR ? (int)tc::cluster_ctarank() : 0;
+  const int u0 = C::PAIR ? (int)tc::cluster_id_x() : (int)blockIdx.x;
+  const int us = C::PAIR ? (int)tc::ncluster_x() : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
+    // a pair's even CTA: its full barriers count both CTAs' operand bytes
+    // (one arrival, its own producer's), its accumulator-empty barriers both
+    // CTAs' epilogue warps
+    const int both = C::PAIR && rank == 0 ? 2 : 1;
     for (int s = 0; s < C::STAGES; ++s) {
       tc::mbar_init(&sh->full[s], 1);
       tc::mbar_init(&sh->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(&sh->tfull[a], 1);
-      tc::mbar_init(&sh->tempty[a], kEpiWarps);
+      tc::mbar_init(&sh->tempty[a], kEpiWarps * both);
     }
     for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&sh->ebar[w], 1);
     tc::mbar_init(&sh->epi_bar, kEpiWarps);
@@ -465,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if constexpr (C::DW && C::ROUTED) {
     if (warp == 2)  // an epilogue warp (idle until the first tile is ready)
-      dw_chunk_schedule(p.counts, p.experts, p.n_mt * p.n_nt, gridDim.x, choff);
+      dw_chunk_schedule(p.counts, p.experts, (C::PAIR ? p.n_mt / 2 : p.n_mt) * p.n_nt, us,
+                        choff);
   }
   if constexpr (C::EK == E_DZ && C::ROUTED) {
     // the chunk tickets of the weight-gradient launches that follow start at 0
@@ -477,7 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tma_prefetch_desc(&m.b0);
     tc::tma_prefetch_desc(&m.b1);
   }
-  if (warp == 1) {
+  if constexpr (C::PAIR) {
+    // both CTAs' barriers are initialised before either signals the other's
+    tc::cluster_sync();
+    if (warp == 1) {
+      tc::tmem_alloc_pair(&sh->tmem_base, C::TMEM_COLS);
+      tc::tmem_relinquish_pair();
+    }
+  } else if (warp == 1) {
     tc::tmem_alloc(&sh->tmem_base, C::TMEM_COLS);
     tc::tmem_relinquish();
   }
@@ -496,18 +529,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       Tile tl;
-      for (int t = blockIdx.x; !aborted && get_tile<C>(p, t, nrow_tiles, tl, choff); t += gridDim.x) {
+      for (int t = u0; !aborted && get_tile<C>(p, t, nrow_tiles, tl, choff, rank); t += us) {
         int brow0 = 0;
         if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
         if constexpr (C::DW) brow0 = tl.row0;
         for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-          if (!wait_or_abort(&sh->empty[stage], phase ^ 1, sh, p.status, 100)) {
+          if (!wait_or_abort<C::PAIR>(&sh->empty[stage], phase ^ 1, sh, p.status, 100)) {
             aborted = true;
             break;
           }
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
           uint64_t* fb = &sh->full[stage];
+          if constexpr (C::PAIR) {
+            // both CTAs' copies complete on the even CTA's barrier, which
+            // expects the bytes of both
+            const uint32_t fbc = tc::peer_addr(fb, 0);
+            if (rank == 0) tc::mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+            const int krow = tl.row0 + kb * C::BK;
+            tc::tma_load_2d_pair(sA, &m.a, fbc, tl.m0, krow);
+            tc::tma_load_2d_pair(sA + 8192, &m.a, fbc, tl.m0 + 64, krow);
+#pragma unroll
+            for (int j = 0; j < C::BN / 128; ++j)
+              tc::tma_load_2d_pair(sB + j * 8192, &m.b0, fbc,
+                                   tl.n0 + rank * (C::BN / 2) + 64 * j, krow);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           // ---- A ----
           if constexpr (C::AK == A_K_TMA) {
@@ -538,21 +589,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == 1 && C::PAIR && rank == 1) {
+    // odd CTA of a pair: the even CTA issues the pair's MMAs
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     int stage = 0, acc = 0;
     uint32_t phase = 0, aphase = 0;
     Tile tl;
-    for (int t = blockIdx.x; !aborted && get_tile<C, false>(p, t, nrow_tiles, tl, choff);
-         t += gridDim.x) {
-      if (!wait_or_abort(&sh->tempty[acc], aphase ^ 1, sh, p.status, 200)) {
+    for (int t = u0; !aborted && get_tile<C, false>(p, t, nrow_tiles, tl, choff, rank);
+         t += us) {
+      if (!wait_or_abort<C::PAIR>(&sh->tempty[acc], aphase ^ 1, sh, p.status, 200)) {
         aborted = true;
         break;
       }
       tc::tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * C::BN;
       for (int kb = tl.kb0; kb < tl.kb1; ++kb) {
-        if (!wait_or_abort(&sh->full[stage], phase, sh, p.status, 300)) {
+        if (!wait_or_abort<C::PAIR>(&sh->full[stage], phase, sh, p.status, 300)) {
           aborted = true;
           break;
         }
@@ -566,9 +619,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         : tc::sw128_desc(a0 + s * 32, 0, 1024);
             const uint64_t bd = C::B_MN ? tc::sw128_desc(b0 + s * 2048, 8192, 1024)
                                         : tc::sw128_desc(b0 + s * 32, 0, 1024);
-            tc::mma_bf16(d_tmem, ad, bd, C::IDESC, (kb > tl.kb0 || s > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > tl.kb0 || s > 0) ? 1u : 0u;
+            if constexpr (C::PAIR) tc::mma_bf16_pair(d_tmem, ad, bd, C::IDESC, accum);
+            else tc::mma_bf16(d_tmem, ad, bd, C::IDESC, accum);
           }
-          tc::mma_commit(&sh->empty[stage]);
+          if constexpr (C::PAIR) tc::mma_commit_pair(&sh->empty[stage]);
+          else tc::mma_commit(&sh->empty[stage]);
         }
         __syncwarp();
         if (++stage == C::STAGES) {
@@ -577,7 +633,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (aborted) break;
-      if (lane == 0) tc::mma_commit(&sh->tfull[acc]);
+      if (lane == 0) {
+        if constexpr (C::PAIR) tc::mma_commit_pair(&sh->tfull[acc]);
+        else tc::mma_commit(&sh->tfull[acc]);
+      }
       __syncwarp();
       if (++acc == 2) {
         acc = 0;
@@ -599,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t aphase = 0, epi_phase = 0;
     Tile tl, tn;
-    int t = blockIdx.x;
-    bool have = get_tile<C>(p, t, nrow_tiles, tl, choff);
+    int t = u0;
+    bool have = get_tile<C>(p, t, nrow_tiles, tl, choff, rank);
     // DZ: saved a_g / a_u of this warp's first chunk, loaded ahead of the MMA
     if constexpr (C::EK == E_DZ) {
       if (have && lane == 0) {
@@ -611,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     while (have && !aborted) {
       // the next tile's metadata is read while this one is processed
-      const bool have_next = get_tile<C>(p, t + gridDim.x, nrow_tiles, tn, choff);
+      const bool have_next = get_tile<C>(p, t + us, nrow_tiles, tn, choff, rank);
       // per-row metadata of this tile (routed kinds): issued before the wait
       int32_t pr = -1;
       float gt = 1.f;
@@ -623,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           gt = 0.f;
         }
       }
-      if (!wait_or_abort(&sh->tfull[acc], aphase, sh, p.status, 400)) {
+      if (!wait_or_abort<C::PAIR>(&sh->tfull[acc], aphase, sh, p.status, 400)) {
         aborted = true;
         break;
       }
@@ -849,7 +908,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sh->tempty[acc]);
+      if (lane == 0) {
+        // a pair's MMA issuer (even CTA) waits for both CTAs' epilogues
+        if (C::PAIR && rank == 1) tc::mbar_arrive_cluster(tc::peer_addr(&sh->tempty[acc], 0));
+        else tc::mbar_arrive(&sh->tempty[acc]);
+      }
       if constexpr (C::DW && C::ROUTED) {
         if (tl.ns > 1 && !dw_chunk_fixup<C>(p, tl, choff, sh, row, half, epi_phase)) {
           aborted = true;
@@ -860,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc = 0;
         aphase ^= 1;
       }
-      t += gridDim.x;
+      t += us;
       tl = tn;
       have = have_next;
     }
@@ -878,8 +941,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  tc::tc_fence_after();
-  if (warp == 1) tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  if constexpr (C::PAIR) {
+    // neither CTA leaves while the even CTA's MMAs may still touch the odd
+    // CTA's shared or tensor memory, or the odd CTA may still arrive on the
+    // even CTA's barriers
+    tc::cluster_sync();
+    tc::tc_fence_after();
+    if (warp == 1) tc::tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  } else {
+    tc::tc_fence_after();
+    if (warp == 1) tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -907,8 +979,37 @@ void launch_tc(const Maps& maps, const Params& p, int64_t max_tiles, const char*
     attr = true;
   }
   const int sms = sm_count();
-  const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-  MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, s>>>(maps, p));
+  if constexpr (C::PAIR) {
+    // max_tiles counts pair units; two CTAs (one cluster) per unit, no more
+    // clusters than can be resident at once (an SM whose partner SM is not
+    // available takes no pair, and a cluster left for a second wave would
+    // double the persistent schedule's time)
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr1[1];
+    attr1[0].id = cudaLaunchAttributeClusterDimension;
+    attr1[0].val.clusterDim.x = 2;
+    attr1[0].val.clusterDim.y = 1;
+    attr1[0].val.clusterDim.z = 1;
+    cfg.attrs = attr1;
+    cfg.numAttrs = 1;
+    static int resident = 0;
+    if (resident == 0) {
+      cfg.gridDim = dim3(sms, 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1)
+        n = sms / 2;
+      resident = n;
+    }
+    const int pairs = (int)(max_tiles < resident ? max_tiles : resident);
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    MOE_LAUNCH(name, s, cudaLaunchKernelEx(&cfg, tc_gemm_kernel<C>, maps, p));
+  } else {
+    const int grid = (int)(max_tiles < sms ? max_tiles : sms);
+    MOE_LAUNCH(name, s, tc_gemm_kernel<C><<<grid, kThreads, C::SMEM_BYTES, s>>>(maps, p));
+  }
 }
 
 }  // namespace tcg

@@ -125,12 +125,18 @@ void reduce_splits(const Params& q, float* out0, float* out1, cudaStream_t s) {
 // (balanced against the row counts; the last chunk of a tile to finish sums
 // the chunks' partials); the work units are bounded by
 // (E + grid / tiles_per_expert + 1) chunks.
-int64_t set_chunks(Params& q, const Layout& L, void* ws) {
+// With CTA pairs (pair = true) a unit covers two row tiles and the grid
+// holds half as many units.
+int64_t set_chunks(Params& q, const Layout& L, void* ws, bool pair = false) {
   q.part = at<float>(ws, L.dwpart);
   q.dw_tick = at<int>(ws, L.dw_tick);
-  const int64_t tpe = (int64_t)q.n_mt * q.n_nt;
-  return (q.experts + sm_count() / tpe + 1) * tpe;
+  const int64_t tpe = (int64_t)(pair ? q.n_mt / 2 : q.n_mt) * q.n_nt;
+  const int64_t grid = pair ? sm_count() / 2 : sm_count();
+  return (q.experts + grid / tpe + 1) * tpe;
 }
+
+// Routed weight-gradient launches run as CTA pairs (256 output rows per
+// unit) when the output rows split into 256-row units and BN >= 128.
 
 // dW_down[e] = sum over the expert's rows of H_r^T (g dy)_r: A = the
 // forward's saved H (MN-major: rows are K), B = the gate-scaled sorted dy
@@ -158,8 +164,14 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(mp, q, set_chunks(q, L, ws),
-                                                        "tc_dw_down", s);
+    if constexpr (BN >= 128) {
+      if (h % 256 == 0) {
+        launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true, true>>(
+            mp, q, set_chunks(q, L, ws, true), "tc_dw_down", s);
+        return true;
+      }
+    }
+    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(mp, q, set_chunks(q, L, ws), "tc_dw_down", s);
     return true;
   } else {
     set_splits(q, L, ws, (d.tokens + 63) / 64, false);
@@ -202,8 +214,14 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(mp, q, set_chunks(q, L, ws),
-                                                        "tc_dw_gateup", s);
+    if constexpr (BN >= 128) {
+      if (dm % 256 == 0) {
+        launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true, true>>(
+            mp, q, set_chunks(q, L, ws, true), "tc_dw_gateup", s);
+        return true;
+      }
+    }
+    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true>>(mp, q, set_chunks(q, L, ws), "tc_dw_gateup", s);
     return true;
   } else {
     set_splits(q, L, ws, (d.tokens + 63) / 64, false);
