@@ -12,7 +12,8 @@
 
 namespace moe {
 
-constexpr int kRowPad = 128;      // each expert's sorted rows start on a multiple of this
+constexpr int kRowPad = 256;      // the largest expert row padding (row_pad: 128 or 256)
+constexpr int kTileRows = 128;    // rows of one tile-list entry
 constexpr int kPermRounds = 16;   // 32-pair rounds per warp chunk in the counting sort
 constexpr int kPermChunk = 32 * kPermRounds;
 constexpr int kMaxExperts = 256;
@@ -81,14 +82,40 @@ struct Layout {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-inline int64_t padded_rows(const moe_dims& d) {
-  int64_t P = d.tokens * (int64_t)d.top_k;
-  int64_t cap = P + (int64_t)d.experts * (kRowPad - 1);
-  return (cap + kRowPad - 1) / kRowPad * kRowPad;
-}
-
 // Column tile of a grouped GEMM with n output columns.
 inline int pick_bn(int n) { return n % 256 == 0 ? 256 : n % 128 == 0 ? 128 : 64; }
+
+// CTA pairs (tcgen05 cta_group::2, 256 x 256 tiles over two SMs) halve the
+// B operand bytes each SM receives per FLOP.  They pay where the tensor
+// cores bound the GEMM and the column tile is 256 wide:
+//   a row GEMM with K-deep rows and N output columns moves a row of A in
+//   and a row of D out per 2*K*N FLOPs, K*N/(K+N) FLOPs per byte; at 300 and
+//   above it is past the ratio of the bf16 tensor peak to the HBM rate
+//   (about 280 on GB300), below it is HBM-bound and pairs measured slower;
+//   the weight-gradient GEMMs pair whenever BN = 256 and M splits into
+//   256-row units.
+inline bool row_gemm_pairs(int64_t K, int64_t N) {
+  return pick_bn((int)N) == 256 && K * N >= 300 * (K + N);
+}
+// the down projection (K = h) and the input-gradient GEMM (K = 2h), N = d
+inline bool down_pairs(int64_t h, int64_t dm) { return row_gemm_pairs(h, dm); }
+inline bool dx_pairs(int64_t h, int64_t dm) { return row_gemm_pairs(2 * h, dm); }
+
+// Expert row padding: 256 when a routed row GEMM runs as CTA pairs (a pair
+// takes two 128-row tiles of one expert), else 128.
+inline int row_pad(const moe_dims& d) {
+  return d.dtype == MOE_BF16 && (down_pairs(d.d_hidden, d.d_model) ||
+                                 dx_pairs(d.d_hidden, d.d_model))
+             ? 256
+             : 128;
+}
+
+inline int64_t padded_rows(const moe_dims& d) {
+  const int pad = row_pad(d);
+  int64_t P = d.tokens * (int64_t)d.top_k;
+  int64_t cap = P + (int64_t)d.experts * (pad - 1);
+  return (cap + pad - 1) / pad * pad;
+}
 
 // Most K splits a weight-gradient GEMM with `tiles` output tiles may use
 // (a power of two; 1 when the tiles alone fill any GPU of <= 256 SMs).
@@ -112,7 +139,7 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.elem = d.dtype == MOE_BF16 ? 2 : 4;
   L.P = d.tokens * (int64_t)d.top_k;
   L.PPcap = padded_rows(d);
-  L.MTcap = L.PPcap / kRowPad;
+  L.MTcap = L.PPcap / kTileRows;
   L.NWc = (L.P + kPermChunk - 1) / kPermChunk;
   const int64_t E = d.experts, T = d.tokens, h = d.d_hidden, dm = d.d_model,
                 hs = d.shared_hidden;

@@ -128,7 +128,7 @@ struct Cfg {
   static_assert(BN == 64 || BN == 128 || BN == 256, "BN");
   static_assert(!DUALN || BN >= 128, "the gate/up tile holds 64-column halves");
   static_assert(STAGES >= 2, "shared memory");
-  static_assert(!PAIR || (DW && B_MN && BN >= 128), "pairs: weight-gradient kinds");
+  static_assert(!PAIR || (EK != E_ROUTER && BN >= 128), "pairs: BN >= 128, no router");
 };
 
 struct Tile {
@@ -191,9 +191,12 @@ template <class C, bool META = true>
 __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles, Tile& tl,
                                          const int* choff = nullptr, int rank = 0) {
   if constexpr (!C::DW) {
-    const int mt = t / p.n_nt;
+    // row tiles of 128 rows; a pair takes two consecutive ones (the same
+    // expert: each expert's rows are padded to 256)
+    const int mu = t / p.n_nt;
     tl.nt = t % p.n_nt;
-    if (mt >= nrow_tiles) return false;
+    const int mt = C::PAIR ? 2 * mu + rank : mu;
+    if ((C::PAIR ? 2 * mu : mt) >= nrow_tiles) return false;
     if constexpr (C::ROUTED) {
       if constexpr (META) {
         const int4 v = p.tiles[mt];
@@ -207,7 +210,7 @@ __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles,
       tl.e = 0;
       tl.row0 = mt * C::BM;
       const int64_t left = p.rows - tl.row0;
-      tl.nvalid = left < C::BM ? (int)left : C::BM;
+      tl.nvalid = left < C::BM ? (left > 0 ? (int)left : 0) : C::BM;
     }
     tl.m0 = 0;
     tl.n0 = tl.nt * (C::DUALN ? C::BN / 2 : C::BN);
@@ -541,45 +544,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sA = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sA + C::A_BYTES;
           uint64_t* fb = &sh->full[stage];
-          if constexpr (C::PAIR) {
-            // both CTAs' copies complete on the even CTA's barrier, which
-            // expects the bytes of both
-            const uint32_t fbc = tc::peer_addr(fb, 0);
-            if (rank == 0) tc::mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
-            const int krow = tl.row0 + kb * C::BK;
-            tc::tma_load_2d_pair(sA, &m.a, fbc, tl.m0, krow);
-            tc::tma_load_2d_pair(sA + 8192, &m.a, fbc, tl.m0 + 64, krow);
-#pragma unroll
-            for (int j = 0; j < C::BN / 128; ++j)
-              tc::tma_load_2d_pair(sB + j * 8192, &m.b0, fbc,
-                                   tl.n0 + rank * (C::BN / 2) + 64 * j, krow);
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
-            continue;
-          }
-          tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          // a pair: both CTAs' copies complete on the even CTA's barrier,
+          // which expects the bytes of both
+          const uint32_t fbc = C::PAIR ? tc::peer_addr(fb, 0) : 0u;
+          if (!C::PAIR) tc::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          else if (rank == 0) tc::mbar_arrive_expect_tx(fb, 2 * C::STAGE_BYTES);
+          auto load = [&](void* dst, const CUtensorMap* mp, int x, int y) {
+            if constexpr (C::PAIR) tc::tma_load_2d_pair(dst, mp, fbc, x, y);
+            else tc::tma_load_2d(dst, mp, fb, x, y);
+          };
           // ---- A ----
           if constexpr (C::AK == A_K_TMA) {
-            tc::tma_load_2d(sA, &m.a, fb, kb * C::BK, tl.row0);
+            load(sA, &m.a, kb * C::BK, tl.row0);
           } else {  // MN-major: two 64-column blocks of 64 K rows
             const int krow = (C::DW ? tl.row0 : 0) + kb * C::BK;
-            tc::tma_load_2d(sA, &m.a, fb, tl.m0, krow);
-            tc::tma_load_2d(sA + 8192, &m.a, fb, tl.m0 + 64, krow);
+            load(sA, &m.a, tl.m0, krow);
+            load(sA + 8192, &m.a, tl.m0 + 64, krow);
           }
-          // ---- B ----
+          // ---- B ----  (a pair holds half of B's columns per CTA; gate/up:
+          // the even CTA the gate half, the odd CTA the up half)
+          constexpr int BNL = C::PAIR ? C::BN / 2 : C::BN;
+          const int nb0 = tl.n0 + (C::PAIR && !C::DUALN ? rank * BNL : 0);
           if constexpr (C::BKIND == B_MN_TMA) {
 #pragma unroll
-            for (int j = 0; j < C::BN / 64; ++j) {
-              const bool second = C::DUALN && j >= C::BN / 128;
-              const int x = C::DUALN ? tl.n0 + 64 * (second ? j - C::BN / 128 : j) : tl.n0 + 64 * j;
-              tc::tma_load_2d(sB + j * 8192, second ? &m.b1 : &m.b0, fb, x, brow0 + kb * C::BK);
+            for (int j = 0; j < BNL / 64; ++j) {
+              const CUtensorMap* mp = &m.b0;
+              int x = nb0 + 64 * j;
+              if constexpr (C::DUALN && C::PAIR) {
+                if (rank) mp = &m.b1;
+              } else if constexpr (C::DUALN) {
+                const bool second = j >= C::BN / 128;
+                x = tl.n0 + 64 * (second ? j - C::BN / 128 : j);
+                if (second) mp = &m.b1;
+              }
+              load(sB + j * 8192, mp, x, brow0 + kb * C::BK);
             }
-          } else {
+          } else {  // K-major: BNL rows of 64 K (the tensor map's box)
             const bool second = C::DUALK && kb >= p.kb_split;
             const int x = (second ? kb - p.kb_split : kb) * C::BK;
-            tc::tma_load_2d(sB, second ? &m.b1 : &m.b0, fb, x, brow0 + tl.n0);
+            load(sB, second ? &m.b1 : &m.b0, x, brow0 + nb0);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -690,6 +693,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tacc = tmem_base + ((uint32_t)(32 * q) << 16) + acc * C::BN;
       const bool has_k = tl.kb1 > tl.kb0;
       const int yrow = tl.row0 + 32 * q;  // first row of this warp's tiles
+      // dense row kinds: a pair's odd CTA may hold a tile past the last token
+      // (odd tile count); its stores are skipped
+      const bool ystore = C::ROUTED || (int64_t)yrow < p.rows;
 
       if constexpr (C::EK == E_GU) {
         // H = silu(a_g) * a_u with a_g, a_u rounded to bf16 first (the values
@@ -762,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage_write_row(stg, lane, o);
           tc::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
+          if (lane == 0 && ystore) {
             tc::tma_store_2d(&m.o0, stg, tl.n0 + 32 * c, yrow);
             tc::bulk_commit();
           }
@@ -817,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage_write_row(stg + 6144, lane, dau);
           tc::fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
+          if (lane == 0 && ystore) {
             const int x = tl.n0 + 32 * c;
             tc::tma_store_2d(&m.o0, stg + 4096, x, yrow);
             tc::tma_store_2d(&m.o0, stg + 6144, h + x, yrow);

@@ -9,8 +9,9 @@
 // Permutation: the `sort_permute` piece of kernel_gmm_gpu.json (dispatch
 // `sorted`): pairs p = t*k + j ordered by expert, stable in p, plus an
 // expert-padded copy of the order in which every expert's rows start on a
-// multiple of 128 (the row tiles of the grouped GEMMs never straddle two
-// experts) and the token of every padded row.
+// multiple of 128, or of 256 where the grouped GEMMs run CTA pairs over
+// 256-row units (tiles never straddle two experts), and the token of every
+// padded row.
 #include "kernels.cuh"
 
 namespace moe {
@@ -339,7 +340,7 @@ __global__ void __launch_bounds__(1024) perm_colscan_kernel(const int* __restric
 // device status (an index the histogram pass rejected is rejected again by
 // the scatter pass) and the combine's block ticket.  s_off / s_poff receive
 // the offsets the scatter pass uses.
-__device__ void finalize_block(int* __restrict__ counts_ws, int E, int capacity, int64_t P,
+__device__ void finalize_block(int* __restrict__ counts_ws, int E, int capacity, int pad, int64_t P,
                                int32_t* counts_out, int32_t* offsets_out, int* poff, int4* tiles,
                                int* ntiles, int32_t* rowpair, int32_t* perm, int* status,
                                int* loss_tick, int* s_off, int* s_poff) {
@@ -356,8 +357,11 @@ __device__ void finalize_block(int* __restrict__ counts_ws, int E, int capacity,
     for (int base = 0; base < E; base += 32) {
       const int e = base + lane;
       const int c = e < E ? s_cnt[e] : 0;
-      const int nt = (c + kRowPad - 1) / kRowPad;
-      int ic = c, ip = nt * kRowPad, it = nt;  // inclusive scans over the lanes
+      // padded to `pad` rows, listed as kTileRows-row tiles (the last
+      // one of an expert may hold no rows when pad = 256)
+      const int np = (c + pad - 1) / pad;
+      const int nt = np * (pad / kTileRows);
+      int ic = c, ip = np * pad, it = nt;  // inclusive scans over the lanes
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int vc = __shfl_up_sync(0xffffffffu, ic, d);
@@ -371,7 +375,7 @@ __device__ void finalize_block(int* __restrict__ counts_ws, int E, int capacity,
       }
       if (e < E) {
         s_off[e] = o + ic - c;
-        s_poff[e] = po + ip - nt * kRowPad;
+        s_poff[e] = po + ip - np * pad;
         s_toff[e] = to + it - nt;
       }
       o += __shfl_sync(0xffffffffu, ic, 31);
@@ -404,22 +408,22 @@ __device__ void finalize_block(int* __restrict__ counts_ws, int E, int capacity,
     const int c = s_cnt[e];
     const int nt = s_toff[e + 1] - s_toff[e];
     for (int j = lane; j < nt; j += 32) {
-      const int valid = min(kRowPad, c - j * kRowPad);
-      tiles[s_toff[e] + j] = make_int4(e, s_poff[e] + j * kRowPad, valid, 0);
+      const int valid = max(0, min(kTileRows, c - j * kTileRows));
+      tiles[s_toff[e] + j] = make_int4(e, s_poff[e] + j * kTileRows, valid, 0);
     }
     for (int r = s_poff[e] + c + lane; r < s_poff[e + 1]; r += 32) rowpair[r] = -1;
   }
 }
 
 __global__ void __launch_bounds__(1024) perm_finalize_kernel(int* __restrict__ counts_ws, int E,
-                                                             int capacity, int64_t P,
+                                                             int capacity, int pad, int64_t P,
                                                              int32_t* counts_out,
                                                              int32_t* offsets_out, int* poff,
                                                              int4* tiles, int* ntiles,
                                                              int32_t* rowpair, int32_t* perm,
                                                              int* status, int* loss_tick) {
   __shared__ int s_off[kMaxExperts + 1], s_poff[kMaxExperts + 1];
-  finalize_block(counts_ws, E, capacity, P, counts_out, offsets_out, poff, tiles, ntiles, rowpair,
+  finalize_block(counts_ws, E, capacity, pad, P, counts_out, offsets_out, poff, tiles, ntiles, rowpair,
                  perm, status, loss_tick, s_off, s_poff);
 }
 
@@ -466,7 +470,7 @@ void launch_permute(const moe_dims& d, const Layout& L, const int32_t* idx, int3
     zero_fill_i32(counts_ws, E, s);
   }
   MOE_LAUNCH("perm_finalize", s,
-             perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, d.capacity, L.P, counts,
+             perm_finalize_kernel<<<1, 1024, 0, s>>>(counts_ws, E, d.capacity, row_pad(d), L.P, counts,
                                                      offsets, poff, tiles, ntiles, rowpair,
                                                      perm, status, at<int>(ws, L.loss_tick)));
   if (NW > 0)

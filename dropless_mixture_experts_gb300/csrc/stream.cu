@@ -82,9 +82,9 @@ __global__ void __launch_bounds__(kThreads)
     scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ pairrow,
                         const float* __restrict__ gates, uint4* __restrict__ out, int64_t Tn,
                         int cpt, int k, const int32_t* __restrict__ poff,
-                        const int32_t* __restrict__ counts, int E) {
+                        const int32_t* __restrict__ counts, int E, int pad) {
   const int64_t n = Tn * cpt;
-  const int64_t per_e = (int64_t)(kRowPad - 1) * cpt;
+  const int64_t per_e = (int64_t)(pad - 1) * cpt;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n + E * per_e;
        i += stride) {
@@ -366,13 +366,15 @@ void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, vo
                          cudaStream_t s, const float* gates) {
   if (d.tokens == 0) return;
   const int cpt = (int)((int64_t)d.d_model * L.elem / 16);
-  const int64_t items = d.tokens * cpt + (int64_t)d.experts * (kRowPad - 1) * cpt;
+  const int pad = row_pad(d);
+  const int64_t items = d.tokens * cpt + (int64_t)d.experts * (pad - 1) * cpt;
   auto launch = [&](auto kernel) {
     MOE_LAUNCH("scatter_rows", s,
                kernel<<<stream_grid(items, INT32_MAX), kThreads, 0, s>>>(
                    reinterpret_cast<const uint4*>(src), at<const int32_t>(ws, L.pairrow), gates,
                    reinterpret_cast<uint4*>(out), d.tokens, cpt, d.top_k,
-                   at<const int32_t>(ws, L.poff), at<const int32_t>(ws, L.counts), d.experts));
+                   at<const int32_t>(ws, L.poff), at<const int32_t>(ws, L.counts), d.experts,
+                   pad));
   };
   if (!gates) launch(scatter_rows_kernel<__nv_bfloat16, false>);
   else if (d.dtype == MOE_BF16) launch(scatter_rows_kernel<__nv_bfloat16, true>);

@@ -34,9 +34,12 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   if (!make_map_sw64(&mp.i0, routed ? p.a_gate : p.as_gate, rows, h)) return false;
   if (!make_map_sw64(&mp.i1, routed ? p.a_up : p.as_up, rows, h)) return false;
   mp.o1 = mp.o2 = mp.o0;
+  // single CTAs: this kernel is bound by its HBM traffic, which CTA pairs
+  // do not reduce (their coupled epilogues measured slower)
+  constexpr int BROWS = BN;
   if (routed) {
     if (!make_map(&mp.a, at<void>(ws, L.dys), L.PPcap, dm, 64, 128)) return false;
-    if (!make_map(&mp.b0, p.w_down, (uint64_t)d.experts * h, dm, 64, BN)) return false;
+    if (!make_map(&mp.b0, p.w_down, (uint64_t)d.experts * h, dm, 64, BROWS)) return false;
     mp.b1 = mp.b0;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
@@ -50,7 +53,7 @@ bool dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DZ, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_dz", s);
   } else {
     if (!make_map(&mp.a, p.dy, d.tokens, dm, 64, 128)) return false;
-    if (!make_map(&mp.b0, p.ws_down, h, dm, 64, BN)) return false;
+    if (!make_map(&mp.b0, p.ws_down, h, dm, 64, BROWS)) return false;
     mp.b1 = mp.b0;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
@@ -75,24 +78,42 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
   if (!make_map_sw64(&mp.o0, at<void>(ws, routed ? L.dxsort : L.dxs),
                      routed ? L.PPcap : d.tokens, dm))
     return false;
+  // CTA pairs where the tensor cores bound this GEMM (the routed rows are
+  // then padded to 256): BN / 2 rows of the K-major B per CTA
+  const bool pr = BN == 256 && dx_pairs(h, dm);
+  const int BROWS = pr ? BN / 2 : BN;
   if (routed) {
     if (!make_map(&mp.a, at<void>(ws, L.dA), L.PPcap, 2 * h, 64, 128)) return false;
-    if (!make_map(&mp.b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, BN)) return false;
-    if (!make_map(&mp.b1, p.w_up, (uint64_t)d.experts * dm, h, 64, BN)) return false;
+    if (!make_map(&mp.b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, BROWS)) return false;
+    if (!make_map(&mp.b1, p.w_up, (uint64_t)d.experts * dm, h, 64, BROWS)) return false;
     q.tiles = at<int4>(ws, L.tiles);
     q.ntiles_dev = at<int>(ws, L.ntiles);
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = dm;
+    if constexpr (BN == 256) {
+      if (pr) {
+        launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true, true>>(mp, q, L.MTcap / 2 * q.n_nt,
+                                                               "tc_dx", s);
+        return true;
+      }
+    }
     launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_dx", s);
   } else {
     if (!make_map(&mp.a, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 128)) return false;
-    if (!make_map(&mp.b0, p.ws_gate, dm, h, 64, BN)) return false;
-    if (!make_map(&mp.b1, p.ws_up, dm, h, 64, BN)) return false;
+    if (!make_map(&mp.b0, p.ws_gate, dm, h, 64, BROWS)) return false;
+    if (!make_map(&mp.b1, p.ws_up, dm, h, 64, BROWS)) return false;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
-    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt, "tc_dx_sh",
-                                                       s);
+    if constexpr (BN == 256) {
+      if (pr) {
+        launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false, true>>(
+            mp, q, (int64_t)(q.n_mt + 1) / 2 * q.n_nt, "tc_dx_sh", s);
+        return true;
+      }
+    }
+    launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt,
+                                                       "tc_dx_sh", s);
   }
   return true;
 }
@@ -136,7 +157,22 @@ int64_t set_chunks(Params& q, const Layout& L, void* ws, bool pair = false) {
 }
 
 // Routed weight-gradient launches run as CTA pairs (256 output rows per
-// unit) when the output rows split into 256-row units and BN >= 128.
+// unit) when the output rows split into 256-row units and BN = 256.
+
+// A dense (shared-expert) weight-gradient launch with M output rows: CTA
+// pairs when the rows split into 256-row units and BN = 256.
+template <int BN>
+void launch_dense_dw(const Maps& mp, const Params& q, int M, const char* name, cudaStream_t s) {
+  if constexpr (BN == 256) {
+    if (M % 256 == 0) {
+      launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false, true>>(
+          mp, q, (int64_t)(q.n_mt / 2) * q.n_nt * q.splits, name, s);
+      return;
+    }
+  }
+  launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt * q.splits,
+                                                      name, s);
+}
 
 // dW_down[e] = sum over the expert's rows of H_r^T (g dy)_r: A = the
 // forward's saved H (MN-major: rows are K), B = the gate-scaled sorted dy
@@ -164,7 +200,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    if constexpr (BN >= 128) {
+    if constexpr (BN == 256) {
       if (h % 256 == 0) {
         launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true, true>>(
             mp, q, set_chunks(q, L, ws, true), "tc_dw_down", s);
@@ -179,8 +215,7 @@ bool dw_down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, b
     if (!make_map(&mp.b0, p.dy, d.tokens, dm, 64, 64)) return false;
     mp.b1 = mp.b0;
     q.rows = d.tokens;
-    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
-        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_down_sh", s);
+    launch_dense_dw<BN>(mp, q, h, "tc_dw_down_sh", s);
   }
   reduce_splits(q, out, nullptr, s);
   return true;
@@ -214,7 +249,7 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     mp.b1 = mp.b0;
     q.counts = at<int>(ws, L.counts);
     q.poff = at<int>(ws, L.poff);
-    if constexpr (BN >= 128) {
+    if constexpr (BN == 256) {
       if (dm % 256 == 0) {
         launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, true, true>>(
             mp, q, set_chunks(q, L, ws, true), "tc_dw_gateup", s);
@@ -229,8 +264,7 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
     if (!make_map(&mp.b0, at<void>(ws, L.dAs), d.tokens, 2 * h, 64, 64)) return false;
     mp.b1 = mp.b0;
     q.rows = d.tokens;
-    launch_tc<Cfg<A_MN_TMA, B_MN_TMA, E_DW, BN, false>>(
-        mp, q, (int64_t)q.n_mt * q.n_nt * q.splits, "tc_dw_gateup_sh", s);
+    launch_dense_dw<BN>(mp, q, dm, "tc_dw_gateup_sh", s);
   }
   reduce_splits(q, g, u, s);
   return true;

@@ -1,4 +1,6 @@
-// Forward launches of the tensor-core GEMMs (bf16 storage): the token rows
+// Forward launches of the tensor-core GEMMs (bf16 storage; the down
+// projection runs as CTA pairs of 256 rows where the tensor cores bound it,
+// the store-heavy gate/up projection on single CTAs): the token rows
 // are first gathered into expert-sorted order (one HBM pass), then
 //   gate/up projection of the sorted rows with SwiGLU in the epilogue, and
 //   the down projection with the gate-weighted combine in the epilogue;
@@ -81,6 +83,13 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
     q.top_k = d.top_k;
     q.brow_stride = h;
     q.gates = p.gates;
+    if constexpr (BN == 256) {
+      if (down_pairs(h, dm)) {  // the expert rows are then padded to 256
+        launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, true, true>>(mp, q, L.MTcap / 2 * q.n_nt,
+                                                                  "tc_down", s);
+        return true;
+      }
+    }
     launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, true>>(mp, q, L.MTcap * q.n_nt, "tc_down", s);
   } else {
     if (!make_map(&mp.a, p.hs_buf, d.tokens, h, 64, 128)) return false;
@@ -88,6 +97,13 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
     mp.b1 = mp.b0;
     q.rows = d.tokens;
     q.n_mt = (int)((d.tokens + 127) / 128);
+    if constexpr (BN == 256) {
+      if (down_pairs(h, dm)) {
+        launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, false, true>>(
+            mp, q, (int64_t)(q.n_mt + 1) / 2 * q.n_nt, "tc_down_sh", s);
+        return true;
+      }
+    }
     launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, false>>(mp, q, (int64_t)q.n_mt * q.n_nt,
                                                           "tc_down_sh", s);
   }

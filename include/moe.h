@@ -45,7 +45,7 @@
  *   check) do not fault: they set a code in the workspace that
  *   moe_read_device_status returns.
  * - Expert-sorted activation buffers (h_buf, a_gate_saved, a_up_saved) hold
- *   moe_padded_rows() rows: each expert's rows start on a multiple of 128 and
+ *   moe_padded_rows() rows: each expert's rows start on a multiple of 256 and
  *   the rows between experts are padding.
  */
 #ifndef MOE_GB300_H

@@ -45,7 +45,14 @@ def test_workspace_and_padded_rows(lib):
     fwd = abi.moe_workspace_bytes(d, abi.MOE_FWD_ONLY)
     train = abi.moe_workspace_bytes(d, abi.MOE_SAVE_FOR_BWD)
     assert 0 < fwd < train
-    assert abi.moe_padded_rows(d) == ((32768 * 2 + 8 * 127 + 127) // 128) * 128
+    # h = 1024, d = 512: the down and input-gradient GEMMs run as CTA pairs
+    # over 256-row units, so each expert's rows are padded to 256
+    assert abi.moe_padded_rows(d) == ((32768 * 2 + 8 * 255 + 255) // 256) * 256
+    # fine-grained experts (h = 128, HBM-bound: single CTAs) and float32: 128
+    d1 = abi.make_dims(16384, 512, 128, 64, 8, 1024, abi.MOE_BF16)
+    assert abi.moe_padded_rows(d1) == ((16384 * 8 + 64 * 127 + 127) // 128) * 128
+    d2 = abi.make_dims(32768, 512, 1024, 8, 2, 0, abi.MOE_F32)
+    assert abi.moe_padded_rows(d2) == ((32768 * 2 + 8 * 127 + 127) // 128) * 128
     d0 = abi.make_dims(0, 512, 1024, 8, 2, 0, abi.MOE_BF16)
     assert abi.moe_workspace_bytes(d0, abi.MOE_FWD_ONLY) > 0
 

@@ -27,6 +27,13 @@ SMALL = [
     MoEConfig(300, 192, 64, 32, 32, 64, "bf16", "bf16_k32_shared"),
     MoEConfig(200, 64, 64, 32, 32, 0, "f32", "f32_k32"),
     MoEConfig(333, 640, 128, 8, 2, 0, "bf16", "bf16_d640"),
+    # d = 512, h = 1024: the down, input-gradient and weight-gradient GEMMs
+    # run as CTA pairs over experts padded to 256 rows (the last 128-row
+    # tile of an expert may be empty); with a shared expert of 1024 over an
+    # odd number of 128-row token tiles (the last pair's odd CTA past the
+    # tokens)
+    MoEConfig(1500, 512, 1024, 4, 2, 0, "bf16", "bf16_pairs"),
+    MoEConfig(1100, 512, 1024, 4, 2, 1024, "bf16", "bf16_pairs_shared"),
     # capacity routing: about half the pairs dropped; with a shared expert;
     # float32; one pair per expert
     MoEConfig(2000, 128, 128, 8, 2, 0, "bf16", "bf16_capacity_half", capacity=250),
