@@ -39,6 +39,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
+                    help="graph: each timed step replays a CUDA graph of the whole step; "
+                         "stream: the library's launches are issued one by one")
     ap.add_argument("--skew", type=float, default=0.0,
                     help="router bias ramp: skew * 4 logit std from expert 0 down to expert E-1")
     ap.add_argument("--capacity-factor", type=float, default=0.0,
@@ -477,16 +480,25 @@ def main():
                "empty_experts": int((per_expert == 0).sum()), "capacity": cfg.capacity,
                "kept_pairs_frac": kept / P}
 
+    run_train, run_fwd = train, fwd
+    if args.launch == "graph":
+        # the same passes recorded once; each timed step replays all of it
+        run_train, run_fwd = layer.capture(train), layer.capture(fwd)
+        for _ in range(args.warmup):
+            run_train()
+            run_fwd()
+        torch.cuda.synchronize()
+
     clocks = ClockSampler(local)
     time.sleep(0.3)
     barrier()
     torch.cuda.synchronize()
     clocks.mark_start()
-    train_ms = timed(train, args.steps)
+    train_ms = timed(run_train, args.steps)
     torch.cuda.synchronize()
     barrier()
     clocks.mark_stop()
-    fwd_ms = timed(fwd, args.steps)
+    fwd_ms = timed(run_fwd, args.steps)
     clk = clocks.finish()
 
     ms = statistics.mean(train_ms)
@@ -503,14 +515,19 @@ def main():
     # (the layer's host-input step copies the upstream gradient on a side
     # stream behind the forward pass)
     loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    layer.train_step_from_host(host["x"], p, host["upstream"], loss_host)  # first-call setup
+
+    def e2e_step():
+        layer.train_step_from_host(host["x"], p, host["upstream"], loss_host)
+
+    e2e_step()  # first-call setup
+    run_e2e = layer.capture(e2e_step) if args.launch == "graph" else e2e_step
     torch.cuda.synchronize()
     e2e_times = []
     for _ in range(max(3, args.steps // 2)):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        layer.train_step_from_host(host["x"], p, host["upstream"], loss_host)
+        run_e2e()
         torch.cuda.synchronize()
         e2e_times.append(time.perf_counter() - t0)
     e2e_s = statistics.median(e2e_times)
@@ -602,6 +619,8 @@ def main():
                        "shared_hidden": cfg.shared_hidden, "step": "train (value_and_grad)",
                        "routing": routing,
                        "l2": "flushed between timed steps (256 MiB write)",
+                       "launch": ("a CUDA graph of the whole step, replayed per step"
+                                  if args.launch == "graph" else "stream launches"),
                        "parallelism": f"independent batch per GPU x{world}"},
             "fwd_tokens_per_s": fwd_value, "fwd_ms": fms,
             "pct_bf16_peak": {"train": f_train / (ms / 1e3) / 1e12 / bf16_peak,

@@ -161,6 +161,26 @@ class MoELayer:
             loss_host.copy_(self.loss, non_blocking=True)
         return self.loss, self.dx, self.grads
 
+    def capture(self, fn):
+        """Records ``fn()`` -- a composed pass (``train_step``, ``forward``,
+        ``train_step_from_host``) on fixed buffers -- into a CUDA graph and
+        returns its replay.  The library's calls only launch stream-ordered
+        work and allocate nothing, so they record as they are; ``fn`` runs
+        once on a side stream first so that one-time setup (kernel
+        attributes, the layer's input buffers) happens outside the capture.
+        A replay repeats the recorded pass on whatever the buffers hold."""
+        main = torch.cuda.current_stream(self.device)
+        warm = torch.cuda.Stream(self.device)
+        warm.wait_stream(main)
+        with torch.cuda.stream(warm):
+            fn()
+        main.wait_stream(warm)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        self._graphs = getattr(self, "_graphs", []) + [graph]  # kept alive with the layer
+        return graph.replay
+
     def device_status(self):
         """(status, detail) recorded by the kernels; synchronises the stream."""
         return abi.moe_read_device_status(self.ws_ptr, self.ws_bytes, self._stream())

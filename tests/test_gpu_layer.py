@@ -208,3 +208,36 @@ def test_train_step_from_host_matches_device_inputs():
         assert torch.equal(dx2, ref[1])
         for k, v in ref[2].items():
             assert torch.equal(g2[k], v), k
+
+
+def test_captured_train_step_replays_the_eager_results():
+    # a CUDA graph of the train step (and of the host-input step) gives the
+    # eager step's results bit for bit on every replay
+    cfg = MoEConfig(1500, 512, 1024, 4, 2, 1024, "bf16", "graph")
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, "bf16")
+    p = {k: dev[k] for k in params_of(inp)}
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                     cfg.shared_hidden, "bf16", train=True)
+    loss, dx, g = layer.train_step(dev["x"], p, dev["upstream"])
+    torch.cuda.synchronize()
+    ref = (loss.clone(), dx.clone(), {k: v.clone() for k, v in g.items() if v is not None})
+    replay = layer.capture(lambda: layer.train_step(dev["x"], p, dev["upstream"]))
+    xh = dev["x"].cpu().pin_memory()
+    gh = dev["upstream"].cpu().pin_memory()
+    lh = torch.empty(1, dtype=torch.float32).pin_memory()
+    replay_host = layer.capture(lambda: layer.train_step_from_host(xh, p, gh, lh))
+    for run in (replay, replay, replay_host):
+        layer.loss.zero_()
+        layer.dx.zero_()
+        for v in layer.grads.values():
+            if v is not None:
+                v.zero_()
+        run()
+        torch.cuda.synchronize()
+        assert torch.equal(layer.loss, ref[0])
+        assert torch.equal(layer.dx, ref[1])
+        for k, v in ref[2].items():
+            assert torch.equal(layer.grads[k], v), k
+    assert float(lh[0]) == float(ref[0][0])
