@@ -276,8 +276,9 @@ struct Shared {
 
 // CLUSTER: a barrier of a CTA pair (arrivals from the other CTA, or from
 // the pair's MMA completions): polled without suspending, cluster-scope
-// acquire.
-template <bool CLUSTER = false>
+// acquire; NAP: the many epilogue warps sleep 64 ns between polls, leaving
+// the issue slots to the warps at work.
+template <bool CLUSTER = false, bool NAP = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Shared* sh,
                                               int* status, int where) {
   auto try_wait = [&] {
@@ -286,6 +287,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sh
   if (try_wait()) return true;
   const uint64_t t0 = tc::globaltimer();
   while (true) {
+    if (CLUSTER && NAP) __nanosleep(64);
     if (try_wait()) return true;
     if (sh->abort) return false;
     if (tc::globaltimer() - t0 > 2000000000ull) {
@@ -685,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           gt = 0.f;
         }
       }
-      if (!wait_or_abort<C::PAIR>(&sh->tfull[acc], aphase, sh, p.status, 400)) {
+      if (!wait_or_abort<C::PAIR, true>(&sh->tfull[acc], aphase, sh, p.status, 400)) {
         aborted = true;
         break;
       }
