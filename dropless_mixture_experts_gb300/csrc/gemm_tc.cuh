@@ -110,7 +110,9 @@ struct Cfg {
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per-warp staging: 2 KB per bf16 32x32 tile
-  static constexpr int EPI_BYTES = EK == E_GU ? 3 * 2048
+  // (gate/up through the load/store units: two tiles, a_u reuses H's slot,
+  // which leaves room for a fourth operand stage)
+  static constexpr int EPI_BYTES = EK == E_GU ? (kGuStoreLsu ? 2 : 3) * 2048
                                    : EK == E_DZ ? 4 * 2048
                                    : (EK == E_DOWN || EK == E_DX) ? 2048 : 0;
   // routed DW kinds keep their chunk schedule (E + 1 ints) after the barriers
@@ -718,16 +720,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (kGuStoreLsu) {
             __syncwarp();  // the previous chunk's copies have read the staging
             stage_write_row(stg, lane, hv);
-            if (p.save) {
-              stage_write_row(stg + 2048, lane, gv);
-              stage_write_row(stg + 4096, lane, uv);
-            }
+            if (p.save) stage_write_row(stg + 2048, lane, gv);
             __syncwarp();
             const int x = tl.n0 + 32 * c;
             staged_copy_out(stg, p.dst0, yrow, x, p.ld_out, p.rows_out, lane);
             if (p.save) {
               staged_copy_out(stg + 2048, p.dst1, yrow, x, p.ld_out, p.rows_out, lane);
-              staged_copy_out(stg + 4096, p.dst2, yrow, x, p.ld_out, p.rows_out, lane);
+              __syncwarp();  // H's copies have read the first slot
+              stage_write_row(stg, lane, uv);
+              __syncwarp();
+              staged_copy_out(stg, p.dst2, yrow, x, p.ld_out, p.rows_out, lane);
             }
           } else {
             if (lane == 0) tc::bulk_wait_read0();  // staging free again
