@@ -261,9 +261,41 @@ def oracle_tokens_per_s(cfg, inputs, target_s=10.0, max_tokens=None):
         S = min(cap, int(S * max(2.0, target_s / max(dt, 1e-3) * 0.8)))
 
 
+# ---------------------------------------------------------------------------
+# ranks (torchrun): independent batches, the job's time is its slowest rank's
+# ---------------------------------------------------------------------------
+def rank_info():
+    """(world size, rank, local rank) from the launcher's environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed_offset(rank):
+    """Each rank draws its own batch (and weights) from the seeded generator."""
+    return 100 * rank
+
+
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the process group (times: the
+    job waits for its slowest rank); the values themselves without one."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_tokens_per_s(world, tokens, seconds):
+    """Whole-job throughput: every rank processes its own batch of `tokens`,
+    the job takes the slowest rank's `seconds` (weak scaling)."""
+    return world * tokens / seconds
+
+
 def reference_arm(args, cfg):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    _, rank, _ = rank_info()
+    if rank != 0:  # rank 0 alone times the oracle; the others leave without work
         return
     from dropless_mixture_experts_gb300.synthetic import make_inputs, params_of
     import oracle
@@ -424,9 +456,7 @@ def main():
     from dropless_mixture_experts_gb300.layer import MoELayer
     from dropless_mixture_experts_gb300.synthetic import make_inputs, params_of
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_info()
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl")
@@ -437,7 +467,7 @@ def main():
 
     abi.load()
     td = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
-    inputs = make_inputs(cfg, seed_offset=100 * rank)
+    inputs = make_inputs(cfg, seed_offset=rank_seed_offset(rank))
     host = {k: (None if v is None else
                 torch.from_numpy(v).to(torch.float32 if k == "router_bias" else td).pin_memory())
             for k, v in inputs.items()}
@@ -503,12 +533,9 @@ def main():
 
     ms = statistics.mean(train_ms)
     fms = statistics.mean(fwd_ms)
-    if world > 1:
-        t = torch.tensor([ms, fms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, fms = float(t[0]), float(t[1])
-    value = world * cfg.tokens / (ms / 1e3)
-    fwd_value = world * cfg.tokens / (fms / 1e3)
+    ms, fms = max_over_ranks([ms, fms], "cuda")
+    value = job_tokens_per_s(world, cfg.tokens, ms / 1e3)
+    fwd_value = job_tokens_per_s(world, cfg.tokens, fms / 1e3)
 
     # end to end through the public API with host buffers: H2D of the batch
     # (x and the upstream gradient) and D2H of the loss inside the timed region
@@ -532,7 +559,9 @@ def main():
         e2e_times.append(time.perf_counter() - t0)
     e2e_s = statistics.median(e2e_times)
     h2d = host["x"].numel() * host["x"].element_size() * 2
-    e2e = {"value": world * cfg.tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+    (e2e_s,) = max_over_ranks([e2e_s], "cuda")
+    e2e = {"value": job_tokens_per_s(world, cfg.tokens, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": 4}
 
     # per-kernel device time and launch count of the forward and of the step
