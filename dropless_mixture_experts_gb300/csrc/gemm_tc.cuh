@@ -11,10 +11,12 @@
 //   warps 2-9  epilogue, two warps per 32-lane quarter of the accumulator
 //              splitting its columns: tcgen05.ld, then the fused SwiGLU,
 //              gate-weighted combine, SwiGLU backward or gradient stores.
-//              bf16 tiles the epilogue reads or writes (the SwiGLU outputs,
-//              the saved pre-activations, the backward's dA) go
-//              through a per-warp 32x32 staging tile in shared memory and
-//              move with TMA loads and stores.
+//              bf16 tiles the epilogue reads or writes go through a
+//              per-warp 32x32 staging tile in shared memory: the saved
+//              pre-activations and dA, down and dX rows move with TMA loads
+//              and stores; the SwiGLU outputs leave through the load/store
+//              units (coalesced 16-byte copies), which keeps the TMA engine
+//              for the operand loads.
 //
 // Tiles are 128 rows x BN columns with K blocks of 64 (one 128-byte swizzle
 // row of bf16); shared memory holds a ring of STAGES operand stages and the
@@ -39,16 +41,12 @@ enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4, E_ROUTER = 5 };
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kSmemLimit = 232448;  // dynamic shared memory per block (227 KB)
-// Gate/up epilogue: the staged 32x32 tiles leave through the load/store
-// units (coalesced 16-byte copies, four lanes per row) instead of TMA stores,
-// which keeps the TMA engine for the operand loads.
-constexpr bool kGuStoreLsu = true;
 
 // Tensor maps of one launch: the two operands (B may come from two maps,
 // split along N or K) and the epilogue's bf16 outputs / inputs.
 struct Maps {
   CUtensorMap a, b0, b1;
-  CUtensorMap o0, o1, o2;  // GU: H, a_g, a_u;  DZ: dA, gate*H
+  CUtensorMap o0, o1, o2;  // DOWN / DX: output rows; DZ: dA
   CUtensorMap i0, i1;      // DZ: saved a_g, a_u
 };
 
@@ -110,9 +108,9 @@ struct Cfg {
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // per-warp staging: 2 KB per bf16 32x32 tile
-  // (gate/up through the load/store units: two tiles, a_u reuses H's slot,
-  // which leaves room for a fourth operand stage)
-  static constexpr int EPI_BYTES = EK == E_GU ? (kGuStoreLsu ? 2 : 3) * 2048
+  // (gate/up: two tiles, a_u reuses H's slot, which leaves room for a
+  // fourth operand stage)
+  static constexpr int EPI_BYTES = EK == E_GU ? 2 * 2048
                                    : EK == E_DZ ? 4 * 2048
                                    : (EK == E_DOWN || EK == E_DX) ? 2048 : 0;
   // routed DW kinds keep their chunk schedule (E + 1 ints) after the barriers
@@ -703,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if constexpr (C::EK == E_GU) {
         // H = silu(a_g) * a_u with a_g, a_u rounded to bf16 first (the values
-        // a backward pass reads back); 32x32 tiles stored by TMA
+        // a backward pass reads back); staged 32x32 tiles copied out by the
+        // load/store units
 #pragma unroll 1
         for (int c = half; c < C::BN / 64; c += 2) {
           uint32_t g[32], u[32];
@@ -717,39 +716,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uv[i] = bf16r(__uint_as_float(u[i]));
             hv[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
           }
-          if constexpr (kGuStoreLsu) {
-            __syncwarp();  // the previous chunk's copies have read the staging
-            stage_write_row(stg, lane, hv);
-            if (p.save) stage_write_row(stg + 2048, lane, gv);
+          __syncwarp();  // the previous chunk's copies have read the staging
+          stage_write_row(stg, lane, hv);
+          if (p.save) stage_write_row(stg + 2048, lane, gv);
+          __syncwarp();
+          const int x = tl.n0 + 32 * c;
+          staged_copy_out(stg, p.dst0, yrow, x, p.ld_out, p.rows_out, lane);
+          if (p.save) {
+            staged_copy_out(stg + 2048, p.dst1, yrow, x, p.ld_out, p.rows_out, lane);
+            __syncwarp();  // H's copies have read the first slot
+            stage_write_row(stg, lane, uv);
             __syncwarp();
-            const int x = tl.n0 + 32 * c;
-            staged_copy_out(stg, p.dst0, yrow, x, p.ld_out, p.rows_out, lane);
-            if (p.save) {
-              staged_copy_out(stg + 2048, p.dst1, yrow, x, p.ld_out, p.rows_out, lane);
-              __syncwarp();  // H's copies have read the first slot
-              stage_write_row(stg, lane, uv);
-              __syncwarp();
-              staged_copy_out(stg, p.dst2, yrow, x, p.ld_out, p.rows_out, lane);
-            }
-          } else {
-            if (lane == 0) tc::bulk_wait_read0();  // staging free again
-            __syncwarp();
-            stage_write_row(stg, lane, hv);
-            if (p.save) {
-              stage_write_row(stg + 2048, lane, gv);
-              stage_write_row(stg + 4096, lane, uv);
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              const int x = tl.n0 + 32 * c;
-              tc::tma_store_2d(&m.o0, stg, x, yrow);
-              if (p.save) {
-                tc::tma_store_2d(&m.o1, stg + 2048, x, yrow);
-                tc::tma_store_2d(&m.o2, stg + 4096, x, yrow);
-              }
-              tc::bulk_commit();
-            }
+            staged_copy_out(stg, p.dst2, yrow, x, p.ld_out, p.rows_out, lane);
           }
         }
       } else if constexpr (C::EK == E_DOWN || C::EK == E_DX) {

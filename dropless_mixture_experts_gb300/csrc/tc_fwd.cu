@@ -29,14 +29,10 @@ bool gateup(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, vo
   void* H = routed ? p.h_buf : p.hs_buf;
   void* AG = routed ? p.a_gate : p.as_gate;
   void* AU = routed ? p.a_up : p.as_up;
-  q.rows_out = rows;
+  q.rows_out = rows;  // the epilogue's load/store-unit copies go straight to these
   q.dst0 = H;
   q.dst1 = AG;
   q.dst2 = AU;
-  if (!make_map_sw64(&mp.o0, H, rows, h)) return false;
-  mp.o1 = mp.o2 = mp.o0;
-  if (save && (!make_map_sw64(&mp.o1, AG, rows, h) || !make_map_sw64(&mp.o2, AU, rows, h)))
-    return false;
   if (routed) {
     if (!make_map(&mp.a, at<void>(ws, L.xs), L.PPcap, dm, 64, 128)) return false;
     if (!make_map(&mp.b0, p.w_gate, (uint64_t)d.experts * dm, h, 64, 64)) return false;

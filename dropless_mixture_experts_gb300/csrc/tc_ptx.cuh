@@ -1,5 +1,5 @@
 // Inline-PTX building blocks of the sm_103a tensor-core GEMMs: mbarriers
-// with bounded waits, TMA tile and gather4 loads, tcgen05 MMA / TMEM access
+// with bounded waits, TMA tile loads and stores, tcgen05 MMA / TMEM access
 // and the shared-memory matrix descriptors.
 #pragma once
 
@@ -84,19 +84,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar_cluster)
-      : "memory");
-}
-
-// Four rows (y0..y3) of `box_x` elements starting at column x; the tensor map
-// has a one-row box.  The rows land one after another in shared memory.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                            int32_t x, int32_t y0, int32_t y1, int32_t y2,
-                                            int32_t y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
-      "r"(smem_u32(bar))
       : "memory");
 }
 
