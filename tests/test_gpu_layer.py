@@ -34,6 +34,10 @@ SMALL = [
     # tokens)
     MoEConfig(1500, 512, 1024, 4, 2, 0, "bf16", "bf16_pairs"),
     MoEConfig(1100, 512, 1024, 4, 2, 1024, "bf16", "bf16_pairs_shared"),
+    # the same pair paths with capacity routing (kept counts padded to 256)
+    # and with skewed routing (empty and hot experts)
+    MoEConfig(1500, 512, 1024, 4, 2, 0, "bf16", "bf16_pairs_capacity", capacity=500),
+    MoEConfig(1500, 512, 1024, 8, 2, 0, "bf16", "bf16_pairs_skew", skew=0.9),
     # capacity routing: about half the pairs dropped; with a shared expert;
     # float32; one pair per expert
     MoEConfig(2000, 128, 128, 8, 2, 0, "bf16", "bf16_capacity_half", capacity=250),
