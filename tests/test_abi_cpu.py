@@ -26,6 +26,28 @@ def declared_functions():
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+(moe_\w+)\s*\(", text, re.M)))
 
 
+def declared_parameter_counts():
+    """Name -> number of parameters of every prototype in the header
+    (comments stripped; `void` alone counts as none)."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    out = {}
+    for m in re.finditer(r"(moe_\w+)\s*\(([^;{]*?)\)\s*;", text, re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    # the Python binding passes exactly as many arguments as each prototype
+    # declares (an ABI change that misses the binding fails here, not on a GPU)
+    counts = declared_parameter_counts()
+    assert set(counts) == set(abi.EXPORTS)
+    for name, (argtypes, _) in abi._SIGS.items():
+        assert len(argtypes) == counts[name], (name, len(argtypes), counts[name])
+
+
 def test_header_declarations_are_exported(lib):
     names = declared_functions()
     assert len(names) >= 9
