@@ -63,6 +63,24 @@ def test_train_step_matches_oracle(cfg):
     assert not bad, (errs, cfg)
 
 
+# The numerics grid the kernel_gmm_gpu page planned for its check mode
+# (1000 tokens, d128, h256; E 8 / 64; top-1 / top-4; skew 0 / 0.9; fp32 /
+# bf16; its results are absent from the page): every combination, train step
+# against the oracle.
+SWEEP = [MoEConfig(1000, 128, 256, E, k, 0, dt, f"sweep_E{E}_k{k}_s{sk}_{dt}", skew=sk)
+         for E in (8, 64) for k in (1, 4) for sk in (0.0, 0.9) for dt in ("f32", "bf16")]
+
+
+@pytest.mark.parametrize("cfg", SWEEP, ids=[c.name for c in SWEEP])
+def test_planned_numerics_sweep(cfg):
+    inp, layer, dev, res = run_layer(cfg)
+    assert res["status"] == 0
+    check_routing_bit_exact(res, cfg)
+    errs = compare_layer(inp, res, cfg, train=True)
+    bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
+    assert not bad, (errs, cfg)
+
+
 @pytest.mark.parametrize("cfg", SMALL[:3], ids=[c.name for c in SMALL[:3]])
 def test_forward_only_matches_train_forward(cfg):
     inp, _, _, r_train = run_layer(cfg, train=True)
