@@ -97,6 +97,28 @@ def step_flops(cfg, kept_frac=1.0):
     return fwd, 3 * fwd
 
 
+# The pages' train-step times (ms) for the bf16 workloads: the RTX 3090 layer
+# runs of kernel_gmm_gpu.json (pallas, dispatch sorted) and the H100 NVL
+# decoder rows of gpu_moe_h100.json (pallas, sorted).  Another machine's
+# numbers: context for the ratio, not a target.
+PAGE_TRAIN_MS = {
+    "e8k2_bf16_32k": (16.02, "RTX 3090, pallas sorted bf16, 32768 tokens (kernel_gmm_gpu.json)"),
+    "e8k2_bf16_128k": (65.46, "RTX 3090, pallas sorted bf16, 131072 tokens (kernel_gmm_gpu.json)"),
+    "e64k4_bf16_32k": (13.37, "RTX 3090, pallas sorted bf16, E64 k4 h256 (kernel_gmm_gpu.json)"),
+    "decoder_bf16_16k": (2.628, "H100 NVL, pallas sorted, decoder 16384 tokens (gpu_moe_h100.json)"),
+    "decoder_bf16_128k": (19.126, "H100 NVL, pallas sorted, decoder 131072 tokens (gpu_moe_h100.json)"),
+}
+
+
+def vs_page(cfg, value):
+    """value / the pages' train-step tokens/s for the same workload (None
+    without one; skewed or capacity routing has none)."""
+    ent = PAGE_TRAIN_MS.get(cfg.name)
+    if ent is None or cfg.skew or cfg.capacity:
+        return None, None
+    return value / (cfg.tokens / (ent[0] / 1e3)), ent[1]
+
+
 def kernel_work(cfg, kept=None):
     """Algorithmic work per step of each kernel name: {"flop": f, "byte": b}.
     f = 2*M*N*K over real rows (routed launches count the kept pairs; the
@@ -637,10 +659,12 @@ def main():
                "sample": f"float64 train step on the first {S} of {cfg.tokens} tokens ({dt:.1f} s)"}
 
     if rank == 0:
+        vs, vs_basis = vs_page(cfg, value)
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": vs,
+            "vs_baseline_basis": vs_basis,
             "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
             "data": "synthetic",
             "config": {"workload": cfg.name, "tokens": cfg.tokens, "d_model": cfg.d_model,

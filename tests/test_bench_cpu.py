@@ -37,3 +37,14 @@ def test_binding_roofline():
     wd = bench.kernel_work(CONFIGS["decoder_bf16_128k"])
     for k in ("gateup", "down", "dz", "dx", "dw_down", "dw_gateup"):
         assert bench.kernel_bound("tc_" + k, wd[k], PEAKS)[0] == "hbm", k
+
+
+def test_vs_baseline_uses_the_pages_train_time_for_the_same_workload():
+    cfg = CONFIGS["e8k2_bf16_32k"]
+    v, basis = bench.vs_page(cfg, 32768 / 16.02e-3)  # the page's own tokens/s
+    assert abs(v - 1.0) < 1e-12 and "RTX 3090" in basis
+    # no page number: float32 workloads, skewed or capacity routing
+    assert bench.vs_page(CONFIGS["e8k2_f32_4k"], 1.0) == (None, None)
+    import dataclasses
+    assert bench.vs_page(dataclasses.replace(cfg, skew=0.9), 1.0) == (None, None)
+    assert bench.vs_page(dataclasses.replace(cfg, capacity=100), 1.0) == (None, None)
