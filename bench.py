@@ -181,12 +181,39 @@ def kernel_bound(name, wk, peaks):
     return (cb if t_c >= t_m else "hbm"), comp, hbm
 
 
-def src_hash():
+def code_text(text):
+    """CUDA/C++ source with comments and blank space removed (what a
+    compiler sees); string literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # a string literal, escapes included
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def src_hash(csrc=None):
+    """Hash of the CUDA sources' code (comments and blank space ignored): the
+    key under which per-launch DRAM traffic counters stay valid."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "dropless_mixture_experts_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "dropless_mixture_experts_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(f.encode())
+            h.update(code_text(open(os.path.join(csrc, f), encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

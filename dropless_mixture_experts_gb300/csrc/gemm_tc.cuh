@@ -21,7 +21,10 @@
 // Tiles are 128 rows x BN columns with K blocks of 64 (one 128-byte swizzle
 // row of bf16); shared memory holds a ring of STAGES operand stages and the
 // accumulator is double-buffered in tensor memory so the epilogue of one
-// tile overlaps the main loop of the next.  Every wait is bounded: a wait
+// tile overlaps the main loop of the next.  Where the tensor cores bound a
+// contraction, a two-CTA cluster shares one 256-row tile (tcgen05
+// cta_group::2, Cfg::PAIR): each CTA holds its 128 rows of A and half of B's
+// columns, the even CTA issues the MMAs.  Every wait is bounded: a wait
 // that runs out records MOE_ERR_TIMEOUT, makes the other roles leave, lets
 // in-flight copies land and frees the tensor memory before returning.
 #pragma once

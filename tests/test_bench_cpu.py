@@ -48,3 +48,11 @@ def test_vs_baseline_uses_the_pages_train_time_for_the_same_workload():
     import dataclasses
     assert bench.vs_page(dataclasses.replace(cfg, skew=0.9), 1.0) == (None, None)
     assert bench.vs_page(dataclasses.replace(cfg, capacity=100), 1.0) == (None, None)
+
+
+def test_traffic_key_ignores_comments_only():
+    a = 'int f() { return 1; } // note\n/* block */ const char* s = "x // y";'
+    b = 'int f() {\n  return 1;  // another note\n}\nconst char* s = "x // y";'
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(a.replace("return 1", "return 2"))
+    assert bench.code_text('"a /* b */"') == '"a /* b */"'  # inside a string: code
