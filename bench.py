@@ -27,7 +27,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s fwd and train step (bf16), % of dense BF16 tensor peak"
-DEFAULT_CONFIG = "e8k2_bf16_32k"
+DEFAULT_CONFIG = "decoder_bf16_128k"
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -46,6 +46,10 @@ def parse():
                     help="router bias ramp: skew * 4 logit std from expert 0 down to expert E-1")
     ap.add_argument("--capacity-factor", type=float, default=0.0,
                     help="capacity routing: each expert keeps ceil(F * T * k / E) pairs (0: dropless)")
+    ap.add_argument("--also", default=None,
+                    help="comma-separated further workloads measured in the same run and "
+                         "reported under 'also' (default: e8k2_bf16_128k beside the default "
+                         "workload, none otherwise)")
     ap.add_argument("--sweep", default="", choices=["", "maxtok"],
                     help="maxtok: the largest train-step token count that fits in free HBM")
     return ap.parse_args()
@@ -485,36 +489,24 @@ def maxtok_sweep(args, cfg):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def main():
-    args = parse()
-    from dropless_mixture_experts_gb300.synthetic import CONFIGS
+NOMINAL_BF16_TFLOPS = 2250.0  # GB300 dense bf16 tensor peak (NVIDIA's published, no sparsity)
 
-    cfg = with_routing(CONFIGS[args.config], args)
-    if args.impl == "reference":
-        reference_arm(args, cfg)
-        return
-    if args.sweep == "maxtok":
-        maxtok_sweep(args, cfg)
-        return
 
-    import numpy as np
+def also_default(name):
+    """The second 131072-token bf16 workload reported beside the default one."""
+    return "e8k2_bf16_128k" if name == DEFAULT_CONFIG else ""
+
+
+def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
+    """Times one workload: the train step and the forward (graph replays by
+    default), the end-to-end host-input step, and the per-kernel split.
+    Returns the bench line's fields for it (rank 0 prints them)."""
     import torch
-    import torch.distributed as dist
 
     from dropless_mixture_experts_gb300 import abi
     from dropless_mixture_experts_gb300.layer import MoELayer
     from dropless_mixture_experts_gb300.synthetic import make_inputs, params_of
 
-    world, rank, local = rank_info()
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    abi.load()
     td = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     inputs = make_inputs(cfg, seed_offset=rank_seed_offset(rank))
     host = {k: (None if v is None else
@@ -587,13 +579,15 @@ def main():
     fwd_value = job_tokens_per_s(world, cfg.tokens, fms / 1e3)
 
     # end to end through the public API with host buffers: H2D of the batch
-    # (x and the upstream gradient) and D2H of the loss inside the timed region
-    # (the layer's host-input step copies the upstream gradient on a side
-    # stream behind the forward pass)
+    # (x and the upstream gradient), D2H of the loss and of the input
+    # gradient dx inside the timed region (the layer's host-input step copies
+    # the upstream gradient on a side stream behind the forward pass); the
+    # weight gradients stay on the device for an optimizer step
     loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    dx_host = torch.empty(cfg.tokens, cfg.d_model, dtype=td).pin_memory()
 
     def e2e_step():
-        layer.train_step_from_host(host["x"], p, host["upstream"], loss_host)
+        layer.train_step_from_host(host["x"], p, host["upstream"], loss_host, dx_host)
 
     e2e_step()  # first-call setup
     run_e2e = layer.capture(e2e_step) if args.launch == "graph" else e2e_step
@@ -608,12 +602,15 @@ def main():
         e2e_times.append(time.perf_counter() - t0)
     e2e_s = statistics.median(e2e_times)
     h2d = host["x"].numel() * host["x"].element_size() * 2
+    d2h = loss_host.numel() * loss_host.element_size() + dx_host.numel() * dx_host.element_size()
     (e2e_s,) = max_over_ranks([e2e_s], "cuda")
     e2e = {"value": job_tokens_per_s(world, cfg.tokens, e2e_s), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": 4}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "copies": "H2D x and the upstream gradient; D2H the loss and dx"}
 
     # per-kernel device time and launch count of the forward and of the step
+    # (stream launches with an event pair around each launch: a little
+    # slower than the graph-replayed step, so each fraction is a lower bound)
     prof_steps = 3
     abi.moe_profile_enable(True)
     for _ in range(prof_steps):
@@ -630,11 +627,7 @@ def main():
     pieces = pieces_of(fwd_rec, rec, prof_steps)
     launches_per_step = sum(n for n, _ in rec.values()) / prof_steps
     work = kernel_work(cfg, kept)
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except Exception:
-        pass
+
     # the dominant kernel with a known algorithmic amount of work, under
     # whichever of its compute and HBM rooflines is the binding one
     def work_of(name):
@@ -678,36 +671,97 @@ def main():
         kernels[k_] = ent
 
     f_fwd, f_train = step_flops(cfg, kept / P)
-    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    measured_bf16 = float(peaks.get("bf16_tflops", 1900.0))
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
+    if cpu_baseline and rank == 0 and world == 1:
         v, S, dt = oracle_tokens_per_s(cfg, inputs)
         cpu = {"value": v, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"float64 train step on the first {S} of {cfg.tokens} tokens ({dt:.1f} s)"}
+    out = {
+        "value": value, "ms_per_step": ms, "fwd_tokens_per_s": fwd_value, "fwd_ms": fms,
+        "config": {"workload": cfg.name, "tokens": cfg.tokens, "d_model": cfg.d_model,
+                   "d_hidden": cfg.d_hidden, "experts": cfg.experts, "top_k": cfg.top_k,
+                   "shared_hidden": cfg.shared_hidden, "step": "train (value_and_grad)",
+                   "routing": routing,
+                   "l2": "flushed between timed steps (256 MiB write)",
+                   "launch": ("a CUDA graph of the whole step, replayed per step"
+                              if args.launch == "graph" else "stream launches"),
+                   "kernel_timing": ("pieces_ms, kernels and roofline: a separate pass of "
+                                     "stream launches with an event pair around each launch"),
+                   "parallelism": f"independent batch per GPU x{world}"},
+        # the dense bf16 tensor peak of the part, and the measured cuBLAS
+        # matmul rate (the roofline denominator) beside it
+        "pct_bf16_peak": {"train": f_train / (ms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
+                          "fwd": f_fwd / (fms / 1e3) / 1e12 / NOMINAL_BF16_TFLOPS,
+                          "peak_tflops": NOMINAL_BF16_TFLOPS,
+                          "peak_source": "GB300 dense bf16 tensor peak, published (2.25 PFLOP/s)"},
+        "pct_of_measured_matmul": {"train": f_train / (ms / 1e3) / 1e12 / measured_bf16,
+                                   "fwd": f_fwd / (fms / 1e3) / 1e12 / measured_bf16,
+                                   "peak_tflops": measured_bf16,
+                                   "peak_source": "measured bf16 matmul burst"},
+        "clocks": clk, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
+        "roofline": roofline, "cpu_baseline": cpu, "pieces_ms": pieces, "kernels": kernels,
+    }
+    del layer, dev, host, flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    args = parse()
+    from dropless_mixture_experts_gb300.synthetic import CONFIGS
+
+    cfg = with_routing(CONFIGS[args.config], args)
+    if args.impl == "reference":
+        reference_arm(args, cfg)
+        return
+    if args.sweep == "maxtok":
+        maxtok_sweep(args, cfg)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    from dropless_mixture_experts_gb300 import abi
+
+    world, rank, local = rank_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    abi.load()
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        pass
+    main_res = measure(cfg, args, world, rank, local, barrier, peaks, not args.no_cpu_baseline)
+    also = {}
+    also_name = args.also if args.also is not None else also_default(args.config)
+    for name in [n for n in also_name.split(",") if n]:
+        r = measure(with_routing(CONFIGS[name], args), args, world, rank, local, barrier, peaks,
+                    False)
+        also[name] = {k: r[k] for k in ("value", "ms_per_step", "fwd_tokens_per_s", "fwd_ms",
+                                        "pct_bf16_peak", "pct_of_measured_matmul", "roofline",
+                                        "e2e", "clocks", "pieces_ms", "kernels")}
 
     if rank == 0:
-        vs, vs_basis = vs_page(cfg, value)
+        vs, vs_basis = vs_page(cfg, main_res["value"])
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "metric": METRIC, "value": main_res["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": main_res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": vs,
             "vs_baseline_basis": vs_basis,
             "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
             "data": "synthetic",
-            "config": {"workload": cfg.name, "tokens": cfg.tokens, "d_model": cfg.d_model,
-                       "d_hidden": cfg.d_hidden, "experts": cfg.experts, "top_k": cfg.top_k,
-                       "shared_hidden": cfg.shared_hidden, "step": "train (value_and_grad)",
-                       "routing": routing,
-                       "l2": "flushed between timed steps (256 MiB write)",
-                       "launch": ("a CUDA graph of the whole step, replayed per step"
-                                  if args.launch == "graph" else "stream launches"),
-                       "parallelism": f"independent batch per GPU x{world}"},
-            "fwd_tokens_per_s": fwd_value, "fwd_ms": fms,
-            "pct_bf16_peak": {"train": f_train / (ms / 1e3) / 1e12 / bf16_peak,
-                              "fwd": f_fwd / (fms / 1e3) / 1e12 / bf16_peak},
-            "clocks": clk, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
-            "roofline": roofline, "cpu_baseline": cpu, "pieces_ms": pieces, "kernels": kernels,
         }
+        line.update({k: v for k, v in main_res.items() if k not in line})
+        if also:
+            line["also"] = also
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -9,6 +9,12 @@
 // zero: every entry a call reads was written earlier in that same call).
 // Calls that overlap on the GPU (different streams, or different host
 // threads without ordering) race on it.
+//
+// An expert index outside [0, E) gets what moe_permute gives it: no sorted
+// position (inv_perm = -1), and perm reads -1 past offsets[E].  Unlike
+// moe_permute, which records MOE_ERR_DEVICE_CHECK in its workspace, this
+// entry has no status word a caller could read: the -1 entries are the
+// only sign.
 #include <mutex>
 
 #include "kernels.cuh"
@@ -19,7 +25,8 @@ namespace {
 constexpr int kNaRounds = 16;              // 32-pair rounds per warp chunk
 constexpr int kNaChunk = 32 * kNaRounds;   // pairs per warp chunk
 constexpr int64_t kNaHist = int64_t(1) << 19;  // max (warp chunks) x (experts)
-constexpr int kNaOff = 64;                 // ints [64, 64 + 257): expert offsets
+constexpr int kNaOff = 64;                 // ints [64, 64 + 257): expert offsets, then
+                                           // the number of sorted pairs
 constexpr int kNaHistAt = 64 + 320;        // ints: histograms, then their prefix sums
 constexpr int64_t kNaInts = kNaHistAt + 2 * kNaHist;
 
@@ -31,8 +38,7 @@ static __device__ __align__(256) int g_noalloc_scratch[kNaInts];
 template <bool SCATTER>
 __device__ __forceinline__ void na_walk(const int32_t* __restrict__ idx, int64_t P, int E,
                                         int64_t chunk, int* hist, const int* base_e,
-                                        const int* off_e, int32_t* perm, int32_t* inv_perm,
-                                        int* status) {
+                                        const int* off_e, int32_t* perm, int32_t* inv_perm) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   for (int r = 0; r < kNaRounds; ++r) {
@@ -41,8 +47,8 @@ __device__ __forceinline__ void na_walk(const int32_t* __restrict__ idx, int64_t
     if (p < P) {
       e = idx[p];
       if (e < 0 || e >= E) {
-        status[0] = MOE_ERR_DEVICE_CHECK;
-        e = -1;
+        e = -1;  // rejected: no sorted position
+        if (SCATTER) inv_perm[p] = -1;
       }
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(256) na_hist_kernel(const int32_t* __restrict_
   for (int e = lane; e < E; e += 32) hist[w][e] = 0;
   __syncwarp();
   if (chunk >= NW) return;
-  na_walk<false>(idx, P, E, chunk, hist[w], nullptr, nullptr, nullptr, nullptr, scratch);
+  na_walk<false>(idx, P, E, chunk, hist[w], nullptr, nullptr, nullptr, nullptr);
   int* out = scratch + kNaHistAt;
   for (int e = lane; e < E; e += 32) out[chunk * E + e] = hist[w][e];
 }
@@ -111,6 +117,7 @@ __global__ void na_offsets_kernel(const int32_t* __restrict__ counts, int E, int
     o += counts[e];
   }
   offsets[E] = o;
+  scratch[kNaOff + E] = o;
 }
 
 __global__ void __launch_bounds__(256) na_scatter_kernel(const int32_t* __restrict__ idx,
@@ -123,13 +130,16 @@ __global__ void __launch_bounds__(256) na_scatter_kernel(const int32_t* __restri
   for (int e = threadIdx.x; e < E; e += blockDim.x) s_off[e] = scratch[kNaOff + e];
   for (int e = lane; e < E; e += 32) hist[w][e] = 0;
   __syncthreads();
+  // sorted positions past the sorted pairs (pairs with a rejected index)
+  const int64_t sorted = scratch[kNaOff + E];
+  for (int64_t r = sorted + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < P;
+       r += (int64_t)gridDim.x * blockDim.x)
+    perm[r] = -1;
   const int64_t chunk = (int64_t)blockIdx.x * 8 + w;
   if (chunk >= NW) return;
   const int* base = scratch + kNaHistAt + kNaHist + chunk * E;
-  na_walk<true>(idx, P, E, chunk, hist[w], base, s_off, perm, inv_perm, scratch);
+  na_walk<true>(idx, P, E, chunk, hist[w], base, s_off, perm, inv_perm);
 }
-
-__global__ void na_clear_status_kernel(int* scratch) { scratch[0] = 0; }
 
 std::mutex g_na_mu;
 constexpr int kNaMaxDevices = 64;
@@ -173,7 +183,6 @@ extern "C" moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* t
   int* scratch = nullptr;
   const moe_status st = na_scratch(&scratch);
   if (st != MOE_OK) return st;
-  na_clear_status_kernel<<<1, 1, 0, stream>>>(scratch);
   const unsigned blocks = (unsigned)((NW + 7) / 8);
   if (NW > 0) na_hist_kernel<<<blocks, 256, 0, stream>>>(topk_idx, P, E, NW, scratch);
   na_scan_kernel<<<E, 1024, 0, stream>>>(NW, E, scratch, counts);

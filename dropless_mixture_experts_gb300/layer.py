@@ -130,13 +130,15 @@ class MoELayer:
         self.backward(x, p, dy)
         return self.loss, self.dx, self.grads
 
-    def train_step_from_host(self, x_host, p, dy_host, loss_host=None):
+    def train_step_from_host(self, x_host, p, dy_host, loss_host=None, dx_host=None):
         """The train step on a batch in pinned host memory: x is copied to the
         device on the current stream, the upstream gradient on a side stream
         while the forward pass runs (only the combine needs it), and the value
-        is copied back into ``loss_host`` (pinned, optional).  Returns the
-        same device buffers as ``train_step``; the copies land in the layer's
-        own input buffers."""
+        and the input gradient are copied back into ``loss_host`` [1] and
+        ``dx_host`` [T, d] (pinned, each optional).  Returns the same device
+        buffers as ``train_step``; the copies land in the layer's own input
+        buffers.  The weight gradients stay on the device, where an optimizer
+        step would read them."""
         if self.mode != abi.MOE_SAVE_FOR_BWD:
             raise RuntimeError("layer was built with train=False")
         if getattr(self, "x_dev", None) is None:
@@ -159,6 +161,8 @@ class MoELayer:
         self.backward(x, p, self.dy_dev)
         if loss_host is not None:
             loss_host.copy_(self.loss, non_blocking=True)
+        if dx_host is not None:
+            dx_host.copy_(self.dx, non_blocking=True)
         return self.loss, self.dx, self.grads
 
     def capture(self, fn):

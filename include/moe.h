@@ -206,7 +206,8 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream, int32_t* detail);
 
 /* moe_permute_noalloc: the same counting sort as moe_permute (counts,
- * offsets, perm, inv_perm; identical results) for callers that cannot
+ * offsets, perm, inv_perm; identical results, also for rejected expert
+ * indices) for callers that cannot
  * allocate device memory -- code running where cudaMalloc is unavailable or
  * not allowed, such as an engine plugin handed no workspace, a serving loop
  * whose memory was reserved up front by another allocator, or a caller that
@@ -226,8 +227,10 @@ moe_status moe_read_device_status(void* workspace, size_t workspace_bytes,
  * calls that overlap on the GPU (other streams, unsynchronised threads)
  * race.  The first call on a device looks up the array's device address,
  * which loads the library's device code there; make that first call before
- * any stream capture.  Expert indices outside [0, E) are skipped (their
- * outputs stay unwritten). */
+ * any stream capture.  An expert index outside [0, E) is treated as
+ * moe_permute treats it: its pair gets no sorted position (inv_perm = -1)
+ * and perm reads -1 past offsets[E]; this entry has no status word, so
+ * those -1 entries are the only report. */
 moe_status moe_permute_noalloc(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
                                int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                                cudaStream_t stream);

@@ -16,6 +16,21 @@ from dropless_mixture_experts_gb300.synthetic import make_inputs, params_of
 TOL = {"f32": 1e-4, "bf16": 2e-2}
 
 
+def elem_err(a, ref):
+    """The elementwise companion of rel_err: max over elements of
+    |a - ref| / (|ref| + 1e-3 max|ref|) (reported beside the normwise metric,
+    not held to the tolerance: near-zero elements of a bf16 result carry the
+    rounding of the large terms that cancelled in them)."""
+    a = np.asarray(a, np.float64)
+    ref = np.asarray(ref, np.float64)
+    if not ref.size:
+        return 0.0
+    floor = 1e-3 * float(np.max(np.abs(ref)))
+    if floor == 0.0:
+        return float(np.max(np.abs(a)))
+    return float(np.max(np.abs(a - ref) / (np.abs(ref) + floor)))
+
+
 def rel_err(a, ref):
     a = np.asarray(a, np.float64)
     ref = np.asarray(ref, np.float64)
@@ -93,18 +108,53 @@ def oracle_on_device_routing(inp, res, cfg, train=True):
 
 
 GRADS = ("dw_router", "dw_gate", "dw_up", "dw_down", "dws_gate", "dws_up", "dws_down")
+ROUTED = ("dw_gate", "dw_up", "dw_down")
 
 
-def compare_layer(inp, res, cfg, train=True):
-    """Returns {name: rel_err} for every output of the forward / train step."""
+def per_expert_err(a, ref, counts):
+    """max over experts with at least one (kept) row of rel_err(a[e], ref[e]),
+    each expert against its own scale: an expert with a handful of rows has
+    a gradient far smaller than a hot expert's, and a whole-tensor scale
+    would hide its errors."""
+    worst = 0.0
+    for e in np.nonzero(np.asarray(counts) > 0)[0]:
+        worst = max(worst, rel_err(a[e], ref[e]))
+    return worst
+
+
+def compare_layer(inp, res, cfg, train=True, report=None):
+    """Returns {name: rel_err} for every output of the forward / train step,
+    with the routed weight gradients also checked expert by expert
+    ("<name>/expert").  `report` (a dict), when given, receives the
+    elementwise metric of every output beside the normwise one."""
     L, fwd, grads = oracle_on_device_routing(inp, res, cfg, train)
     errs = {"y": rel_err(res["y"], fwd["y"])}
+    elem = {"y": elem_err(res["y"], fwd["y"])}
     logits_ref = oracle.router_logits(inp["x"], inp["w_router"], inp.get("router_bias"))
     errs["logits"] = rel_err(res["logits"], logits_ref)
     if train:
         errs["loss"] = abs(res["loss"] - L) / max(1e-30, float(np.sum(np.abs(fwd["y"] * inp["upstream"]))))
         errs["dx"] = rel_err(res["dx"], grads["dx"])
+        elem["dx"] = elem_err(res["dx"], grads["dx"])
         for k in GRADS:
             if k in grads:
                 errs[k] = rel_err(res[k], grads[k])
+                elem[k] = elem_err(res[k], grads[k])
+        for k in ROUTED:
+            errs[k + "/expert"] = per_expert_err(res[k], grads[k], res["counts"])
+    if report is not None:
+        report["normwise"] = dict(errs)
+        report["elementwise"] = elem
     return errs
+
+
+def log_report(name, report):
+    """Appends one parity record to the JSON-lines file named by the
+    MOE_PARITY_LOG environment variable (nothing when it is unset)."""
+    import json
+    import os
+    path = os.environ.get("MOE_PARITY_LOG")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": name, **report}) + "\n")

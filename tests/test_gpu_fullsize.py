@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from dropless_mixture_experts_gb300.synthetic import CONFIGS
-from gpu_util import TOL, check_routing_bit_exact, compare_layer, run_layer
+from gpu_util import TOL, check_routing_bit_exact, compare_layer, log_report, run_layer
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -22,7 +22,9 @@ def test_full_size_train_step(name):
     inp, layer, dev, res = run_layer(cfg, train=True)
     assert res["status"] == 0
     check_routing_bit_exact(res, cfg)
-    errs = compare_layer(inp, res, cfg, train=True)
+    report = {}
+    errs = compare_layer(inp, res, cfg, train=True, report=report)
+    log_report(name + "/train", report)
     bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
     assert not bad, (name, errs)
     # routing sanity against the pages' layer runs: no empty expert, the
@@ -31,3 +33,19 @@ def test_full_size_train_step(name):
     assert counts.sum() == cfg.tokens * cfg.top_k
     assert np.count_nonzero(counts == 0) == 0
     assert counts.max() / counts.sum() < 2.0 / cfg.experts
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_full_size_forward_only(name):
+    # the forward-only mode (nothing saved for a backward) the forward
+    # throughput is measured in, against the oracle's forward on the same
+    # device routing
+    cfg = CONFIGS[name]
+    inp, layer, dev, res = run_layer(cfg, train=False)
+    assert res["status"] == 0
+    check_routing_bit_exact(res, cfg)
+    report = {}
+    errs = compare_layer(inp, res, cfg, train=False, report=report)
+    log_report(name + "/forward", report)
+    bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
+    assert not bad, (name, errs)

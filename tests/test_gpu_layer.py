@@ -10,7 +10,8 @@ import torch
 
 import oracle
 from dropless_mixture_experts_gb300.synthetic import MoEConfig, make_inputs, params_of
-from gpu_util import (TOL, check_routing_bit_exact, compare_layer, rel_err, run_layer, to_dev)
+from gpu_util import (TOL, check_routing_bit_exact, compare_layer, log_report, rel_err, run_layer,
+                      to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +59,9 @@ def test_train_step_matches_oracle(cfg):
     inp, layer, dev, res = run_layer(cfg)
     assert res["status"] == 0
     check_routing_bit_exact(res, cfg)
-    errs = compare_layer(inp, res, cfg, train=True)
+    report = {}
+    errs = compare_layer(inp, res, cfg, train=True, report=report)
+    log_report(cfg.name, report)
     bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
     assert not bad, (errs, cfg)
 
@@ -76,7 +79,9 @@ def test_planned_numerics_sweep(cfg):
     inp, layer, dev, res = run_layer(cfg)
     assert res["status"] == 0
     check_routing_bit_exact(res, cfg)
-    errs = compare_layer(inp, res, cfg, train=True)
+    report = {}
+    errs = compare_layer(inp, res, cfg, train=True, report=report)
+    log_report(cfg.name, report)
     bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
     assert not bad, (errs, cfg)
 
