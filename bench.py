@@ -50,6 +50,10 @@ def parse():
                     help="comma-separated further workloads measured in the same run and "
                          "reported under 'also' (default: e8k2_bf16_128k beside the default "
                          "workload, none otherwise)")
+    ap.add_argument("--shared-sms", type=int, default=-1,
+                    help="SMs of the side stream that runs the shared expert beside the routed "
+                         "experts (0: one stream; default: 48 of 152, scaled to the device, "
+                         "for workloads with a shared expert)")
     ap.add_argument("--sweep", default="", choices=["", "maxtok"],
                     help="maxtok: the largest train-step token count that fits in free HBM")
     return ap.parse_args()
@@ -497,6 +501,19 @@ def also_default(name):
     return "e8k2_bf16_128k" if name == DEFAULT_CONFIG else ""
 
 
+def shared_sms_of(cfg, args):
+    """SMs of the shared expert's side stream: the command line's, else 48 of
+    152 (the best of a sweep at the decoder workloads), scaled to the
+    device; 0 without a shared expert."""
+    import torch
+    if not cfg.shared_hidden:
+        return 0
+    if args.shared_sms >= 0:
+        return args.shared_sms
+    n = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return max(1, round(n * 48 / 152))
+
+
 def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
     """Times one workload: the train step and the forward (graph replays by
     default), the end-to-end host-input step, and the per-kernel split.
@@ -514,8 +531,10 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
             for k, v in inputs.items()}
     dev = {k: (None if v is None else v.to("cuda", non_blocking=True)) for k, v in host.items()}
     p = {k: dev[k] for k in params_of(inputs)}
+    shared_sms = shared_sms_of(cfg, args)
     layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
-                     cfg.shared_hidden, cfg.dtype, train=True, capacity=cfg.capacity)
+                     cfg.shared_hidden, cfg.dtype, train=True, capacity=cfg.capacity,
+                     shared_sms=shared_sms)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -610,7 +629,9 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
 
     # per-kernel device time and launch count of the forward and of the step
     # (stream launches with an event pair around each launch: a little
-    # slower than the graph-replayed step, so each fraction is a lower bound)
+    # slower than the graph-replayed step, so each fraction is a lower bound;
+    # every kernel on one stream, so that each is timed alone)
+    layer.shared_sms = 0
     prof_steps = 3
     abi.moe_profile_enable(True)
     for _ in range(prof_steps):
@@ -624,6 +645,7 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
         train()
     rec = abi.moe_profile_read()
     abi.moe_profile_enable(False)
+    layer.shared_sms = shared_sms
     pieces = pieces_of(fwd_rec, rec, prof_steps)
     launches_per_step = sum(n for n, _ in rec.values()) / prof_steps
     work = kernel_work(cfg, kept)
@@ -686,8 +708,11 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
                    "l2": "flushed between timed steps (256 MiB write)",
                    "launch": ("a CUDA graph of the whole step, replayed per step"
                               if args.launch == "graph" else "stream launches"),
+                   "shared_expert_stream": (f"side stream, {shared_sms} SMs" if shared_sms
+                                            else "same stream"),
                    "kernel_timing": ("pieces_ms, kernels and roofline: a separate pass of "
-                                     "stream launches with an event pair around each launch"),
+                                     "stream launches on one stream with an event pair "
+                                     "around each launch"),
                    "parallelism": f"independent batch per GPU x{world}"},
         # the dense bf16 tensor peak of the part, and the measured cuBLAS
         # matmul rate (the roofline denominator) beside it

@@ -23,12 +23,14 @@ MOE_F32 = 0
 MOE_BF16 = 1
 MOE_FWD_ONLY = 0
 MOE_SAVE_FOR_BWD = 1
+MOE_SHARED_READY = 2
 
 # every symbol the header declares
 EXPORTS = (
     "moe_status_string", "moe_workspace_bytes", "moe_padded_rows", "moe_route",
     "moe_permute", "moe_grouped_ffn_fwd", "moe_combine", "moe_backward",
     "moe_read_device_status", "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc",
+    "moe_shared_ffn_fwd", "moe_shared_backward", "moe_backward_routed", "moe_set_sm_limit",
 )
 
 
@@ -65,6 +67,10 @@ _SIGS = {
     "moe_grouped_ffn_fwd": ([_D, ctypes.c_int] + [_P] * 9 + [_S, _P], ctypes.c_int),
     "moe_combine": ([_D, ctypes.c_int] + [_P] * 11 + [_S, _P], ctypes.c_int),
     "moe_backward": ([_D] + [_P] * 26 + [_S, _P], ctypes.c_int),
+    "moe_shared_ffn_fwd": ([_D, ctypes.c_int] + [_P] * 8 + [_S, _P], ctypes.c_int),
+    "moe_shared_backward": ([_D] + [_P] * 12 + [_S, _P], ctypes.c_int),
+    "moe_backward_routed": ([_D] + [_P] * 18 + [_S, _P], ctypes.c_int),
+    "moe_set_sm_limit": ([ctypes.c_int], ctypes.c_int),
     "moe_read_device_status": ([_P, _S, _P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
     "moe_profile_enable": ([ctypes.c_int], ctypes.c_int),
     "moe_permute_noalloc": ([_D, _P, _P, _P, _P, _P, _P], ctypes.c_int),
@@ -171,6 +177,45 @@ def moe_backward(dims, dy, x, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws
     if check:
         _check(s, "moe_backward")
     return s
+
+
+def moe_shared_ffn_fwd(dims, mode, x, ws_gate, ws_up, ws_down, hs_buf, as_gate_saved, as_up_saved,
+                       ws, ws_bytes, stream, check=True):
+    s = load().moe_shared_ffn_fwd(ctypes.byref(dims), int(mode), _p(x), _p(ws_gate), _p(ws_up),
+                                  _p(ws_down), _p(hs_buf), _p(as_gate_saved), _p(as_up_saved),
+                                  _p(ws), ws_bytes, _p(stream))
+    if check:
+        _check(s, "moe_shared_ffn_fwd")
+    return s
+
+
+def moe_shared_backward(dims, dy, x, ws_gate, ws_up, ws_down, as_gate_saved, as_up_saved,
+                        hs_saved, dws_gate, dws_up, dws_down, ws, ws_bytes, stream, check=True):
+    args = [dy, x, ws_gate, ws_up, ws_down, as_gate_saved, as_up_saved, hs_saved, dws_gate,
+            dws_up, dws_down, ws]
+    s = load().moe_shared_backward(ctypes.byref(dims), *[_p(a) for a in args], ws_bytes,
+                                   _p(stream))
+    if check:
+        _check(s, "moe_shared_backward")
+    return s
+
+
+def moe_backward_routed(dims, dy, x, w_router, w_gate, w_up, w_down, topk_idx, gates,
+                        a_gate_saved, a_up_saved, h_saved, dx, dw_router, dw_gate, dw_up,
+                        dw_down, shared_done, ws, ws_bytes, stream, check=True):
+    args = [dy, x, w_router, w_gate, w_up, w_down, topk_idx, gates, a_gate_saved, a_up_saved,
+            h_saved, dx, dw_router, dw_gate, dw_up, dw_down, shared_done, ws]
+    s = load().moe_backward_routed(ctypes.byref(dims), *[_p(a) for a in args], ws_bytes,
+                                   _p(stream))
+    if check:
+        _check(s, "moe_backward_routed")
+    return s
+
+
+def moe_set_sm_limit(sms: int):
+    """Caps the SMs the calling thread's later persistent launches may fill
+    (0: all); see include/moe.h."""
+    _check(load().moe_set_sm_limit(int(sms)), "moe_set_sm_limit")
 
 
 def moe_read_device_status(ws, ws_bytes, stream):

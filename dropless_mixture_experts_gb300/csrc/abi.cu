@@ -176,8 +176,11 @@ moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void
                        void* hs_buf, void* as_gate_saved, void* as_up_saved, const void* upstream,
                        float* loss, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
+  // MOE_SHARED_READY: moe_shared_ffn_fwd already left the shared output
+  const bool shared_ready = (mode & MOE_SHARED_READY) != 0;
+  mode &= ~MOE_SHARED_READY;
   if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
-  const bool shared = dims->shared_hidden > 0;
+  const bool shared = dims->shared_hidden > 0 && !shared_ready;
   if (dims->tokens > 0) {
     if (!y) return MOE_ERR_INVALID_ARG;
     if (shared && (!x || !ws_gate || !ws_up || !ws_down || !hs_buf)) return MOE_ERR_INVALID_ARG;
@@ -209,23 +212,65 @@ moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void
   return cuda_status();
 }
 
-moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, const void* w_router,
-                        const void* w_gate, const void* w_up, const void* w_down,
-                        const void* ws_gate, const void* ws_up, const void* ws_down,
-                        const int32_t* topk_idx, const float* gates, const void* a_gate_saved,
-                        const void* a_up_saved, const void* h_saved, const void* as_gate_saved,
-                        const void* as_up_saved, const void* hs_saved, void* dx,
-                        float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
-                        float* dws_gate, float* dws_up, float* dws_down, void* workspace,
-                        size_t workspace_bytes, cudaStream_t stream) {
+moe_status moe_shared_ffn_fwd(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
+                              const void* ws_up, const void* ws_down, void* hs_buf,
+                              void* as_gate_saved, void* as_up_saved, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
   if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
-  const bool shared = dims->shared_hidden > 0;
-  if (!dw_router || !dw_gate || !dw_up || !dw_down || !w_router) return MOE_ERR_INVALID_ARG;
+  if (mode != MOE_FWD_ONLY && mode != MOE_SAVE_FOR_BWD) return MOE_ERR_INVALID_ARG;
+  if (dims->shared_hidden == 0) return MOE_OK;
+  if (dims->tokens > 0) {
+    if (!x || !ws_gate || !ws_up || !ws_down || !hs_buf) return MOE_ERR_INVALID_ARG;
+    if (mode == MOE_SAVE_FOR_BWD && (!as_gate_saved || !as_up_saved)) return MOE_ERR_INVALID_ARG;
+  }
+  if (!aligned16({x, ws_gate, ws_up, ws_down, hs_buf, as_gate_saved, as_up_saved}))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(shape_supported(dims));
+  MOE_TRY(check_ws(dims, MOE_FWD_ONLY, workspace, workspace_bytes));
+  if (dims->tokens == 0) return MOE_OK;
+  const Layout L = make_layout(*dims, MOE_FWD_ONLY);
+  LayerPtrs p;
+  p.x = x;
+  p.ws_gate = ws_gate;
+  p.ws_up = ws_up;
+  p.ws_down = ws_down;
+  p.hs_buf = hs_buf;
+  p.as_gate = as_gate_saved;
+  p.as_up = as_up_saved;
+  if (dims->dtype == MOE_BF16) {
+    if (!tc_shared_fwd(*dims, L, mode, p, workspace, stream)) return MOE_ERR_CUDA;
+  } else {
+    simt_shared_fwd(*dims, L, mode, p, workspace, stream);
+  }
+  return cuda_status();
+}
+
+namespace {
+
+// The backward's shared part (dws_*, and the shared expert's rows of dx in
+// the workspace) and routed part (the routed experts' GEMMs and the router
+// backward, which also forms dx); `parts`: 1 shared, 2 routed, 3 both.
+moe_status backward_parts(int parts, const moe_dims* dims, const void* dy, const void* x,
+                          const void* w_router, const void* w_gate, const void* w_up,
+                          const void* w_down, const void* ws_gate, const void* ws_up,
+                          const void* ws_down, const int32_t* topk_idx, const float* gates,
+                          const void* a_gate_saved, const void* a_up_saved, const void* h_saved,
+                          const void* as_gate_saved, const void* as_up_saved,
+                          const void* hs_saved, void* dx, float* dw_router, float* dw_gate,
+                          float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
+                          float* dws_down, cudaEvent_t shared_done, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  if (!dims_ok(dims)) return MOE_ERR_INVALID_ARG;
+  const bool routed = parts & 2;
+  const bool shared = (parts & 1) && dims->shared_hidden > 0;
+  if (routed && (!dw_router || !dw_gate || !dw_up || !dw_down || !w_router))
+    return MOE_ERR_INVALID_ARG;
   if (shared && (!dws_gate || !dws_up || !dws_down || !ws_gate || !ws_up || !ws_down))
     return MOE_ERR_INVALID_ARG;
   if (dims->tokens > 0) {
-    if (!dy || !x || !w_gate || !w_up || !w_down || !topk_idx || !gates || !a_gate_saved ||
-        !a_up_saved || !h_saved || !dx)
+    if (!dy || !x) return MOE_ERR_INVALID_ARG;
+    if (routed && (!w_gate || !w_up || !w_down || !topk_idx || !gates || !a_gate_saved ||
+                   !a_up_saved || !h_saved || !dx))
       return MOE_ERR_INVALID_ARG;
     if (shared && (!as_gate_saved || !as_up_saved || !hs_saved)) return MOE_ERR_INVALID_ARG;
   }
@@ -235,16 +280,18 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
     return MOE_ERR_INVALID_ARG;
   MOE_TRY(shape_supported(dims));
   // the router backward keeps W_r^T and one dW_r column block in shared memory
-  if (!router_backward_supported(*dims)) return MOE_ERR_UNSUPPORTED;
+  if (routed && !router_backward_supported(*dims)) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_ws(dims, MOE_SAVE_FOR_BWD, workspace, workspace_bytes));
   const Layout L = make_layout(*dims, MOE_SAVE_FOR_BWD);
   const int64_t E = dims->experts, dm = dims->d_model, h = dims->d_hidden,
                 hs = dims->shared_hidden;
   if (dims->tokens == 0) {
-    zero_fill_f32(dw_router, dm * E, stream);
-    zero_fill_f32(dw_gate, E * dm * h, stream);
-    zero_fill_f32(dw_up, E * dm * h, stream);
-    zero_fill_f32(dw_down, E * h * dm, stream);
+    if (routed) {
+      zero_fill_f32(dw_router, dm * E, stream);
+      zero_fill_f32(dw_gate, E * dm * h, stream);
+      zero_fill_f32(dw_up, E * dm * h, stream);
+      zero_fill_f32(dw_down, E * h * dm, stream);
+    }
     if (shared) {
       zero_fill_f32(dws_gate, dm * hs, stream);
       zero_fill_f32(dws_up, dm * hs, stream);
@@ -278,18 +325,76 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, con
   p.dws_gate = dws_gate;
   p.dws_up = dws_up;
   p.dws_down = dws_down;
+  const bool bf = dims->dtype == MOE_BF16;
+  if (shared) {
+    if (bf) {
+      if (!tc_backward_shared(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
+    } else {
+      simt_backward_shared(*dims, L, p, workspace, stream);
+    }
+  }
+  if (!routed) return cuda_status();
   // gate-gradient partials per pair: one per DZ column tile (and column
   // half of the tensor-core epilogue), pairs 2*h/64 apart
   const int dg_ld = (int)(2 * h / 64);
   int dg_n = (int)(h / 64);
-  if (dims->dtype == MOE_BF16) {
-    if (!tc_backward_gemms(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
+  if (bf) {
+    if (!tc_backward_routed(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
     dg_n = (int)(2 * h / tc_dz_bn((int)h));
   } else {
-    simt_backward_gemms(*dims, L, p, workspace, stream);
+    simt_backward_routed(*dims, L, p, workspace, stream);
   }
-  launch_router_backward(*dims, L, p, dg_n, dg_ld, workspace, stream);
+  launch_router_backward(*dims, L, p, dg_n, dg_ld, workspace, stream, shared_done);
   return cuda_status();
+}
+
+}  // namespace
+
+moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x, const void* w_router,
+                        const void* w_gate, const void* w_up, const void* w_down,
+                        const void* ws_gate, const void* ws_up, const void* ws_down,
+                        const int32_t* topk_idx, const float* gates, const void* a_gate_saved,
+                        const void* a_up_saved, const void* h_saved, const void* as_gate_saved,
+                        const void* as_up_saved, const void* hs_saved, void* dx,
+                        float* dw_router, float* dw_gate, float* dw_up, float* dw_down,
+                        float* dws_gate, float* dws_up, float* dws_down, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  return backward_parts(3, dims, dy, x, w_router, w_gate, w_up, w_down, ws_gate, ws_up, ws_down,
+                        topk_idx, gates, a_gate_saved, a_up_saved, h_saved, as_gate_saved,
+                        as_up_saved, hs_saved, dx, dw_router, dw_gate, dw_up, dw_down, dws_gate,
+                        dws_up, dws_down, nullptr, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_shared_backward(const moe_dims* dims, const void* dy, const void* x,
+                               const void* ws_gate, const void* ws_up, const void* ws_down,
+                               const void* as_gate_saved, const void* as_up_saved,
+                               const void* hs_saved, float* dws_gate, float* dws_up,
+                               float* dws_down, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  if (dims && dims->shared_hidden == 0) return dims_ok(dims) ? MOE_OK : MOE_ERR_INVALID_ARG;
+  return backward_parts(1, dims, dy, x, nullptr, nullptr, nullptr, nullptr, ws_gate, ws_up,
+                        ws_down, nullptr, nullptr, nullptr, nullptr, nullptr, as_gate_saved,
+                        as_up_saved, hs_saved, nullptr, nullptr, nullptr, nullptr, nullptr,
+                        dws_gate, dws_up, dws_down, nullptr, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_backward_routed(const moe_dims* dims, const void* dy, const void* x,
+                               const void* w_router, const void* w_gate, const void* w_up,
+                               const void* w_down, const int32_t* topk_idx, const float* gates,
+                               const void* a_gate_saved, const void* a_up_saved,
+                               const void* h_saved, void* dx, float* dw_router, float* dw_gate,
+                               float* dw_up, float* dw_down, cudaEvent_t shared_done,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return backward_parts(2, dims, dy, x, w_router, w_gate, w_up, w_down, nullptr, nullptr, nullptr,
+                        topk_idx, gates, a_gate_saved, a_up_saved, h_saved, nullptr, nullptr,
+                        nullptr, dx, dw_router, dw_gate, dw_up, dw_down, nullptr, nullptr,
+                        nullptr, shared_done, workspace, workspace_bytes, stream);
+}
+
+moe_status moe_set_sm_limit(int sms) {
+  if (sms < 0) return MOE_ERR_INVALID_ARG;
+  tcg::set_sm_limit(sms);
+  return MOE_OK;
 }
 
 moe_status moe_read_device_status(void* workspace, size_t workspace_bytes, cudaStream_t stream,

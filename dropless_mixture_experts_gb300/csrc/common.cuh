@@ -72,7 +72,9 @@ struct Layout {
   size_t gH, gHs;  // gate * H for the W_down gradients (float32 path only)
   size_t dl;      // dense router-logit gradient [T, E] (bf16 path)
   size_t wrt;     // W_r^T [E, d]
-  size_t dwpart;  // per-split / per-chunk partials of the weight-gradient GEMMs
+  size_t dwpart;  // per-split / per-chunk partials of the routed and router weight-gradient GEMMs
+  size_t dwpart_sh;  // per-split partials of the shared expert's weight gradients (a region of
+                     // its own: the shared expert's backward may run beside the routed one)
   size_t dw_tick;    // the routed weight gradients' per-tile chunk tickets [dw_tick_n]
   int64_t dw_tick_n;
   size_t total;
@@ -194,12 +196,14 @@ inline Layout make_layout(const moe_dims& d, int mode) {
     };
     int64_t pf = chunked(h, dm, pick_bn((int)dm));
     pf = std::max(pf, chunked(dm, 2 * h, pick_bn((int)h)));
+    int64_t pfs = 0;
     if (hs > 0) {
-      pf = std::max(pf, need(1, hs, dm, pick_bn((int)dm), false));
-      pf = std::max(pf, need(1, dm, 2 * hs, pick_bn((int)hs), false));
+      pfs = std::max(pfs, need(1, hs, dm, pick_bn((int)dm), false));
+      pfs = std::max(pfs, need(1, dm, 2 * hs, pick_bn((int)hs), false));
     }
     pf = std::max(pf, (int64_t)router_dw_split_bound((dm + 127) / 128) * dm * 64);
     L.dwpart = take(sizeof(float) * pf);
+    L.dwpart_sh = take(sizeof(float) * pfs);
     L.dw_tick_n = std::max(E * ((h + 127) / 128) * (dm / pick_bn((int)dm)),
                            E * ((dm + 127) / 128) * (2 * h / pick_bn((int)h)));
     L.dw_tick = take(sizeof(int) * L.dw_tick_n);

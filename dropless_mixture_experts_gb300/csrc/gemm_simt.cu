@@ -455,13 +455,12 @@ void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs&
   launch<DOWN, T, false>(b, b.n_ntiles * mt, s);
 }
 
+// the shared expert's backward (dxs and its weight gradients)
 template <typename T>
-void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, cudaStream_t s) {
-  const int h = d.d_hidden, dm = d.d_model, E = d.experts, hs = d.shared_hidden;
-  void* dA = at<void>(ws, L.dA);
-  void* gH = at<void>(ws, L.gH);
+void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                       cudaStream_t s) {
+  const int dm = d.d_model, hs = d.shared_hidden;
   const int64_t mt_dense = (d.tokens + BM - 1) / BM;
-
   if (hs > 0) {
     void* dAs = at<void>(ws, L.dAs);
     void* gHs = at<void>(ws, L.gHs);
@@ -521,8 +520,15 @@ void backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws
     g.n_ntiles = 2 * hs / BN;
     launch<DWGU, T, false>(g, (int64_t)g.n_ntiles * g.n_mtiles, s);
   }
+}
 
-  // routed experts
+// the routed experts' backward
+template <typename T>
+void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                       cudaStream_t s) {
+  const int h = d.d_hidden, dm = d.d_model, E = d.experts;
+  void* dA = at<void>(ws, L.dA);
+  void* gH = at<void>(ws, L.gH);
   SimtArgs z;
   z.tiles = at<int4>(ws, L.tiles);
   z.ntiles = at<int>(ws, L.ntiles);
@@ -604,10 +610,15 @@ void simt_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPt
   if (d.dtype == MOE_BF16) shared_fwd_t<__nv_bfloat16>(d, L, mode, p, ws, s);
   else shared_fwd_t<float>(d, L, mode, p, ws, s);
 }
-void simt_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
-                         cudaStream_t s) {
-  if (d.dtype == MOE_BF16) backward_t<__nv_bfloat16>(d, L, p, ws, s);
-  else backward_t<float>(d, L, p, ws, s);
+void simt_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                          cudaStream_t s) {
+  if (d.dtype == MOE_BF16) backward_routed_t<__nv_bfloat16>(d, L, p, ws, s);
+  else backward_routed_t<float>(d, L, p, ws, s);
+}
+void simt_backward_shared(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                          cudaStream_t s) {
+  if (d.dtype == MOE_BF16) backward_shared_t<__nv_bfloat16>(d, L, p, ws, s);
+  else backward_shared_t<float>(d, L, p, ws, s);
 }
 
 }  // namespace moe

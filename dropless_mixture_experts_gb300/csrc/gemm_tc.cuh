@@ -68,6 +68,9 @@ struct Params {
   float* part = nullptr;            // DW kinds: per-split partials [splits][E][M][ldp]
   int ldp = 0;                      //   (reduced in a fixed order by a second kernel)
                                     // routed DW kinds: per-chunk partials [chunk][M][ldp]
+  int sched_units = 0;              // routed DW kinds: the work units the chunk schedule
+                                    //   balances over (the whole device's, so that the
+                                    //   schedule and the results do not depend on the grid)
   int* dw_tick = nullptr;           // routed DW kinds: per output tile, the chunks done;
                                     //   routed DZ zeroes them (dw_tick_n) for the DW launches
   int dw_tick_n = 0;
@@ -498,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if constexpr (C::DW && C::ROUTED) {
     if (warp == 2)  // an epilogue warp (idle until the first tile is ready)
-      dw_chunk_schedule(p.counts, p.experts, (C::PAIR ? p.n_mt / 2 : p.n_mt) * p.n_nt, us,
-                        choff);
+      dw_chunk_schedule(p.counts, p.experts, (C::PAIR ? p.n_mt / 2 : p.n_mt) * p.n_nt,
+                        p.sched_units > 0 ? p.sched_units : us, choff);
   }
   if constexpr (C::EK == E_DZ && C::ROUTED) {
     // the chunk tickets of the weight-gradient launches that follow start at 0
@@ -949,7 +952,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // host side
 // ---------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn();
-int sm_count();
+int sm_count();    // SMs of the current device
+int launch_sms();  // SMs the calling thread's launches may fill (moe_set_sm_limit)
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, out-of-bounds
 // elements read as zero (stores outside are dropped).  Operand tiles use the
@@ -969,7 +973,7 @@ void launch_tc(const Maps& maps, const Params& p, int64_t max_tiles, const char*
                          C::SMEM_BYTES);
     attr = true;
   }
-  const int sms = sm_count();
+  const int sms = launch_sms();
   if constexpr (C::PAIR) {
     // max_tiles counts pair units; two CTAs (one cluster) per unit, no more
     // clusters than can be resident at once (an SM whose partner SM is not
@@ -988,13 +992,15 @@ void launch_tc(const Maps& maps, const Params& p, int64_t max_tiles, const char*
     cfg.numAttrs = 1;
     static int resident = 0;
     if (resident == 0) {
-      cfg.gridDim = dim3(sms, 1, 1);
+      cfg.gridDim = dim3(sm_count(), 1, 1);
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<C>, &cfg) != cudaSuccess || n < 1)
-        n = sms / 2;
+        n = sm_count() / 2;
       resident = n;
     }
-    const int pairs = (int)(max_tiles < resident ? max_tiles : resident);
+    int cap = resident < sms / 2 ? resident : sms / 2;
+    if (cap < 1) cap = 1;
+    const int pairs = (int)(max_tiles < cap ? max_tiles : cap);
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     MOE_LAUNCH(name, s, cudaLaunchKernelEx(&cfg, tc_gemm_kernel<C>, maps, p));
   } else {

@@ -15,6 +15,13 @@ void prof_end(cudaStream_t s);
     ::moe::prof_end(stream);            \
   } while (0)
 
+// SMs the calling thread's launches may fill (tc_host.cu; moe_set_sm_limit)
+namespace tcg {
+int launch_sms();
+void set_sm_limit(int n);
+}  // namespace tcg
+inline int tcg_launch_sms() { return tcg::launch_sms(); }
+
 // utility kernels (misc.cu)
 void zero_fill_i32(int32_t* p, int64_t n, cudaStream_t s);
 void zero_fill_f32(float* p, int64_t n, cudaStream_t s);
@@ -73,8 +80,10 @@ void simt_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerP
                       cudaStream_t s);
 void simt_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                      cudaStream_t s);
-void simt_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
-                         cudaStream_t s);
+void simt_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                          cudaStream_t s);
+void simt_backward_shared(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                          cudaStream_t s);
 
 // grouped expert GEMMs on the tensor cores (tc_fwd.cu, tc_bwd.cu: bfloat16
 // storage); false when a tensor map could not be encoded
@@ -82,8 +91,10 @@ bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtr
                     cudaStream_t s);
 bool tc_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                    cudaStream_t s);
-bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
-                       cudaStream_t s);
+bool tc_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                        cudaStream_t s);
+bool tc_backward_shared(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                        cudaStream_t s);
 int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials per row)
 // router weight gradient x^T dlogits on the tensor cores (bf16, E a multiple of 8, <= 64)
 bool tc_router_dw_supported(const moe_dims& d);
@@ -110,7 +121,9 @@ void launch_router_dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, co
 
 // router backward (router_bwd.cu)
 bool router_backward_supported(const moe_dims& d);
+// the input-gradient kernel (which adds the shared expert's dx rows) waits
+// for `shared_done` when it is given
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
-                            int dg_ld, void* ws, cudaStream_t s);
+                            int dg_ld, void* ws, cudaStream_t s, cudaEvent_t shared_done = nullptr);
 
 }  // namespace moe

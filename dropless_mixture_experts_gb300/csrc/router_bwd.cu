@@ -136,10 +136,11 @@ __global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __re
 
 template <typename T>
 void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
-                       int dg_ld, void* ws, cudaStream_t s) {
+                       int dg_ld, void* ws, cudaStream_t s, cudaEvent_t shared_done) {
   const int dm = d.d_model, E = d.experts, k = d.top_k;
   if (d.tokens == 0) {
     zero_fill_f32(p.dw_router, (int64_t)dm * E, s);
+    if (shared_done) cudaStreamWaitEvent(s, shared_done, 0);
     return;
   }
   float* dsel = at<float>(ws, L.dsel);
@@ -168,10 +169,15 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
                  tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr, dsel_blocks,
                  reinterpret_cast<const T*>(p.w_router), dm, wt));
 
-  launch_router_dx(d, L, p, dsel, wt, ws, s);
-
+  // the router weight gradient first: the input gradient also needs the
+  // shared expert's rows, which may come from another stream
+  auto input_grad = [&] {
+    if (shared_done) cudaStreamWaitEvent(s, shared_done, 0);
+    launch_router_dx(d, L, p, dsel, wt, ws, s);
+  };
   if (tc_dw) {
     tc_router_dw(d, L, p, ws, s);
+    input_grad();
     return;
   }
   const int ny = (dm + 255) / 256;
@@ -189,14 +195,17 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
   MOE_LAUNCH("router_dw_reduce", s,
              router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
                  part, (int)ranges, n, p.dw_router));
+  input_grad();
 }
 
 }  // namespace
 
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
-                            int dg_ld, void* ws, cudaStream_t s) {
-  if (d.dtype == MOE_BF16) router_backward_t<__nv_bfloat16>(d, L, p, dg_n, dg_ld, ws, s);
-  else router_backward_t<float>(d, L, p, dg_n, dg_ld, ws, s);
+                            int dg_ld, void* ws, cudaStream_t s, cudaEvent_t shared_done) {
+  if (d.dtype == MOE_BF16)
+    router_backward_t<__nv_bfloat16>(d, L, p, dg_n, dg_ld, ws, s, shared_done);
+  else
+    router_backward_t<float>(d, L, p, dg_n, dg_ld, ws, s, shared_done);
 }
 
 bool router_backward_supported(const moe_dims& d) {

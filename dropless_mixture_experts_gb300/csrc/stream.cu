@@ -17,10 +17,16 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBlocksPerSm = 32;  // grid-stride launches: 4 full-occupancy waves
 
-unsigned stream_grid(int64_t items, int64_t cap) {
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+// Grid of a grid-stride launch: up to kBlocksPerSm blocks per SM the launch
+// may fill (capped = false: per SM of the device, for a launch whose
+// reduction order follows its grid and must not depend on the SM limit).
+unsigned stream_grid(int64_t items, int64_t cap, bool capped = true) {
+  int sms = tcg_launch_sms();
+  if (!capped) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
   int64_t b = (items + kThreads - 1) / kThreads;
   const int64_t full = (int64_t)sms * kBlocksPerSm;
   if (b > full) b = full;
@@ -322,7 +328,9 @@ void combine_t(const moe_dims& d, const Layout& L, void* y, const void* G, float
   float* part = G ? at<float>(ws, L.loss_part) : nullptr;
   const T* ys = d.shared_hidden > 0 ? at<const T>(ws, L.ys) : nullptr;
   const int64_t items = d.tokens * (d.d_model / (16 / (int)sizeof(T)));
-  const unsigned blocks = stream_grid(items, kLossBlocks);
+  // the loss partials are summed in block order: the grid must not follow
+  // the SM limit
+  const unsigned blocks = stream_grid(items, kLossBlocks, false);
   auto launch = [&](auto kernel) {
     MOE_LAUNCH("combine", s,
                kernel<<<blocks, kThreads, 0, s>>>(

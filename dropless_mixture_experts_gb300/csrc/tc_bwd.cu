@@ -122,7 +122,7 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
 // than half of the GPU (a split costs a partial write and a reduction), at
 // least four 64-row K blocks per split, never beyond the workspace's bound
 int splits_for(int64_t tiles, int64_t kblocks_per_tile) {
-  const int sms = sm_count();
+  const int sms = sm_count();  // the device's (not the launch limit's): fixed results
   const int cap = split_bound(tiles);
   int s = 1;
   while (tiles * s * 2 <= sms && s < cap && kblocks_per_tile / (s * 2) >= 4) s *= 2;
@@ -131,9 +131,10 @@ int splits_for(int64_t tiles, int64_t kblocks_per_tile) {
 
 // Shared tail of the DW launches: partials when split, the fixed-order
 // reduction afterwards.
+// (the shared expert's weight gradients: partials in a region of their own)
 void set_splits(Params& q, const Layout& L, void* ws, int64_t kblocks, bool always_partials) {
   q.splits = splits_for((int64_t)q.experts * q.n_mt * q.n_nt, kblocks);
-  if (q.splits > 1 || always_partials) q.part = at<float>(ws, L.dwpart);
+  if (q.splits > 1 || always_partials) q.part = at<float>(ws, L.dwpart_sh);
 }
 
 void reduce_splits(const Params& q, float* out0, float* out1, cudaStream_t s) {
@@ -153,6 +154,7 @@ int64_t set_chunks(Params& q, const Layout& L, void* ws, bool pair = false) {
   q.dw_tick = at<int>(ws, L.dw_tick);
   const int64_t tpe = (int64_t)(pair ? q.n_mt / 2 : q.n_mt) * q.n_nt;
   const int64_t grid = pair ? sm_count() / 2 : sm_count();
+  q.sched_units = (int)grid;  // the whole device's units, whatever the launch's SM limit
   return (q.experts + grid / tpe + 1) * tpe;
 }
 
@@ -288,11 +290,15 @@ bool backward_one(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* 
 
 int tc_dz_bn(int h) { return pick_bn(h); }
 
-bool tc_backward_gemms(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
-                       cudaStream_t s) {
+bool tc_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                        cudaStream_t s) {
   launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s, p.gates);
-  if (d.shared_hidden > 0 && !backward_one(d, L, p, ws, false, s)) return false;
   return backward_one(d, L, p, ws, true, s);
+}
+
+bool tc_backward_shared(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                        cudaStream_t s) {
+  return d.shared_hidden == 0 || backward_one(d, L, p, ws, false, s);
 }
 
 bool tc_router_dw_supported(const moe_dims& d) {

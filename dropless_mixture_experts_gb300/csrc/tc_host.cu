@@ -28,6 +28,17 @@ int sm_count() {
   return n > 0 ? n : 1;
 }
 
+namespace {
+thread_local int t_sm_limit = 0;  // 0: every SM
+}
+
+int launch_sms() {
+  const int n = sm_count();
+  return t_sm_limit > 0 && t_sm_limit < n ? t_sm_limit : n;
+}
+
+void set_sm_limit(int n) { t_sm_limit = n > 0 ? n : 0; }
+
 bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
               uint32_t box_rows) {
   auto fn = encode_fn();

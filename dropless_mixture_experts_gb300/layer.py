@@ -22,16 +22,23 @@ def _ptr(t):
 class MoELayer:
     """Buffers and calls for one (tokens, d_model, d_hidden, experts, top_k,
     shared_hidden, dtype) problem on one CUDA device.  capacity > 0 switches
-    on capacity routing (each expert keeps its first ``capacity`` pairs)."""
+    on capacity routing (each expert keeps its first ``capacity`` pairs).
+
+    shared_sms > 0 (with a shared expert): the shared expert's forward and
+    backward run on a second stream beside the routed experts, its
+    persistent kernels capped at ``shared_sms`` SMs and the routed ones at
+    the rest (``moe_set_sm_limit``); the results are the same as with
+    shared_sms = 0, where every call runs on the current stream in turn."""
 
     def __init__(self, tokens, d_model, d_hidden, experts, top_k, shared_hidden=0, dtype="bf16",
-                 device="cuda", train=True, capacity=0):
+                 device="cuda", train=True, capacity=0, shared_sms=0):
         self.T, self.d, self.h, self.E, self.k, self.hs = (
             int(tokens), int(d_model), int(d_hidden), int(experts), int(top_k), int(shared_hidden))
         self.tdtype, cdt = _DT[dtype]
         self.dtype = dtype
         self.device = torch.device(device)
         self.capacity = int(capacity)
+        self.shared_sms = int(shared_sms) if shared_hidden else 0
         self.dims = abi.make_dims(self.T, self.d, self.h, self.E, self.k, self.hs, cdt,
                                   self.capacity)
         self.mode = abi.MOE_SAVE_FOR_BWD if train else abi.MOE_FWD_ONLY
@@ -109,9 +116,80 @@ class MoELayer:
                          _ptr(g["dw_down"]), _ptr(g["dws_gate"]), _ptr(g["dws_up"]),
                          _ptr(g["dws_down"]), self.ws_ptr, self.ws_bytes, self._stream())
 
+    # -- the shared expert on its own stream ---------------------------------
+    def shared_ffn_fwd(self, x, p, mode):
+        abi.moe_shared_ffn_fwd(self.dims, mode, _ptr(x), _ptr(p.get("ws_gate")),
+                               _ptr(p.get("ws_up")), _ptr(p.get("ws_down")), _ptr(self.hs_buf),
+                               _ptr(self.as_gate if mode else None),
+                               _ptr(self.as_up if mode else None), self.ws_ptr, self.ws_bytes,
+                               self._stream())
+
+    def shared_backward(self, x, p, dy):
+        g = self.grads
+        abi.moe_shared_backward(self.dims, _ptr(dy), _ptr(x), _ptr(p.get("ws_gate")),
+                                _ptr(p.get("ws_up")), _ptr(p.get("ws_down")), _ptr(self.as_gate),
+                                _ptr(self.as_up), _ptr(self.hs_buf), _ptr(g["dws_gate"]),
+                                _ptr(g["dws_up"]), _ptr(g["dws_down"]), self.ws_ptr,
+                                self.ws_bytes, self._stream())
+
+    def backward_routed(self, x, p, dy, shared_done=None):
+        g = self.grads
+        abi.moe_backward_routed(self.dims, _ptr(dy), _ptr(x), _ptr(p["w_router"]),
+                                _ptr(p["w_gate"]), _ptr(p["w_up"]), _ptr(p["w_down"]),
+                                _ptr(self.idx), _ptr(self.gates), _ptr(self.a_gate),
+                                _ptr(self.a_up), _ptr(self.h_buf), _ptr(self.dx),
+                                _ptr(g["dw_router"]), _ptr(g["dw_gate"]), _ptr(g["dw_up"]),
+                                _ptr(g["dw_down"]),
+                                None if shared_done is None else shared_done.cuda_event,
+                                self.ws_ptr, self.ws_bytes, self._stream())
+
+    def _side(self):
+        if getattr(self, "sh_stream", None) is None:
+            self.sh_stream = torch.cuda.Stream(self.device)
+            self.sh_fwd_done = torch.cuda.Event()
+            self.sh_bwd_done = torch.cuda.Event()
+        return self.sh_stream
+
+    def _overlapped(self, x, p, mode, upstream, dy, logits_in, dy_ready=None):
+        """The pass with the shared expert (forward, and backward when dy is
+        given) on the side stream beside the routed experts on the current
+        stream; the combine waits for the shared forward, the input
+        gradient for the shared backward, and the current stream joins the
+        side stream at the end."""
+        main = torch.cuda.current_stream(self.device)
+        side = self._side()
+        n = torch.cuda.get_device_properties(self.device).multi_processor_count
+        side.wait_stream(main)  # x and the weights are ready
+        with torch.cuda.stream(side):
+            abi.moe_set_sm_limit(self.shared_sms)
+            self.shared_ffn_fwd(x, p, mode)
+            self.sh_fwd_done.record(side)
+            if dy is not None:
+                if dy_ready is not None:
+                    side.wait_event(dy_ready)
+                self.shared_backward(x, p, dy)
+                self.sh_bwd_done.record(side)
+        abi.moe_set_sm_limit(max(1, n - self.shared_sms))
+        try:
+            self.route(x, p["w_router"], logits_in, p.get("router_bias"))
+            self.permute()
+            self.grouped_ffn_fwd(x, p, mode)
+            main.wait_event(self.sh_fwd_done)
+            if dy_ready is not None:
+                main.wait_event(dy_ready)
+            self.combine(x, p, mode | abi.MOE_SHARED_READY, upstream=upstream)
+            if dy is not None:
+                self.backward_routed(x, p, dy, shared_done=self.sh_bwd_done)
+        finally:
+            abi.moe_set_sm_limit(0)
+        main.wait_stream(side)
+
     # -- composed passes ---------------------------------------------------
     def forward(self, x, p, logits_in=None):
         """y = layer(x); returns the output buffer (valid until the next call)."""
+        if self.shared_sms > 0:
+            self._overlapped(x, p, abi.MOE_FWD_ONLY, None, None, logits_in)
+            return self.y
         self.route(x, p["w_router"], logits_in, p.get("router_bias"))
         self.permute()
         self.grouped_ffn_fwd(x, p, abi.MOE_FWD_ONLY)
@@ -123,6 +201,9 @@ class MoELayer:
         dx, grads dict); all are the layer's buffers."""
         if self.mode != abi.MOE_SAVE_FOR_BWD:
             raise RuntimeError("layer was built with train=False")
+        if self.shared_sms > 0:
+            self._overlapped(x, p, abi.MOE_SAVE_FOR_BWD, dy, dy, logits_in)
+            return self.loss, self.dx, self.grads
         self.route(x, p["w_router"], logits_in, p.get("router_bias"))
         self.permute()
         self.grouped_ffn_fwd(x, p, abi.MOE_SAVE_FOR_BWD)
@@ -153,12 +234,16 @@ class MoELayer:
             self.dy_dev.copy_(dy_host, non_blocking=True)
             self.dy_ready.record(self.side)
         x = self.x_dev
-        self.route(x, p["w_router"], None, p.get("router_bias"))
-        self.permute()
-        self.grouped_ffn_fwd(x, p, abi.MOE_SAVE_FOR_BWD)
-        main.wait_event(self.dy_ready)
-        self.combine(x, p, abi.MOE_SAVE_FOR_BWD, upstream=self.dy_dev)
-        self.backward(x, p, self.dy_dev)
+        if self.shared_sms > 0:
+            self._overlapped(x, p, abi.MOE_SAVE_FOR_BWD, self.dy_dev, self.dy_dev, None,
+                             dy_ready=self.dy_ready)
+        else:
+            self.route(x, p["w_router"], None, p.get("router_bias"))
+            self.permute()
+            self.grouped_ffn_fwd(x, p, abi.MOE_SAVE_FOR_BWD)
+            main.wait_event(self.dy_ready)
+            self.combine(x, p, abi.MOE_SAVE_FOR_BWD, upstream=self.dy_dev)
+            self.backward(x, p, self.dy_dev)
         if loss_host is not None:
             loss_host.copy_(self.loss, non_blocking=True)
         if dx_host is not None:

@@ -74,7 +74,10 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
 typedef enum {
   MOE_FWD_ONLY = 0,      /* forward only: nothing saved for a backward     */
-  MOE_SAVE_FOR_BWD = 1   /* forward of a train step: pre-activations saved */
+  MOE_SAVE_FOR_BWD = 1,  /* forward of a train step: pre-activations saved */
+  MOE_SHARED_READY = 2   /* moe_combine flag (OR-ed into the mode): the
+                            shared expert's output was already produced by
+                            moe_shared_ffn_fwd on this workspace          */
 } moe_mode;
 
 typedef struct {
@@ -102,7 +105,10 @@ moe_status moe_workspace_bytes(const moe_dims* dims, int mode, size_t* bytes);
  * T*k + E*127 rounded up to 128. */
 moe_status moe_padded_rows(const moe_dims* dims, int64_t* rows);
 
-/* Router: logits = x W_r (+ router_bias) (float32 accumulate), then per
+/* Passage: the `route` piece of kernel_gmm_gpu.json (pieces suite) and the
+ * `top_k` field of gpu_moe_h100.json; the bias-free d x E router from the
+ * parameter count of gpu_nn.json.
+ * Router: logits = x W_r (+ router_bias) (float32 accumulate), then per
  * token the top-k experts (ties to the lower index, descending slots) and
  * the softmax of the selected logits.
  *   x          [T, d]  (dtype)            w_router [d, E] (dtype)
@@ -121,7 +127,9 @@ moe_status moe_route(const moe_dims* dims, const void* x, const void* w_router,
                      int32_t* topk_idx, float* gates, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream);
 
-/* Counting sort of the T*k pairs p = t*k + j by expert topk_idx[p],
+/* Passage: the `sort_permute` piece and the `sorted` dispatch of
+ * kernel_gmm_gpu.json.
+ * Counting sort of the T*k pairs p = t*k + j by expert topk_idx[p],
  * stable in p.
  *   counts   [E]     int32 out: pairs per expert
  *   offsets  [E+1]   int32 out: exclusive prefix sum of counts
@@ -141,7 +149,9 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
                        int32_t* offsets, int32_t* perm, int32_t* inv_perm,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Grouped SwiGLU experts over the expert-sorted rows (the token rows are
+/* Passage: the `experts_grouped_swiglu` piece of kernel_gmm_gpu.json (the
+ * three bias-free 512 x 1024 matrices per expert of gpu_nn.json's count).
+ * Grouped SwiGLU experts over the expert-sorted rows (the token rows are
  * first gathered into expert-sorted order inside the workspace):
  *   h_buf[r] = silu(x_t W_gate[e]) * (x_t W_up[e])     [padded_rows, h] (dtype)
  *   then, for the down projection, gates[t, j] * (h_buf[r] W_down[e]) is
@@ -155,7 +165,11 @@ moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x,
                                void* a_up_saved, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream);
 
-/* Combine: y[t] = shared(x_t) + sum over slots j of the pairs' shares left
+/* Passage: the `unpermute_combine` piece of kernel_gmm_gpu.json; the shared
+ * expert is the `shared: 1024` field of gpu_moe_h100.json; the value
+ * sum(y * upstream) is the train step's value of the value_and_grad
+ * description of gpu_moe_h100.json.
+ * Combine: y[t] = shared(x_t) + sum over slots j of the pairs' shares left
  * by moe_grouped_ffn_fwd, summed in slot order and cast to dtype, where
  * shared(x) = (silu(x Ws_gate) * (x Ws_up)) Ws_down when hs > 0 (its
  * weights are ignored and may be NULL when hs == 0).
@@ -166,13 +180,19 @@ moe_status moe_grouped_ffn_fwd(const moe_dims* dims, int mode, const void* x,
  *                          pre-activations in MOE_SAVE_FOR_BWD, else NULL
  *   upstream [T, d] (dtype), nullable; when given, *loss (f32, device)
  *   receives sum(y * upstream), the train step's value, reduced in a fixed
- *   order.  The result is bit-identical from run to run. */
+ *   order.  The result is bit-identical from run to run.
+ * With MOE_SHARED_READY OR-ed into `mode`, the shared expert's output is
+ * taken from the workspace, where moe_shared_ffn_fwd left it (the caller
+ * orders that call before this one); x, the shared weights and its buffers
+ * are then ignored. */
 moe_status moe_combine(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
                        const void* ws_up, const void* ws_down, void* y, void* hs_buf,
                        void* as_gate_saved, void* as_up_saved, const void* upstream, float* loss,
                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Backward of the train step for L = sum(y * dy):
+/* Passage: the value_and_grad description of gpu_moe_h100.json (gradients
+ * with respect to the input and every parameter).
+ * Backward of the train step for L = sum(y * dy):
  *   inputs : dy [T, d], x, all weights, topk_idx, gates, and what a
  *            MOE_SAVE_FOR_BWD forward that used the same workspace left:
  *            its pre-activations a_gate_saved / a_up_saved [padded_rows, h]
@@ -197,6 +217,53 @@ moe_status moe_backward(const moe_dims* dims, const void* dy, const void* x,
                         float* dw_up, float* dw_down, float* dws_gate, float* dws_up,
                         float* dws_down, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
+
+/* The shared expert on its own, so that it can run on another stream beside
+ * the routed experts (the two share no buffer):
+ *
+ * moe_shared_ffn_fwd: the shared expert's forward (the `shared` field of
+ * gpu_moe_h100.json): its output rows go to the workspace for a following
+ * moe_combine(mode | MOE_SHARED_READY); hs_buf / as_gate_saved /
+ * as_up_saved as in moe_combine.  Nothing to do (MOE_OK) when hs == 0.
+ *
+ * moe_shared_backward: the shared expert's share of the value_and_grad
+ * backward (gpu_moe_h100.json): dws_gate / dws_up [d, hs], dws_down [hs, d]
+ * (f32, overwritten) and its rows of dx, which it leaves in the workspace
+ * for moe_backward_routed.  Reads what the forward on this workspace saved.
+ *
+ * moe_backward_routed: moe_backward without the shared expert: the routed
+ * experts' and the router's gradients, and dx, which adds the shared
+ * expert's rows when hs > 0.  shared_done (nullable) is an event recorded
+ * after moe_shared_backward was enqueued (on any stream): the kernel that
+ * forms dx waits for it; with NULL the caller orders the two calls itself
+ * (e.g. both on one stream, the shared one first). */
+moe_status moe_shared_ffn_fwd(const moe_dims* dims, int mode, const void* x, const void* ws_gate,
+                              const void* ws_up, const void* ws_down, void* hs_buf,
+                              void* as_gate_saved, void* as_up_saved, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+moe_status moe_shared_backward(const moe_dims* dims, const void* dy, const void* x,
+                               const void* ws_gate, const void* ws_up, const void* ws_down,
+                               const void* as_gate_saved, const void* as_up_saved,
+                               const void* hs_saved, float* dws_gate, float* dws_up,
+                               float* dws_down, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
+moe_status moe_backward_routed(const moe_dims* dims, const void* dy, const void* x,
+                               const void* w_router, const void* w_gate, const void* w_up,
+                               const void* w_down, const int32_t* topk_idx, const float* gates,
+                               const void* a_gate_saved, const void* a_up_saved,
+                               const void* h_saved, void* dx, float* dw_router, float* dw_gate,
+                               float* dw_up, float* dw_down, cudaEvent_t shared_done,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Caps the number of SMs that the persistent kernels launched afterwards
+ * by the calling host thread may occupy (0: every SM).  With the shared
+ * expert on a second stream, the two streams' kernels then run side by side
+ * on disjoint shares of the GPU instead of one waiting for the other.  The
+ * results do not depend on the cap (work schedules that fix a summation
+ * order are sized for the whole device).  A launch recorded into a CUDA
+ * graph keeps the cap it was recorded under.  Not a device setting: it
+ * only sizes this thread's grids. */
+moe_status moe_set_sm_limit(int sms);
 
 /* Synchronises `stream`, then returns the device-side status recorded in
  * the workspace since the last moe_permute (MOE_OK, MOE_ERR_TIMEOUT or

@@ -268,3 +268,51 @@ def test_captured_train_step_replays_the_eager_results():
         for k, v in ref[2].items():
             assert torch.equal(layer.grads[k], v), k
     assert float(lh[0]) == float(ref[0][0])
+
+
+# The shared expert on a side stream beside the routed experts (SM-capped
+# persistent kernels on both streams): the same results, bit for bit, as the
+# serial composition, in the train step, the forward pass and a CUDA-graph
+# replay of the train step.
+OVERLAP = [
+    MoEConfig(2050, 256, 128, 64, 8, 256, "bf16", "overlap_decoder_small"),
+    MoEConfig(1100, 512, 1024, 4, 2, 1024, "bf16", "overlap_pairs_shared"),
+    MoEConfig(300, 64, 64, 5, 5, 64, "f32", "overlap_f32"),
+]
+
+
+@pytest.mark.parametrize("cfg", OVERLAP, ids=[c.name for c in OVERLAP])
+def test_shared_expert_side_stream_matches_serial(cfg):
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, cfg.dtype)
+    p = {k: dev[k] for k in params_of(inp)}
+    outs = []
+    for shared_sms in (0, 40):
+        layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                         cfg.shared_hidden, cfg.dtype, train=True, shared_sms=shared_sms)
+        loss, dx, g = layer.train_step(dev["x"], p, dev["upstream"])
+        torch.cuda.synchronize()
+        assert layer.device_status()[0] == 0
+        res = {"loss": loss.clone(), "dx": dx.clone(), "y": layer.y.clone()}
+        res.update({k: v.clone() for k, v in g.items() if v is not None})
+        fwd = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                       cfg.shared_hidden, cfg.dtype, train=False, shared_sms=shared_sms)
+        res["y_fwd"] = fwd.forward(dev["x"], p).clone()
+        if shared_sms:
+            replay = layer.capture(lambda: layer.train_step(dev["x"], p, dev["upstream"]))
+            layer.dx.zero_()
+            for v in layer.grads.values():
+                if v is not None:
+                    v.zero_()
+            replay()
+            torch.cuda.synchronize()
+            res["dx_graph"] = layer.dx.clone()
+            res["dws_down_graph"] = layer.grads["dws_down"].clone()
+        outs.append(res)
+    serial, over = outs
+    for k, v in serial.items():
+        assert torch.equal(v, over[k]), k
+    assert torch.equal(serial["dx"], over["dx_graph"])
+    assert torch.equal(serial["dws_down"], over["dws_down_graph"])
+    assert torch.equal(serial["y"], serial["y_fwd"])
