@@ -343,6 +343,7 @@ moe_status backward_parts(int parts, const moe_dims* dims, const void* dy, const
     dg_n = (int)(2 * h / tc_dz_bn((int)h));
   } else {
     simt_backward_routed(*dims, L, p, workspace, stream);
+    dg_n = simt_dz_tiles((int)h);
   }
   launch_router_backward(*dims, L, p, dg_n, dg_ld, workspace, stream, shared_done);
   return cuda_status();

@@ -24,7 +24,11 @@ namespace {
 
 enum Kind { LOGITS, GU, DOWN, DZ, DX, DWD, DWGU };
 
-constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
+constexpr int BK = 16, NT = 256;
+
+// The tile edge of a GEMM whose output has N columns and (weight
+// gradients) M rows: 128 where both divide, else 64.
+inline int tile_of(int64_t N, int64_t M = 128) { return N % 128 == 0 && M % 128 == 0 ? 128 : 64; }
 
 struct SimtArgs {
   // operands
@@ -60,6 +64,7 @@ struct SimtArgs {
   float* acc_out2 = nullptr;     // DWGU (up half)
   int ldo = 0;
   int n_ntiles = 1, n_mtiles = 1;
+  int tm = 64;                   // tile edge: 64, or 128 where the dimensions divide
 };
 
 template <typename T>
@@ -85,23 +90,32 @@ __device__ __forceinline__ float comp(const float4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-template <Kind KIND, typename T, bool ROUTED>
+// TM x TM output tiles (TM = 64 or 128), 256 threads as 16 x 16, each
+// thread an R x R micro-tile (R = TM / 16: 4 or 8) made of (R / 4)^2 blocks
+// of 4 x 4 elements 64 rows / columns apart (its rows ty*4 + i + 64*u, its
+// columns tx*4 + j + 64*v), so that every shared-memory operand read is a
+// conflict-free float4 and the 16 threads of a row are 16 consecutive lanes.
+// The 8 x 8 micro-tile issues 64 FFMAs per 4 float4 loads of each k step,
+// the 4 x 4 one 16 per 2.
+template <Kind KIND, typename T, bool ROUTED, int TM>
 __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   constexpr bool A_KCONTIG = (KIND == LOGITS || KIND == GU || KIND == DOWN || KIND == DZ ||
                               KIND == DX);
   constexpr bool B_KCONTIG = (KIND == DZ || KIND == DX);
   constexpr bool DUAL = (KIND == GU);
   constexpr bool DW = (KIND == DWD || KIND == DWGU);
+  constexpr int R = TM / 16;   // micro-tile edge
+  constexpr int U = TM / 64;   // 4 x 4 blocks per micro-tile edge; loads per thread per operand
 
-  __shared__ __align__(16) float As[BK][BM + 4];
-  __shared__ __align__(16) float Bs[BK][BN + 4];
-  __shared__ __align__(16) float Bs2[DUAL ? BK : 1][BN + 4];
-  __shared__ int s_tok[BM];  // source rows of the tile (row kinds)
+  __shared__ __align__(16) float As[BK][TM + 4];
+  __shared__ __align__(16) float Bs[BK][TM + 4];
+  __shared__ __align__(16) float Bs2[DUAL ? BK : 1][DUAL ? TM + 4 : 4];
+  __shared__ int s_tok[TM];  // source rows of the tile (row kinds)
 
   const int tid = threadIdx.x;
   const int ntile = blockIdx.x % a.n_ntiles;
   const int rest = blockIdx.x / a.n_ntiles;
-  const int n0 = ntile * BN;
+  const int n0 = ntile * TM;
 
   int e = 0;
   int64_t row0 = 0;     // first output row (row kinds) / first K row (DW kinds)
@@ -111,19 +125,21 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 
   if constexpr (!DW) {
     if constexpr (ROUTED) {
-      const int mt = rest >> 1, half = rest & 1;
+      // tile-list entries hold 128 rows: one block (TM = 128) or two halves
+      constexpr int PER = 128 / TM;
+      const int mt = rest / PER, part = rest % PER;
       if (mt >= a.ntiles[0]) return;
       const int4 tile = a.tiles[mt];
       e = tile.x;
-      row0 = tile.y + half * BM;
-      nvalid = min(BM, tile.z - half * BM);
+      row0 = tile.y + part * TM;
+      nvalid = min(TM, tile.z - part * TM);
       if (nvalid <= 0) return;
     } else {
-      row0 = (int64_t)rest * BM;
+      row0 = (int64_t)rest * TM;
       if (row0 >= a.rows) return;
-      nvalid = a.rows - row0 < BM ? (int)(a.rows - row0) : BM;
+      nvalid = a.rows - row0 < TM ? (int)(a.rows - row0) : TM;
     }
-    for (int i = tid; i < BM; i += NT) {
+    for (int i = tid; i < TM; i += NT) {
       int64_t src = row0 + i;
       if constexpr (ROUTED) {
         if (KIND == GU || KIND == DZ) {
@@ -138,7 +154,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   } else {
     const int mt = rest % a.n_mtiles;
     e = rest / a.n_mtiles;
-    m0 = mt * BM;
+    m0 = mt * TM;
     if constexpr (ROUTED) {
       kbeg = a.poff[e];
       kend = kbeg + a.counts[e];
@@ -153,80 +169,82 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   const T* B = reinterpret_cast<const T*>(a.B) + (ROUTED ? a.b_estride * e : 0);
   const T* B2 = a.B2 ? reinterpret_cast<const T*>(a.B2) + (ROUTED ? a.b_estride * e : 0) : nullptr;
 
-  float acc[4][4] = {};
-  float acc2[DUAL ? 4 : 1][DUAL ? 4 : 1] = {};
+  float acc[R][R] = {};
+  float acc2[DUAL ? R : 1][DUAL ? R : 1] = {};
   const int ty = tid / 16, tx = tid % 16;
 
-  float4 ra, rb, rb2;
+  float4 ra[U], rb[U], rb2[DUAL ? U : 1];
   auto gload = [&](int64_t kt) {
-    // ---- A ----
-    if constexpr (A_KCONTIG) {
-      const int m = tid / 4, k4 = (tid % 4) * 4;
-      const bool ok = m < nvalid || (KIND == DOWN || KIND == DX);
-      const int64_t src = (KIND == LOGITS || !ROUTED) ? row0 + m : (int64_t)s_tok[m];
-      const bool in = ok && (ROUTED || row0 + m < a.rows);
-      if constexpr (KIND == LOGITS) {
-        ra = load4(A + src * a.lda + kt + k4, in);
-      } else {
-        ra = load4(A + src * a.lda + kt + k4, in);
-      }
-    } else {
-      const int kl = tid / 16, m4 = (tid % 16) * 4;
-      const int64_t r = kbeg + kt + kl;
-      const bool ok = r < kend;
-      int64_t src = r;
-      if (KIND == DWGU && ROUTED && ok) src = a.rowpair[r] / a.top_k;
-      ra = load4(A + src * a.lda + m0 + m4, ok);
-    }
-    // ---- B ----
-    if constexpr (!B_KCONTIG) {
-      const int kl = tid / 16, n4 = (tid % 16) * 4;
-      if constexpr (KIND == LOGITS) {
-        const int64_t kk = kt + kl;
-        float v[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = load1(B + kk * a.ldb + n0 + n4 + q, n0 + n4 + q < a.N);
-        rb = make_float4(v[0], v[1], v[2], v[3]);
-      } else if constexpr (DW) {
+    for (int u = 0; u < U; ++u) {
+      // ---- A ----
+      if constexpr (A_KCONTIG) {
+        const int m = tid / 4 + 64 * u, k4 = (tid % 4) * 4;
+        const bool ok = m < nvalid || (KIND == DOWN || KIND == DX);
+        const int64_t src = (KIND == LOGITS || !ROUTED) ? row0 + m : (int64_t)s_tok[m];
+        const bool in = ok && (ROUTED || row0 + m < a.rows);
+        ra[u] = load4(A + src * a.lda + kt + k4, in);
+      } else {
+        const int kl = tid / 16, m4 = (tid % 16) * 4 + 64 * u;
         const int64_t r = kbeg + kt + kl;
         const bool ok = r < kend;
         int64_t src = r;
-        if (KIND == DWD && ROUTED && ok) src = a.rowpair[r] / a.top_k;
-        rb = load4(B + src * a.ldb + n0 + n4, ok);
-      } else {
-        const int64_t kk = kt + kl;
-        rb = load4(B + kk * a.ldb + n0 + n4, true);
-        if constexpr (DUAL) rb2 = load4(B2 + kk * a.ldb + n0 + n4, true);
+        if (KIND == DWGU && ROUTED && ok) src = a.rowpair[r] / a.top_k;
+        ra[u] = load4(A + src * a.lda + m0 + m4, ok);
       }
-    } else {
-      const int n = tid / 4, k4 = (tid % 4) * 4;
-      const int64_t kk = kt + k4;
-      if constexpr (KIND == DX) {
-        const T* src = kk < a.h ? B + (int64_t)(n0 + n) * a.ldb + kk
-                                : B2 + (int64_t)(n0 + n) * a.ldb + (kk - a.h);
-        rb = load4(src, true);
+      // ---- B ----
+      if constexpr (!B_KCONTIG) {
+        const int kl = tid / 16, n4 = (tid % 16) * 4 + 64 * u;
+        if constexpr (KIND == LOGITS) {
+          const int64_t kk = kt + kl;
+          float v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) v[q] = load1(B + kk * a.ldb + n0 + n4 + q, n0 + n4 + q < a.N);
+          rb[u] = make_float4(v[0], v[1], v[2], v[3]);
+        } else if constexpr (DW) {
+          const int64_t r = kbeg + kt + kl;
+          const bool ok = r < kend;
+          int64_t src = r;
+          if (KIND == DWD && ROUTED && ok) src = a.rowpair[r] / a.top_k;
+          rb[u] = load4(B + src * a.ldb + n0 + n4, ok);
+        } else {
+          const int64_t kk = kt + kl;
+          rb[u] = load4(B + kk * a.ldb + n0 + n4, true);
+          if constexpr (DUAL) rb2[u] = load4(B2 + kk * a.ldb + n0 + n4, true);
+        }
       } else {
-        rb = load4(B + (int64_t)(n0 + n) * a.ldb + kk, true);
+        const int n = tid / 4 + 64 * u, k4 = (tid % 4) * 4;
+        const int64_t kk = kt + k4;
+        if constexpr (KIND == DX) {
+          const T* src = kk < a.h ? B + (int64_t)(n0 + n) * a.ldb + kk
+                                  : B2 + (int64_t)(n0 + n) * a.ldb + (kk - a.h);
+          rb[u] = load4(src, true);
+        } else {
+          rb[u] = load4(B + (int64_t)(n0 + n) * a.ldb + kk, true);
+        }
       }
     }
   };
   auto sstore = [&]() {
-    if constexpr (A_KCONTIG) {
-      const int m = tid / 4, k4 = (tid % 4) * 4;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) As[k4 + q][m] = comp(ra, q);
-    } else {
-      const int kl = tid / 16, m4 = (tid % 16) * 4;
-      *reinterpret_cast<float4*>(&As[kl][m4]) = ra;
-    }
-    if constexpr (!B_KCONTIG) {
-      const int kl = tid / 16, n4 = (tid % 16) * 4;
-      *reinterpret_cast<float4*>(&Bs[kl][n4]) = rb;
-      if constexpr (DUAL) *reinterpret_cast<float4*>(&Bs2[kl][n4]) = rb2;
-    } else {
-      const int n = tid / 4, k4 = (tid % 4) * 4;
+    for (int u = 0; u < U; ++u) {
+      if constexpr (A_KCONTIG) {
+        const int m = tid / 4 + 64 * u, k4 = (tid % 4) * 4;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) Bs[k4 + q][n] = comp(rb, q);
+        for (int q = 0; q < 4; ++q) As[k4 + q][m] = comp(ra[u], q);
+      } else {
+        const int kl = tid / 16, m4 = (tid % 16) * 4 + 64 * u;
+        *reinterpret_cast<float4*>(&As[kl][m4]) = ra[u];
+      }
+      if constexpr (!B_KCONTIG) {
+        const int kl = tid / 16, n4 = (tid % 16) * 4 + 64 * u;
+        *reinterpret_cast<float4*>(&Bs[kl][n4]) = rb[u];
+        if constexpr (DUAL) *reinterpret_cast<float4*>(&Bs2[kl][n4]) = rb2[u];
+      } else {
+        const int n = tid / 4 + 64 * u, k4 = (tid % 4) * 4;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Bs[k4 + q][n] = comp(rb[u], q);
+      }
     }
   };
 
@@ -239,35 +257,43 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
     if (kt + BK < klen) gload(kt + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
-      const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
-      const float am[4] = {av.x, av.y, av.z, av.w};
-      const float bn[4] = {bv.x, bv.y, bv.z, bv.w};
+      float am[R], bn[R], bn2[DUAL ? R : 1];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int u = 0; u < U; ++u) {
+        const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4 + 64 * u]);
+        const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4 + 64 * u]);
+        am[4 * u] = av.x; am[4 * u + 1] = av.y; am[4 * u + 2] = av.z; am[4 * u + 3] = av.w;
+        bn[4 * u] = bv.x; bn[4 * u + 1] = bv.y; bn[4 * u + 2] = bv.z; bn[4 * u + 3] = bv.w;
+        if constexpr (DUAL) {
+          const float4 b2 = *reinterpret_cast<const float4*>(&Bs2[kk][tx * 4 + 64 * u]);
+          bn2[4 * u] = b2.x; bn2[4 * u + 1] = b2.y; bn2[4 * u + 2] = b2.z; bn2[4 * u + 3] = b2.w;
+        }
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(am[i], bn[j], acc[i][j]);
+      for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < R; ++j) acc[i][j] = fmaf(am[i], bn[j], acc[i][j]);
       if constexpr (DUAL) {
-        const float4 b2 = *reinterpret_cast<const float4*>(&Bs2[kk][tx * 4]);
-        const float bn2[4] = {b2.x, b2.y, b2.z, b2.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < R; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc2[i][j] = fmaf(am[i], bn2[j], acc2[i][j]);
+          for (int j = 0; j < R; ++j) acc2[i][j] = fmaf(am[i], bn2[j], acc2[i][j]);
       }
     }
   }
 
   // ---------------- epilogues ----------------
+  // micro-tile element (i, j): row ty*4 + (i % 4) + 64*(i / 4), column
+  // tx*4 + (j % 4) + 64*(j / 4) of the tile
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = ty * 4 + i;
+  for (int i = 0; i < R; ++i) {
+    const int m = ty * 4 + (i & 3) + 64 * (i >> 2);
     const int64_t r = row0 + m;
     if constexpr (KIND == LOGITS) {
       if (r < a.rows)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int n = n0 + tx * 4 + j;
+        for (int j = 0; j < R; ++j) {
+          const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
           if (n < a.N) a.acc_out[r * a.ldo + n] = acc[i][j] + (a.col_bias ? a.col_bias[n] : 0.f);
         }
     } else if constexpr (KIND == GU) {
@@ -276,8 +302,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       T* AG = reinterpret_cast<T*>(a.ag_out);
       T* AU = reinterpret_cast<T*>(a.au_out);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = n0 + tx * 4 + j;
+      for (int j = 0; j < R; ++j) {
+        const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
         // round to the storage type first, so H is computed from exactly the
         // values a backward pass reads back
         const float g = to_f32(from_f32<T>(acc[i][j]));
@@ -297,7 +323,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       if constexpr (ROUTED && KIND == DOWN) sc = a.gates[a.rowpair[r]];
       T* out = reinterpret_cast<T*>(a.slot_out);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) out[r * a.ldo + n0 + tx * 4 + j] = from_f32<T>(sc * acc[i][j]);
+      for (int j = 0; j < R; ++j)
+        out[r * a.ldo + n0 + tx * 4 + (j & 3) + 64 * (j >> 2)] = from_f32<T>(sc * acc[i][j]);
     } else if constexpr (KIND == DZ) {
       const bool exists = ROUTED || r < a.rows;
       const bool valid = m < nvalid;
@@ -310,8 +337,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       const int64_t h = a.h;
       float dgp = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = n0 + tx * 4 + j;
+      for (int j = 0; j < R; ++j) {
+        const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
         const float z = acc[i][j];
         const float ag = valid ? to_f32(AG[r * h + n]) : 0.f;
         const float au = valid ? to_f32(AU[r * h + n]) : 0.f;
@@ -335,10 +362,10 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
         a.dg_part[(int64_t)a.rowpair[r] * a.dg_ld + ntile] = gt * dgp;
     } else {  // DWD / DWGU: plain stores of the expert's gradient tile
       const int64_t om = m0 + m;
-      const int64_t eoff = (int64_t)e * a.n_mtiles * BM;  // expert offset in rows
+      const int64_t eoff = (int64_t)e * a.n_mtiles * TM;  // expert offset in rows
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int n = n0 + tx * 4 + j;
+      for (int j = 0; j < R; ++j) {
+        const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
         if constexpr (KIND == DWGU) {
           if (n < a.h)
             a.acc_out[(eoff + om) * a.h + n] = acc[i][j];
@@ -352,6 +379,9 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   }
 }
 
+// `blocks` counts 64 x 64 tiles; with a.tm = 128 each block takes a
+// 128 x 128 tile (a quarter as many blocks; the routed row kinds, whose tile
+// list holds 128-row entries, half as many per column tile)
 template <Kind KIND, typename T, bool ROUTED>
 void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
   if (blocks <= 0) return;
@@ -360,7 +390,12 @@ void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
        "simt_dw_down_sh", "simt_dw_gateup_sh"},
       {"simt_logits", "simt_gateup", "simt_down", "simt_dz", "simt_dx", "simt_dw_down",
        "simt_dw_gateup"}};
-  MOE_LAUNCH(names[ROUTED ? 1 : 0][KIND], s, simt_gemm_kernel<KIND, T, ROUTED><<<(unsigned)blocks, NT, 0, s>>>(a));
+  if (a.tm == 128)
+    MOE_LAUNCH(names[ROUTED ? 1 : 0][KIND], s,
+               simt_gemm_kernel<KIND, T, ROUTED, 128><<<(unsigned)blocks, NT, 0, s>>>(a));
+  else
+    MOE_LAUNCH(names[ROUTED ? 1 : 0][KIND], s,
+               simt_gemm_kernel<KIND, T, ROUTED, 64><<<(unsigned)blocks, NT, 0, s>>>(a));
 }
 
 template <typename T>
@@ -376,8 +411,8 @@ void router_logits_t(const moe_dims& d, const LayerPtrs& p, float* logits, cudaS
   a.acc_out = logits;
   a.col_bias = p.router_bias;
   a.ldo = d.experts;
-  a.n_ntiles = (d.experts + BN - 1) / BN;
-  launch<LOGITS, T, false>(a, a.n_ntiles * ((d.tokens + BM - 1) / BM), s);
+  a.n_ntiles = (d.experts + 63) / 64;
+  launch<LOGITS, T, false>(a, a.n_ntiles * ((d.tokens + 63) / 64), s);
 }
 
 template <typename T>
@@ -403,8 +438,9 @@ void grouped_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs
   a.ag_out = mode == MOE_SAVE_FOR_BWD ? p.a_gate : nullptr;
   a.au_out = mode == MOE_SAVE_FOR_BWD ? p.a_up : nullptr;
   a.ldo = h;
-  a.n_ntiles = h / BN;
-  launch<GU, T, true>(a, a.n_ntiles * 2 * L.MTcap, s);
+  a.tm = tile_of(h);
+  a.n_ntiles = h / a.tm;
+  launch<GU, T, true>(a, a.n_ntiles * (128 / a.tm) * L.MTcap, s);
   // down projection with the gate-weighted combine
   SimtArgs b = a;
   b.A = p.h_buf;
@@ -417,15 +453,15 @@ void grouped_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs
   b.K = h;
   b.slot_out = at<void>(ws, L.osort);
   b.ldo = dm;
-  b.n_ntiles = dm / BN;
-  launch<DOWN, T, true>(b, b.n_ntiles * 2 * L.MTcap, s);
+  b.tm = tile_of(dm);
+  b.n_ntiles = dm / b.tm;
+  launch<DOWN, T, true>(b, b.n_ntiles * (128 / b.tm) * L.MTcap, s);
 }
 
 template <typename T>
 void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                   cudaStream_t s) {
   const int hs = d.shared_hidden, dm = d.d_model;
-  const int64_t mt = (d.tokens + BM - 1) / BM;
   SimtArgs a;
   a.rows = d.tokens;
   a.A = p.x;
@@ -439,8 +475,9 @@ void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs&
   a.ag_out = mode == MOE_SAVE_FOR_BWD ? p.as_gate : nullptr;
   a.au_out = mode == MOE_SAVE_FOR_BWD ? p.as_up : nullptr;
   a.ldo = hs;
-  a.n_ntiles = hs / BN;
-  launch<GU, T, false>(a, a.n_ntiles * mt, s);
+  a.tm = tile_of(hs);
+  a.n_ntiles = hs / a.tm;
+  launch<GU, T, false>(a, a.n_ntiles * ((d.tokens + a.tm - 1) / a.tm), s);
   SimtArgs b = a;
   b.A = p.hs_buf;
   b.lda = hs;
@@ -451,8 +488,9 @@ void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs&
   b.K = hs;
   b.slot_out = at<void>(ws, L.ys);
   b.ldo = dm;
-  b.n_ntiles = dm / BN;
-  launch<DOWN, T, false>(b, b.n_ntiles * mt, s);
+  b.tm = tile_of(dm);
+  b.n_ntiles = dm / b.tm;
+  launch<DOWN, T, false>(b, b.n_ntiles * ((d.tokens + b.tm - 1) / b.tm), s);
 }
 
 // the shared expert's backward (dxs and its weight gradients)
@@ -460,7 +498,7 @@ template <typename T>
 void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                        cudaStream_t s) {
   const int dm = d.d_model, hs = d.shared_hidden;
-  const int64_t mt_dense = (d.tokens + BM - 1) / BM;
+  auto row_tiles = [&](int tm) { return (d.tokens + tm - 1) / tm; };
   if (hs > 0) {
     void* dAs = at<void>(ws, L.dAs);
     void* gHs = at<void>(ws, L.gHs);
@@ -478,8 +516,9 @@ void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
     z.au_in = p.as_up;
     z.dA_out = dAs;
     z.gH_out = gHs;
-    z.n_ntiles = hs / BN;
-    launch<DZ, T, false>(z, z.n_ntiles * mt_dense, s);
+    z.tm = tile_of(hs);
+    z.n_ntiles = hs / z.tm;
+    launch<DZ, T, false>(z, z.n_ntiles * row_tiles(z.tm), s);
     // dx_acc = dAs [Ws_gate | Ws_up]^T   (plain store: first writer)
     SimtArgs x;
     x.rows = d.tokens;
@@ -493,8 +532,9 @@ void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
     x.h = hs;
     x.slot_out = at<void>(ws, L.dxs);
     x.ldo = dm;
-    x.n_ntiles = dm / BN;
-    launch<DX, T, false>(x, x.n_ntiles * mt_dense, s);
+    x.tm = tile_of(dm);
+    x.n_ntiles = dm / x.tm;
+    launch<DX, T, false>(x, x.n_ntiles * row_tiles(x.tm), s);
     // dWs_down = Hs^T dy ; dWs_gate | dWs_up = x^T dAs
     SimtArgs w;
     w.rows = d.tokens;
@@ -504,8 +544,9 @@ void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
     w.ldb = dm;
     w.acc_out = p.dws_down;
     w.ldo = dm;
-    w.n_mtiles = hs / BM;
-    w.n_ntiles = dm / BN;
+    w.tm = tile_of(dm, hs);
+    w.n_mtiles = hs / w.tm;
+    w.n_ntiles = dm / w.tm;
     launch<DWD, T, false>(w, (int64_t)w.n_ntiles * w.n_mtiles, s);
     SimtArgs g;
     g.rows = d.tokens;
@@ -516,8 +557,9 @@ void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
     g.h = hs;
     g.acc_out = p.dws_gate;
     g.acc_out2 = p.dws_up;
-    g.n_mtiles = dm / BM;
-    g.n_ntiles = 2 * hs / BN;
+    g.tm = tile_of(2 * hs, dm);
+    g.n_mtiles = dm / g.tm;
+    g.n_ntiles = 2 * hs / g.tm;
     launch<DWGU, T, false>(g, (int64_t)g.n_ntiles * g.n_mtiles, s);
   }
 }
@@ -552,8 +594,9 @@ void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
   z.gH_out = gH;
   z.dg_part = at<float>(ws, L.dg_part);
   z.dg_ld = 2 * h / 64;  // per-pair stride of the gate-gradient partials
-  z.n_ntiles = h / BN;
-  launch<DZ, T, true>(z, z.n_ntiles * 2 * L.MTcap, s);
+  z.tm = tile_of(h);     // (one partial per column tile: simt_dz_tiles(h) of them)
+  z.n_ntiles = h / z.tm;
+  launch<DZ, T, true>(z, z.n_ntiles * (128 / z.tm) * L.MTcap, s);
 
   SimtArgs x = base;
   x.A = dA;
@@ -567,8 +610,9 @@ void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
   x.h = h;
   x.slot_out = at<void>(ws, L.dxsort);
   x.ldo = dm;
-  x.n_ntiles = dm / BN;
-  launch<DX, T, true>(x, x.n_ntiles * 2 * L.MTcap, s);
+  x.tm = tile_of(dm);
+  x.n_ntiles = dm / x.tm;
+  launch<DX, T, true>(x, x.n_ntiles * (128 / x.tm) * L.MTcap, s);
 
   SimtArgs w = base;
   w.A = gH;
@@ -577,8 +621,9 @@ void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
   w.ldb = dm;
   w.acc_out = p.dw_down;
   w.ldo = dm;
-  w.n_mtiles = h / BM;
-  w.n_ntiles = dm / BN;
+  w.tm = tile_of(dm, h);
+  w.n_mtiles = h / w.tm;
+  w.n_ntiles = dm / w.tm;
   launch<DWD, T, true>(w, (int64_t)w.n_ntiles * w.n_mtiles * E, s);
 
   SimtArgs g = base;
@@ -589,12 +634,15 @@ void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
   g.h = h;
   g.acc_out = p.dw_gate;
   g.acc_out2 = p.dw_up;
-  g.n_mtiles = dm / BM;
-  g.n_ntiles = 2 * h / BN;
+  g.tm = tile_of(2 * h, dm);
+  g.n_mtiles = dm / g.tm;
+  g.n_ntiles = 2 * h / g.tm;
   launch<DWGU, T, true>(g, (int64_t)g.n_ntiles * g.n_mtiles * E, s);
 }
 
 }  // namespace
+
+int simt_dz_tiles(int h) { return h / tile_of(h); }
 
 void simt_router_logits(const moe_dims& d, const LayerPtrs& p, float* logits, cudaStream_t s) {
   if (d.dtype == MOE_BF16) router_logits_t<__nv_bfloat16>(d, p, logits, s);

@@ -76,6 +76,7 @@ struct LayerPtrs {
 
 // grouped expert GEMMs (gemm_simt.cu: float32 storage)
 void simt_router_logits(const moe_dims& d, const LayerPtrs& p, float* logits, cudaStream_t s);
+int simt_dz_tiles(int h);  // column tiles of the float32 dZ GEMM (its gate-gradient partials per row)
 void simt_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                       cudaStream_t s);
 void simt_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
