@@ -38,7 +38,9 @@ namespace moe {
 namespace tcg {
 
 enum AKind { A_K_TMA = 0, A_MN_TMA = 2 };   // A tile K-major (rows x 64 K) or MN-major
-enum BKind { B_MN_TMA = 0, B_K_TMA = 1 };   // B tile MN-major (64 K rows x BN) or K-major
+// B tile MN-major (64 K rows x BN) or K-major; B_MN_RES: MN-major, every K
+// block loaded once per CTA and kept resident (the router's W_r)
+enum BKind { B_MN_TMA = 0, B_K_TMA = 1, B_MN_RES = 2 };
 enum EKind { E_GU = 0, E_DOWN = 1, E_DZ = 2, E_DX = 3, E_DW = 4, E_ROUTER = 5 };
 
 constexpr int kEpiWarps = 8;
@@ -112,7 +114,10 @@ struct Cfg {
   static constexpr int BM = 128, BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // a resident B (B_MN_RES) holds up to BRES_KB K blocks (K <= 64 * BRES_KB)
+  static constexpr bool BRES = BKIND == B_MN_RES;
+  static constexpr int BRES_KB = 10;
+  static constexpr int STAGE_BYTES = BRES ? A_BYTES : A_BYTES + B_BYTES;
   // per-warp staging: 2 KB per bf16 32x32 tile
   // (gate/up: two tiles, a_u reuses H's slot, which leaves room for a
   // fourth operand stage)
@@ -121,13 +126,14 @@ struct Cfg {
                                    : (EK == E_DOWN || EK == E_DX) ? 2048 : 0;
   // routed DW kinds keep their chunk schedule (E + 1 ints) after the barriers
   static constexpr int SCHED_BYTES = (DW && ROUTED) ? 4 * (kMaxExperts + 1) + 16 : 0;
-  static constexpr int FIXED = kEpiWarps * EPI_BYTES + 1024 + 256 + SCHED_BYTES;
+  static constexpr int FIXED = kEpiWarps * EPI_BYTES + 1024 + 256 + SCHED_BYTES +
+                               (BRES ? BRES_KB * B_BYTES : 0);
   static constexpr int STAGES = (kSmemLimit - FIXED) / STAGE_BYTES > 8
                                     ? 8
                                     : (kSmemLimit - FIXED) / STAGE_BYTES;
 
   static constexpr bool A_MN = AK == A_MN_TMA;
-  static constexpr bool B_MN = BKIND == B_MN_TMA;
+  static constexpr bool B_MN = BKIND != B_K_TMA;
   static constexpr uint32_t IDESC = tc::idesc_bf16(PAIR ? 2 * BM : BM, BN, A_MN, B_MN);
   static constexpr uint32_t TMEM_COLS = 2 * BN;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + FIXED;
@@ -135,6 +141,7 @@ struct Cfg {
   static_assert(!DUALN || BN >= 128, "the gate/up tile holds 64-column halves");
   static_assert(STAGES >= 2, "shared memory");
   static_assert(!PAIR || (EK != E_ROUTER && BN >= 128), "pairs: BN >= 128, no router");
+  static_assert(!BRES || (!PAIR && !DW && !DUALN), "resident B: single-CTA row kinds");
 };
 
 struct Tile {
@@ -275,6 +282,7 @@ struct Shared {
   uint64_t tempty[2];
   uint64_t ebar[kEpiWarps];  // per epilogue warp: its staged input tiles
   uint64_t epi_bar;          // the epilogue warps' own barrier (routed DW chunk fix-up)
+  uint64_t bres;             // resident B (B_MN_RES) has landed
   uint32_t tmem_base;
   volatile int abort;
   volatile int fixup;        // routed DW: this CTA finishes the tile's chunk sum
@@ -472,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* epi = smem + C::STAGES * C::STAGE_BYTES;
+  uint8_t* sBres = smem + C::STAGES * C::STAGE_BYTES;  // resident B (B_MN_RES)
+  uint8_t* epi = sBres + (C::BRES ? C::BRES_KB * C::B_BYTES : 0);
   Shared* sh = reinterpret_cast<Shared*>(epi + kEpiWarps * C::EPI_BYTES);
   int* choff = reinterpret_cast<int*>(sh + 1);  // routed DW kinds: the chunk schedule
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -496,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int w = 0; w < kEpiWarps; ++w) tc::mbar_init(&sh->ebar[w], 1);
     tc::mbar_init(&sh->epi_bar, kEpiWarps);
+    tc::mbar_init(&sh->bres, 1);
     sh->abort = 0;
     tc::fence_barrier_init();
   }
@@ -537,6 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------ producer ------------------------------
     if (lane == 0) {
+      if constexpr (C::BRES) {  // every K block of B once, before the first tile
+        tc::mbar_arrive_expect_tx(&sh->bres, p.kb_total * C::B_BYTES);
+        for (int kb = 0; kb < p.kb_total; ++kb)
+          tc::tma_load_2d(sBres + kb * C::B_BYTES, &m.b0, &sh->bres, 0, kb * C::BK);
+      }
       int stage = 0;
       uint32_t phase = 0;
       Tile tl;
@@ -573,7 +588,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the even CTA the gate half, the odd CTA the up half)
           constexpr int BNL = C::PAIR ? C::BN / 2 : C::BN;
           const int nb0 = tl.n0 + (C::PAIR && !C::DUALN ? rank * BNL : 0);
-          if constexpr (C::BKIND == B_MN_TMA) {
+          if constexpr (C::BRES) {
+          } else if constexpr (C::BKIND == B_MN_TMA) {
 #pragma unroll
             for (int j = 0; j < BNL / 64; ++j) {
               const CUtensorMap* mp = &m.b0;
@@ -606,6 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------ MMA issuer ------------------------------
     int stage = 0, acc = 0;
     uint32_t phase = 0, aphase = 0;
+    if constexpr (C::BRES) {
+      if (!wait_or_abort(&sh->bres, 0, sh, p.status, 310)) aborted = true;
+    }
     Tile tl;
     for (int t = u0; !aborted && get_tile<C, false>(p, t, nrow_tiles, tl, choff, rank);
          t += us) {
@@ -623,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = tc::smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t b0 = a0 + C::A_BYTES;
+          const uint32_t b0 = C::BRES ? tc::smem_u32(sBres + kb * C::B_BYTES) : a0 + C::A_BYTES;
 #pragma unroll
           for (int s = 0; s < C::BK / 16; ++s) {
             const uint64_t ad = C::A_MN ? tc::sw128_desc(a0 + s * 2048, 8192, 1024)

@@ -149,7 +149,13 @@ bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_
   q.out1 = gates;
   q.facc = logits_out;
   q.gates = bias;  // the router's epilogue reads this as its logit offsets
-  launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_ROUTER, 64, false>>(mp, q, q.n_mt, "tc_router", s);
+  // narrow routers keep W_r resident in shared memory (one operand stream
+  // per stage instead of two; measured faster at E = 8, not at E = 64,
+  // whose epilogue's top-8 selection bounds it)
+  if (d.experts <= 32 && d.d_model <= 64 * 10)
+    launch_tc<Cfg<A_K_TMA, B_MN_RES, E_ROUTER, 64, false>>(mp, q, q.n_mt, "tc_router", s);
+  else
+    launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_ROUTER, 64, false>>(mp, q, q.n_mt, "tc_router", s);
   return true;
 }
 
