@@ -67,6 +67,7 @@ struct Layout {
   size_t xs;       // expert-sorted copy of the token rows [padded rows, d]
   size_t pairrow;  // pair -> padded row [P]
   size_t osort;    // gate-weighted expert output per sorted row [padded rows, d]
+  size_t rowgate;  // the gate of each sorted row's pair, 0 on padding [padded rows] (bf16 path)
   size_t ys;       // shared-expert output [T, d]
   size_t dg_part, dA, dxsort, dxs, dAs, dys, dsel, dwr_part;
   size_t gH, gHs;  // gate * H for the W_down gradients (float32 path only)
@@ -165,6 +166,7 @@ inline Layout make_layout(const moe_dims& d, int mode) {
   L.xs = take((size_t)L.elem * L.PPcap * dm);
   L.pairrow = take(sizeof(int) * L.P);
   L.osort = take((size_t)L.elem * L.PPcap * dm);
+  L.rowgate = take(sizeof(float) * L.PPcap);
   L.ys = take((size_t)L.elem * (hs > 0 ? T : 0) * dm);
   if (mode == MOE_SAVE_FOR_BWD) {
     L.dg_part = take(sizeof(float) * L.P * 2 * (h / 64));

@@ -82,7 +82,7 @@ struct Params {
   int brow_stride = 0;              // rows of a B weight matrix per expert (0: activations)
   int M = 0, N = 0;                 // DW output dims / row-kind output columns
   // epilogue
-  const float* gates = nullptr;     // routed DOWN: pair gates; router: logit offsets [E]
+  const float* gates = nullptr;     // routed DOWN: gate per sorted row; router: logit offsets [E]
   int save = 0;                     // GU: also store a_g, a_u
   void* out0 = nullptr;             // router: top-k indices [T, k]
   void* out1 = nullptr;             // router: gates [T, k]
@@ -212,7 +212,7 @@ __device__ __forceinline__ bool get_tile(const Params& p, int t, int nrow_tiles,
     if ((C::PAIR ? 2 * mu : mt) >= nrow_tiles) return false;
     if constexpr (C::ROUTED) {
       if constexpr (META) {
-        const int4 v = p.tiles[mt];
+        const int4 v = tc::ld_ahead_v4(p.tiles + mt);
         tl.e = v.x;
         tl.row0 = v.y;
         tl.nvalid = v.z;
@@ -698,20 +698,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_2d(stg + 2048, &m.i1, ebar, tl.n0 + 32 * half, tl.row0 + 32 * q);
       }
     }
+    // routed DOWN: the gate of this thread's row, read a tile ahead (after
+    // the previous tile's first chunk)
+    float gt_next = 0.f;
+    if constexpr (C::ROUTED && C::EK == E_DOWN) {
+      if (have && row < tl.nvalid) gt_next = p.gates[(int64_t)tl.row0 + row];
+    }
     while (have && !aborted) {
       // the next tile's metadata is read while this one is processed
       const bool have_next = get_tile<C>(p, t + us, nrow_tiles, tn, choff, rank);
       // per-row metadata of this tile (routed kinds): issued before the wait
       int32_t pr = -1;
       float gt = 1.f;
-      if constexpr (C::ROUTED && (C::EK == E_DOWN || C::EK == E_DZ)) {
-        if (row < tl.nvalid) {
-          pr = p.rowpair[(int64_t)tl.row0 + row];
-          if constexpr (C::EK == E_DOWN) gt = p.gates[pr];
-        } else {
-          gt = 0.f;
-        }
+      if constexpr (C::ROUTED && C::EK == E_DZ) {
+        if (row < tl.nvalid) pr = p.rowpair[(int64_t)tl.row0 + row];
       }
+      if constexpr (C::ROUTED && C::EK == E_DOWN) gt = gt_next;
       if (!wait_or_abort<C::PAIR, true>(&sh->tfull[acc], aphase, sh, p.status, 400)) {
         aborted = true;
         break;
@@ -778,6 +780,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0 && ystore) {
             tc::tma_store_2d(&m.o0, stg, tl.n0 + 32 * c, yrow);
             tc::bulk_commit();
+          }
+          if constexpr (C::ROUTED && C::EK == E_DOWN) {
+            if (c == half)
+              gt_next = have_next && row < tn.nvalid
+                            ? tc::ld_ahead_f32(p.gates + (int64_t)tn.row0 + row)
+                            : 0.f;
           }
         }
       } else if constexpr (C::EK == E_DZ) {

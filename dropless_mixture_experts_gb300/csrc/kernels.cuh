@@ -109,9 +109,10 @@ bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_
 
 // row streams (stream.cu)
 // expert-sorted copy of token rows: out[pairrow[t*k + j]] = src[t] (with
-// gates: g_tj src[t]), padding rows zeroed
+// gates and no rowgate: g_tj src[t]), padding rows zeroed; with rowgate the
+// rows are copied unscaled and rowgate[pairrow[t*k + j]] = g_tj (0 on padding)
 void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, void* out, void* ws,
-                         cudaStream_t s, const float* gates = nullptr);
+                         cudaStream_t s, const float* gates, float* rowgate);
 // y = shared + sum of each token's pair rows (from the workspace), and the
 // value sum(y * upstream) when upstream is given
 void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* upstream, float* loss,

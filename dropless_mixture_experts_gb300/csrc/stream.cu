@@ -83,12 +83,15 @@ __device__ __forceinline__ uint4 ldg16(const void* p) {
 // The padding rows of each expert, [poff[e] + counts[e], poff[e+1]), are
 // zeroed by the items past the tokens' (the grouped GEMMs read them; zero
 // rows give zero contributions to every weight gradient).
-template <typename T, bool SCALE>
+// ROWGATE (unscaled copies): the first chunk's item of a row also stores the
+// row's gate (0 for a padding row) into rowgate.
+template <typename T, bool SCALE, bool ROWGATE = false>
 __global__ void __launch_bounds__(kThreads)
     scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ pairrow,
                         const float* __restrict__ gates, uint4* __restrict__ out, int64_t Tn,
                         int cpt, int k, const int32_t* __restrict__ poff,
-                        const int32_t* __restrict__ counts, int E, int pad) {
+                        const int32_t* __restrict__ counts, int E, int pad,
+                        float* __restrict__ rowgate = nullptr) {
   const int64_t n = Tn * cpt;
   const int64_t per_e = (int64_t)(pad - 1) * cpt;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -111,13 +114,17 @@ __global__ void __launch_bounds__(kThreads)
           st16<T>(out + r * cpt + c, f);
         } else {
           out[r * cpt + c] = v;
+          if (ROWGATE && c == 0) rowgate[r] = __ldg(gates + t * k + j);
         }
       }
     } else {
       const int64_t q = i - n;
       const int e = (int)(q / per_e);
       const int64_t r = (int64_t)poff[e] + counts[e] + (q % per_e) / cpt;
-      if (r < poff[e + 1]) out[r * cpt + q % cpt] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < poff[e + 1]) {
+        out[r * cpt + q % cpt] = make_uint4(0u, 0u, 0u, 0u);
+        if (ROWGATE && q % cpt == 0) rowgate[r] = 0.f;
+      }
     }
   }
 }
@@ -371,7 +378,7 @@ void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const f
 }  // namespace
 
 void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, void* out, void* ws,
-                         cudaStream_t s, const float* gates) {
+                         cudaStream_t s, const float* gates, float* rowgate) {
   if (d.tokens == 0) return;
   const int cpt = (int)((int64_t)d.d_model * L.elem / 16);
   const int pad = row_pad(d);
@@ -382,9 +389,10 @@ void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, vo
                    reinterpret_cast<const uint4*>(src), at<const int32_t>(ws, L.pairrow), gates,
                    reinterpret_cast<uint4*>(out), d.tokens, cpt, d.top_k,
                    at<const int32_t>(ws, L.poff), at<const int32_t>(ws, L.counts), d.experts,
-                   pad));
+                   pad, rowgate));
   };
-  if (!gates) launch(scatter_rows_kernel<__nv_bfloat16, false>);
+  if (rowgate) launch(scatter_rows_kernel<__nv_bfloat16, false, true>);
+  else if (!gates) launch(scatter_rows_kernel<__nv_bfloat16, false>);
   else if (d.dtype == MOE_BF16) launch(scatter_rows_kernel<__nv_bfloat16, true>);
   else launch(scatter_rows_kernel<float, true>);
 }

@@ -292,7 +292,7 @@ int tc_dz_bn(int h) { return pick_bn(h); }
 
 bool tc_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                         cudaStream_t s) {
-  launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s, p.gates);
+  launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s, p.gates, nullptr);
   return backward_one(d, L, p, ws, true, s);
 }
 

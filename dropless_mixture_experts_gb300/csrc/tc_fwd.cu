@@ -78,7 +78,7 @@ bool down(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = h;
-    q.gates = p.gates;
+    q.gates = at<float>(ws, L.rowgate);
     if constexpr (BN == 256) {
       if (down_pairs(h, dm)) {  // the expert rows are then padded to 256
         launch_tc<Cfg<A_K_TMA, B_MN_TMA, E_DOWN, BN, true, true>>(mp, q, L.MTcap / 2 * q.n_nt,
@@ -161,7 +161,7 @@ bool tc_router(const moe_dims& d, const Layout& L, const void* x, const void* w_
 
 bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                     cudaStream_t s) {
-  launch_scatter_rows(d, L, p.x, at<void>(ws, L.xs), ws, s);
+  launch_scatter_rows(d, L, p.x, at<void>(ws, L.xs), ws, s, p.gates, at<float>(ws, L.rowgate));
   if (!gateup_any(d, L, mode, p, ws, true, s)) return false;
   return down_any(d, L, p, ws, true, s);
 }

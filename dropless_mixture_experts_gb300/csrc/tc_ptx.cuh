@@ -117,6 +117,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Global loads issued where they stand in the source (the compiler keeps
+// volatile asm in order), for metadata read a tile ahead of its use.
+__device__ __forceinline__ int4 ld_ahead_v4(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_ahead_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 // Byte offset of the 16-byte chunk `c` (0..3) of row `r` in a 64-byte-row
 // tile laid out with the 64-byte TMA swizzle (chunk index XOR (r/2) mod 4).
 __device__ __forceinline__ uint32_t sw64_off(int r, int c) {
