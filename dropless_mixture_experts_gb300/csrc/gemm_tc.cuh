@@ -433,23 +433,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float bf16r(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
-
-// One thread's row (32 bf16) of a 64-byte-swizzled 32x32 staging tile.
-__device__ __forceinline__ void stage_read_row(const uint8_t* tile, int r, float (&v)[32]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::sw64_off(r, k));
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
-      v[8 * k + 2 * j] = f.x;
-      v[8 * k + 2 * j + 1] = f.y;
-    }
-  }
-}
-
 // A staged 32x32 bf16 tile (64-byte swizzle) to rows y0.. / columns x.. of a
 // row-major [rows, ld] bf16 array: lane l copies 16 bytes of rows l/4,
 // l/4 + 8, ... (four lanes per 64-byte row piece), rows past `rows` skipped.
@@ -464,6 +447,26 @@ __device__ __forceinline__ void staged_copy_out(const uint8_t* tile, void* dst, 
       *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(dst) +
                                 ((int64_t)y0 + r) * ld + x + 8 * q) = v;
   }
+}
+
+// One thread's row of a 64-byte-swizzled 32x32 staging tile as 16 bf16 pairs.
+__device__ __forceinline__ void stage_read_packed(const uint8_t* tile, int r, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 u = *reinterpret_cast<const uint4*>(tile + tc::sw64_off(r, k));
+    w[4 * k] = u.x;
+    w[4 * k + 1] = u.y;
+    w[4 * k + 2] = u.z;
+    w[4 * k + 3] = u.w;
+  }
+}
+
+// One thread's row of 32 bf16 already packed in pairs (bf16x2_rn).
+__device__ __forceinline__ void stage_write_packed(uint8_t* tile, int r, const uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4*>(tile + tc::sw64_off(r, k)) =
+        make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
 __device__ __forceinline__ void stage_write_row(uint8_t* tile, int r, const float (&v)[32]) {
@@ -554,8 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int stage = 0;
       uint32_t phase = 0;
-      Tile tl;
-      for (int t = u0; !aborted && get_tile<C>(p, t, nrow_tiles, tl, choff, rank); t += us) {
+      // the next tile's metadata is read while this tile's loads are issued
+      Tile tl, tn;
+      int t = u0;
+      bool have = get_tile<C>(p, t, nrow_tiles, tl, choff, rank);
+      for (; !aborted && have; t += us, tl = tn) {
+        have = get_tile<C>(p, t + us, nrow_tiles, tn, choff, rank);
         int brow0 = 0;
         if constexpr (C::ROUTED && !C::DW) brow0 = tl.e * p.brow_stride;
         if constexpr (C::DW) brow0 = tl.row0;
@@ -728,31 +735,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if constexpr (C::EK == E_GU) {
         // H = silu(a_g) * a_u with a_g, a_u rounded to bf16 first (the values
-        // a backward pass reads back); staged 32x32 tiles copied out by the
-        // load/store units
+        // a backward pass reads back), in float pairs; staged 32x32 tiles
+        // copied out by the load/store units
 #pragma unroll 1
         for (int c = half; c < C::BN / 64; c += 2) {
           uint32_t g[32], u[32];
           tc::tmem_ld32(tacc + 32 * c, g);
           tc::tmem_ld32(tacc + C::BN / 2 + 32 * c, u);
           tc::tmem_ld_wait();
-          float gv[32], uv[32], hv[32];
+          uint32_t gp[16], up[16], hp[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            gv[i] = bf16r(__uint_as_float(g[i]));
-            uv[i] = bf16r(__uint_as_float(u[i]));
-            hv[i] = __fdividef(gv[i], 1.f + __expf(-gv[i])) * uv[i];
+          for (int j = 0; j < 16; ++j) {
+            gp[j] = tc::bf16x2_rn(__uint_as_float(g[2 * j]), __uint_as_float(g[2 * j + 1]));
+            up[j] = tc::bf16x2_rn(__uint_as_float(u[2 * j]), __uint_as_float(u[2 * j + 1]));
+            const uint64_t gx = tc::bf16x2_to_f2(gp[j]);
+            float h0, h1;
+            tc::f2_split(tc::f2_mul(tc::f2_mul(gx, tc::f2_sigmoid(gx)), tc::bf16x2_to_f2(up[j])),
+                         h0, h1);
+            hp[j] = tc::bf16x2_rn(h0, h1);
           }
           __syncwarp();  // the previous chunk's copies have read the staging
-          stage_write_row(stg, lane, hv);
-          if (p.save) stage_write_row(stg + 2048, lane, gv);
+          stage_write_packed(stg, lane, hp);
+          if (p.save) stage_write_packed(stg + 2048, lane, gp);
           __syncwarp();
           const int x = tl.n0 + 32 * c;
           staged_copy_out(stg, p.dst0, yrow, x, p.ld_out, p.rows_out, lane);
           if (p.save) {
             staged_copy_out(stg + 2048, p.dst1, yrow, x, p.ld_out, p.rows_out, lane);
             __syncwarp();  // H's copies have read the first slot
-            stage_write_row(stg, lane, uv);
+            stage_write_packed(stg, lane, up);
             __syncwarp();
             staged_copy_out(stg, p.dst2, yrow, x, p.ld_out, p.rows_out, lane);
           }
@@ -794,7 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // SwiGLU backward from the saved pre-activations (TMA-staged); the
         // partial <dH, H> = g dg over these columns; dA tiles stored by TMA
         const int h = p.ld_out;
-        float dgp = 0.f;
+        uint64_t dgp2 = tc::f2(0.f, 0.f);  // <dH, H> over even / odd columns
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
           uint32_t zv[32];
@@ -805,9 +816,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ephase ^= 1;
-          float ag[32], au[32];
-          stage_read_row(stg, lane, ag);
-          stage_read_row(stg + 2048, lane, au);
+          uint32_t wg[16], wu[16];
+          stage_read_packed(stg, lane, wg);
+          stage_read_packed(stg + 2048, lane, wu);
           __syncwarp();
           // the next input tiles of this warp: next chunk, or the first chunk
           // of the next tile
@@ -821,21 +832,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc::tma_load_2d(stg + 2048, &m.i1, ebar, nx, ny);
             }
           }
-          float dag[32], dau[32];
+          // in float pairs: s = sigmoid(a_g), H = bf16(a_g s a_u) as the
+          // forward stored it, dA_u = dH a_g s, dA_g = dH a_u s (1 + a_g (1 - s))
+          uint32_t dagp[16], daup[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float dh = __uint_as_float(zv[i]);
-            const float s = __fdividef(1.f, 1.f + __expf(-ag[i]));
-            const float sl = ag[i] * s;
-            const float hv = bf16r(sl * au[i]);  // H as the forward stored it
-            dgp = fmaf(dh, hv, dgp);
-            dau[i] = dh * sl;
-            dag[i] = dh * au[i] * s * (1.f + ag[i] * (1.f - s));
+          for (int j = 0; j < 16; ++j) {
+            const uint64_t ag = tc::bf16x2_to_f2(wg[j]), au = tc::bf16x2_to_f2(wu[j]);
+            const uint64_t dh = tc::f2(__uint_as_float(zv[2 * j]), __uint_as_float(zv[2 * j + 1]));
+            const uint64_t sg = tc::f2_sigmoid(ag);
+            const uint64_t sl = tc::f2_mul(ag, sg);
+            float h0, h1;
+            tc::f2_split(tc::f2_mul(sl, au), h0, h1);
+            dgp2 = tc::f2_fma(dh, tc::bf16x2_to_f2(tc::bf16x2_rn(h0, h1)), dgp2);
+            float a0, a1;
+            tc::f2_split(tc::f2_mul(dh, sl), a0, a1);
+            daup[j] = tc::bf16x2_rn(a0, a1);
+            const uint64_t oms = tc::f2_fma(sg, tc::f2(-1.f, -1.f), tc::f2(1.f, 1.f));
+            const uint64_t inner = tc::f2_fma(ag, oms, tc::f2(1.f, 1.f));
+            tc::f2_split(tc::f2_mul(tc::f2_mul(tc::f2_mul(dh, au), sg), inner), a0, a1);
+            dagp[j] = tc::bf16x2_rn(a0, a1);
           }
           if (lane == 0) tc::bulk_wait_read0();
           __syncwarp();
-          stage_write_row(stg + 4096, lane, dag);
-          stage_write_row(stg + 6144, lane, dau);
+          stage_write_packed(stg + 4096, lane, dagp);
+          stage_write_packed(stg + 6144, lane, daup);
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0 && ystore) {
@@ -846,7 +866,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (aborted) break;
-        if (C::ROUTED && pr >= 0) p.dg_part[(int64_t)pr * p.dg_ld + 2 * tl.nt + half] = dgp;
+        if (C::ROUTED && pr >= 0) {
+          float d0, d1;
+          tc::f2_split(dgp2, d0, d1);
+          p.dg_part[(int64_t)pr * p.dg_ld + 2 * tl.nt + half] = d0 + d1;
+        }
       } else if constexpr (C::EK == E_ROUTER) {
         // router: one token per thread of the first four epilogue warps; its
         // E logits come straight from tensor memory, the top-k selection and

@@ -132,6 +132,59 @@ __device__ __forceinline__ float ld_ahead_f32(const float* p) {
   return v;
 }
 
+// ---- pairs of floats in one 64-bit register: one instruction per pair ------
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// two floats rounded to bf16 (nearest even) in one word, `lo` in bits 0..15
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// the two bf16 of a word as a float pair
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// sigmoid of a float pair: 1 / (1 + 2^(-x log2 e))
+__device__ __forceinline__ uint64_t f2_sigmoid(uint64_t x) {
+  float t0, t1;
+  f2_split(f2_mul(x, f2(-1.4426950408889634f, -1.4426950408889634f)), t0, t1);
+  float y0, y1;
+  f2_split(f2_add(f2(ex2_approx(t0), ex2_approx(t1)), f2(1.f, 1.f)), y0, y1);
+  return f2(rcp_approx(y0), rcp_approx(y1));
+}
+
 // Byte offset of the 16-byte chunk `c` (0..3) of row `r` in a 64-byte-row
 // tile laid out with the 64-byte TMA swizzle (chunk index XOR (r/2) mod 4).
 __device__ __forceinline__ uint32_t sw64_off(int r, int c) {
