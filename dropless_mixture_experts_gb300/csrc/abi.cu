@@ -339,13 +339,18 @@ moe_status backward_parts(int parts, const moe_dims* dims, const void* dy, const
   const int dg_ld = (int)(2 * h / 64);
   int dg_n = (int)(h / 64);
   if (bf) {
-    if (!tc_backward_routed(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
+    // dZ, the router logit gradients (dX adds each pair's router term to its
+    // row), dX and the weight gradients, dW_r and dx
+    if (!tc_backward_routed_dz(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
     dg_n = (int)(2 * h / tc_dz_bn((int)h));
+    launch_router_dsel(*dims, L, p, dg_n, dg_ld, workspace, stream, true);
+    if (!tc_backward_routed_rest(*dims, L, p, workspace, stream)) return MOE_ERR_CUDA;
+    launch_router_dw_dx(*dims, L, p, workspace, stream, shared_done, true);
   } else {
     simt_backward_routed(*dims, L, p, workspace, stream);
     dg_n = simt_dz_tiles((int)h);
+    launch_router_backward(*dims, L, p, dg_n, dg_ld, workspace, stream, shared_done);
   }
-  launch_router_backward(*dims, L, p, dg_n, dg_ld, workspace, stream, shared_done);
   return cuda_status();
 }
 

@@ -70,6 +70,7 @@ struct Layout {
   size_t rowgate;  // the gate of each sorted row's pair, 0 on padding [padded rows] (bf16 path)
   size_t ys;       // shared-expert output [T, d]
   size_t dg_part, dA, dxsort, dxs, dAs, dys, dsel, dwr_part;
+  size_t rowdsel;  // the router logit gradient of each sorted row's pair [padded rows] (bf16 path)
   size_t gH, gHs;  // gate * H for the W_down gradients (float32 path only)
   size_t dl;      // dense router-logit gradient [T, E] (bf16 path)
   size_t wrt;     // W_r^T [E, d]
@@ -180,6 +181,7 @@ inline Layout make_layout(const moe_dims& d, int mode) {
     L.gHs = take(gh ? (size_t)L.elem * T * hs : 0);
     L.dys = take((size_t)L.elem * L.PPcap * dm);
     L.dsel = take(sizeof(float) * T * d.top_k);
+    L.rowdsel = take(sizeof(float) * L.PPcap);
     L.dwr_part = take(sizeof(float) * kRouterBwdRanges * dm * E);
     L.dl = take((size_t)2 * T * E);
     L.wrt = take((size_t)L.elem * E * dm);

@@ -82,7 +82,11 @@ struct Params {
   int brow_stride = 0;              // rows of a B weight matrix per expert (0: activations)
   int M = 0, N = 0;                 // DW output dims / row-kind output columns
   // epilogue
-  const float* gates = nullptr;     // routed DOWN: gate per sorted row; router: logit offsets [E]
+  const float* gates = nullptr;     // routed DOWN: gate per sorted row; routed DX: the router
+                                    //   logit gradient of each sorted row's pair (nullable);
+                                    //   router: logit offsets [E]
+  const void* wrow = nullptr;       // routed DX with gates: W_r^T [E, ld_out] bf16, whose row
+                                    //   e times the pair's logit gradient joins the pair's dx
   int save = 0;                     // GU: also store a_g, a_u
   void* out0 = nullptr;             // router: top-k indices [T, k]
   void* out1 = nullptr;             // router: gates [T, k]
@@ -705,11 +709,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tma_load_2d(stg + 2048, &m.i1, ebar, tl.n0 + 32 * half, tl.row0 + 32 * q);
       }
     }
-    // routed DOWN: the gate of this thread's row, read a tile ahead (after
-    // the previous tile's first chunk)
+    // routed DOWN: the gate of this thread's row; routed DX: its pair's
+    // router logit gradient; read a tile ahead (after the previous tile's
+    // first chunk)
+    constexpr bool ROWSC = C::ROUTED && (C::EK == E_DOWN || C::EK == E_DX);
+    const bool rowsc = ROWSC && p.gates;
     float gt_next = 0.f;
-    if constexpr (C::ROUTED && C::EK == E_DOWN) {
-      if (have && row < tl.nvalid) gt_next = p.gates[(int64_t)tl.row0 + row];
+    if constexpr (ROWSC) {
+      if (rowsc && have && row < tl.nvalid) gt_next = p.gates[(int64_t)tl.row0 + row];
+    }
+    // routed DX with the router term: the entries of W_r^T[e] under this
+    // warp's chunks of a tile (c = half, half + 2, ...), spread over the
+    // lanes (lane l: 8 entries at 8 (l % 4) of its (l / 4)-th chunk) and
+    // read a tile ahead; each chunk takes its 32 entries by shuffles
+    constexpr int NCH = C::BN / 64 > 0 ? C::BN / 64 : 1;  // chunks per warp and tile
+    int4 wr_cur = make_int4(0, 0, 0, 0), wr_next = make_int4(0, 0, 0, 0);
+    auto load_wr = [&](const Tile& x) {
+      if (lane < 4 * NCH) {
+        const int c = half + 2 * (lane >> 2);
+        wr_next = tc::ld_ahead_v4(
+            reinterpret_cast<const int4*>(reinterpret_cast<const __nv_bfloat16*>(p.wrow) +
+                                          (int64_t)x.e * p.ld_out + x.n0 + 32 * c) +
+            (lane & 3));
+      }
+    };
+    if constexpr (C::ROUTED && C::EK == E_DX) {
+      if (rowsc && have) load_wr(tl);
     }
     while (have && !aborted) {
       // the next tile's metadata is read while this one is processed
@@ -720,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (C::ROUTED && C::EK == E_DZ) {
         if (row < tl.nvalid) pr = p.rowpair[(int64_t)tl.row0 + row];
       }
-      if constexpr (C::ROUTED && C::EK == E_DOWN) gt = gt_next;
+      if constexpr (ROWSC) gt = gt_next;
+      if constexpr (C::ROUTED && C::EK == E_DX) wr_cur = wr_next;
       if (!wait_or_abort<C::PAIR, true>(&sh->tfull[acc], aphase, sh, p.status, 400)) {
         aborted = true;
         break;
@@ -772,17 +798,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         // one output row per sorted row, stored by TMA as bf16 tiles:
         //   DOWN: gate * (H W_down), the pair's share of its token's output
         //         (the shared expert: its whole output row)
-        //   DX:   [dA_g | dA_u] [W_gate | W_up]^T, the pair's share of dx
+        //   DX:   [dA_g | dA_u] [W_gate | W_up]^T, the pair's share of dx,
+        //         plus (routed, with the router term) dl_pair W_r[:, e]^T
         // the combine gathers the k shares of a token in a fixed order
         const float sc = C::EK == E_DOWN ? gt : 1.f;
 #pragma unroll 1
         for (int c = half; c < C::BN / 32; c += 2) {
+          int4 w4[4];  // the chunk's 32 entries of W_r^T[e] (the same for every row)
+          if constexpr (C::ROUTED && C::EK == E_DX) {
+            if (rowsc) {
+              const int src = 4 * ((c - half) >> 1);
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                w4[k4].x = __shfl_sync(0xffffffffu, wr_cur.x, src + k4);
+                w4[k4].y = __shfl_sync(0xffffffffu, wr_cur.y, src + k4);
+                w4[k4].z = __shfl_sync(0xffffffffu, wr_cur.z, src + k4);
+                w4[k4].w = __shfl_sync(0xffffffffu, wr_cur.w, src + k4);
+              }
+              if (c == half && have_next) load_wr(tn);
+            }
+          }
           uint32_t v[32];
           tc::tmem_ld32(tacc + 32 * c, v);
           tc::tmem_ld_wait();
           float o[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = sc * __uint_as_float(v[i]);
+          if constexpr (C::ROUTED && C::EK == E_DX) {
+            if (rowsc) {
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4) {
+                const uint32_t wv[4] = {(uint32_t)w4[k4].x, (uint32_t)w4[k4].y,
+                                        (uint32_t)w4[k4].z, (uint32_t)w4[k4].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  o[8 * k4 + 2 * j] = fmaf(gt, __uint_as_float(wv[j] << 16), o[8 * k4 + 2 * j]);
+                  o[8 * k4 + 2 * j + 1] =
+                      fmaf(gt, __uint_as_float(wv[j] & 0xFFFF0000u), o[8 * k4 + 2 * j + 1]);
+                }
+              }
+            }
+          }
           if (lane == 0) tc::bulk_wait_read0();
           __syncwarp();
           stage_write_row(stg, lane, o);
@@ -792,8 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::tma_store_2d(&m.o0, stg, tl.n0 + 32 * c, yrow);
             tc::bulk_commit();
           }
-          if constexpr (C::ROUTED && C::EK == E_DOWN) {
-            if (c == half)
+          if constexpr (ROWSC) {
+            if (rowsc && c == half)
               gt_next = have_next && row < tn.nvalid
                             ? tc::ld_ahead_f32(p.gates + (int64_t)tn.row0 + row)
                             : 0.f;

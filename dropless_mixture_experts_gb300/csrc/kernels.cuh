@@ -92,8 +92,13 @@ bool tc_grouped_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtr
                     cudaStream_t s);
 bool tc_shared_fwd(const moe_dims& d, const Layout& L, int mode, const LayerPtrs& p, void* ws,
                    cudaStream_t s);
-bool tc_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
-                        cudaStream_t s);
+// the routed backward in two parts: the row copy of g dy and dZ; then dX
+// (with the router term from the logit gradients per sorted row) and the
+// weight gradients
+bool tc_backward_routed_dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                           cudaStream_t s);
+bool tc_backward_routed_rest(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                             cudaStream_t s);
 bool tc_backward_shared(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
                         cudaStream_t s);
 int tc_dz_bn(int h);  // column tile of the DZ GEMM (its gate-gradient partials per row)
@@ -117,9 +122,11 @@ void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, vo
 // value sum(y * upstream) when upstream is given
 void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* upstream, float* loss,
                     void* ws, cudaStream_t s);
-// dx = shared + sum of each token's pair rows + dlogits W_r^T (wt = W_r^T [E, d])
+// dx = shared + sum of each token's pair rows + dlogits W_r^T (wt = W_r^T [E, d]);
+// term_in_rows: the pair rows already hold their dlogits W_r^T term (added
+// here only for the slots without a row)
 void launch_router_dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, const float* dsel,
-                      const void* wt, void* ws, cudaStream_t s);
+                      const void* wt, void* ws, cudaStream_t s, bool term_in_rows);
 
 // router backward (router_bwd.cu)
 bool router_backward_supported(const moe_dims& d);
@@ -127,5 +134,11 @@ bool router_backward_supported(const moe_dims& d);
 // for `shared_done` when it is given
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                             int dg_ld, void* ws, cudaStream_t s, cudaEvent_t shared_done = nullptr);
+// the same in two parts: the logit gradients (dsel; with rows, also per
+// sorted row for the tensor-core input-gradient GEMM), then dW_r and dx
+void launch_router_dsel(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
+                        int dg_ld, void* ws, cudaStream_t s, bool rows);
+void launch_router_dw_dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                         cudaStream_t s, cudaEvent_t shared_done, bool term_in_rows);
 
 }  // namespace moe

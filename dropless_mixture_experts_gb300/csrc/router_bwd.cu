@@ -17,6 +17,9 @@ namespace {
 // lanes (the power of two >= k) takes one token, lane j of the group its
 // slot j.  With dl given, the token's dense bf16 row of the logit gradient
 // (zero off the selection; E a multiple of 8) is written as well.
+// With rowdsel given, the logit gradient of each pair with a sorted row is
+// also stored at that row (the tensor-core input-gradient GEMM adds the
+// router term to the pair's row).
 // The blocks past the tokens' write W_r^T [E, d] from W_r [d, E] (storage
 // type unchanged) for the router input gradient.
 template <typename T>
@@ -29,7 +32,8 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
                                                           __nv_bfloat16* __restrict__ dl,
                                                           unsigned dsel_blocks,
                                                           const T* __restrict__ w, int d,
-                                                          T* __restrict__ wt) {
+                                                          T* __restrict__ wt,
+                                                          float* __restrict__ rowdsel) {
   if (blockIdx.x >= dsel_blocks) {
     const int64_t n = (int64_t)d * E;
     const int64_t stride = (int64_t)(gridDim.x - dsel_blocks) * blockDim.x;
@@ -44,8 +48,10 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
   const bool own = live && j < k;
   const int64_t p = t * k + j;
   float qj = 0.f, g = 0.f;
+  int32_t prow = -1;
   if (own) {
-    if (pairrow[p] >= 0) {
+    prow = pairrow[p];
+    if (prow >= 0) {
       const float* src = dg_part + p * dg_ld;
       for (int q = 0; q < dg_n; ++q) qj += src[q];
     }
@@ -54,7 +60,10 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
   float sq = qj;
   for (int o = G / 2; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
   const float v = fmaf(-g, sq, qj);
-  if (own) dsel[p] = v;
+  if (own) {
+    dsel[p] = v;
+    if (rowdsel && prow >= 0) rowdsel[prow] = v;
+  }
   if (dl) {
     if (live) {
       uint4* row = reinterpret_cast<uint4*>(dl + t * E);
@@ -134,15 +143,36 @@ __global__ void __launch_bounds__(256) router_dw_reduce_kernel(const float* __re
   dw[i] = s;
 }
 
+int device_sms() {
+  int dev = 0, sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
 template <typename T>
-void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
-                       int dg_ld, void* ws, cudaStream_t s, cudaEvent_t shared_done) {
+void router_dsel_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n, int dg_ld,
+                   void* ws, cudaStream_t s, bool rows) {
   const int dm = d.d_model, E = d.experts, k = d.top_k;
-  if (d.tokens == 0) {
-    zero_fill_f32(p.dw_router, (int64_t)dm * E, s);
-    if (shared_done) cudaStreamWaitEvent(s, shared_done, 0);
-    return;
-  }
+  const int sms = device_sms();
+  int G = 1;
+  while (G < k) G *= 2;
+  const unsigned dsel_blocks = (unsigned)((d.tokens * G + 255) / 256);
+  int64_t tr_blocks = ((int64_t)dm * E + 255) / 256;
+  if (tr_blocks > sms) tr_blocks = sms;
+  MOE_LAUNCH("router_dsel", s,
+             router_dsel_kernel<T><<<dsel_blocks + (unsigned)tr_blocks, 256, 0, s>>>(
+                 p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, G,
+                 at<float>(ws, L.dsel), p.topk_idx, E, at<const int32_t>(ws, L.pairrow),
+                 tc_router_dw_supported(d) ? at<__nv_bfloat16>(ws, L.dl) : nullptr, dsel_blocks,
+                 reinterpret_cast<const T*>(p.w_router), dm, at<T>(ws, L.wrt),
+                 rows ? at<float>(ws, L.rowdsel) : nullptr));
+}
+
+template <typename T>
+void router_dw_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                    cudaStream_t s, cudaEvent_t shared_done, bool term_in_rows) {
+  const int dm = d.d_model, E = d.experts, k = d.top_k;
   float* dsel = at<float>(ws, L.dsel);
   float* part = at<float>(ws, L.dwr_part);
   static bool attr_set = false;
@@ -151,29 +181,15 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
                          kRouterBwdSmem);
     attr_set = true;
   }
-  int dev = 0, sms = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms();
   const bool tc_dw = tc_router_dw_supported(d);
-
-  int G = 1;
-  while (G < k) G *= 2;
   T* wt = at<T>(ws, L.wrt);
-  const unsigned dsel_blocks = (unsigned)((d.tokens * G + 255) / 256);
-  int64_t tr_blocks = ((int64_t)dm * E + 255) / 256;
-  if (tr_blocks > sms) tr_blocks = sms;
-  MOE_LAUNCH("router_dsel", s,
-             router_dsel_kernel<T><<<dsel_blocks + (unsigned)tr_blocks, 256, 0, s>>>(
-                 p.gates, at<float>(ws, L.dg_part), dg_ld, dg_n, d.tokens, k, G, dsel,
-                 p.topk_idx, E, at<const int32_t>(ws, L.pairrow),
-                 tc_dw ? at<__nv_bfloat16>(ws, L.dl) : nullptr, dsel_blocks,
-                 reinterpret_cast<const T*>(p.w_router), dm, wt));
 
   // the router weight gradient first: the input gradient also needs the
   // shared expert's rows, which may come from another stream
   auto input_grad = [&] {
     if (shared_done) cudaStreamWaitEvent(s, shared_done, 0);
-    launch_router_dx(d, L, p, dsel, wt, ws, s);
+    launch_router_dx(d, L, p, dsel, wt, ws, s, term_in_rows);
   };
   if (tc_dw) {
     tc_router_dw(d, L, p, ws, s);
@@ -200,12 +216,30 @@ void router_backward_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, i
 
 }  // namespace
 
+void launch_router_dsel(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
+                        int dg_ld, void* ws, cudaStream_t s, bool rows) {
+  if (d.tokens == 0) return;
+  if (d.dtype == MOE_BF16) router_dsel_t<__nv_bfloat16>(d, L, p, dg_n, dg_ld, ws, s, rows);
+  else router_dsel_t<float>(d, L, p, dg_n, dg_ld, ws, s, rows);
+}
+
+void launch_router_dw_dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                         cudaStream_t s, cudaEvent_t shared_done, bool term_in_rows) {
+  if (d.tokens == 0) {
+    zero_fill_f32(p.dw_router, (int64_t)d.d_model * d.experts, s);
+    if (shared_done) cudaStreamWaitEvent(s, shared_done, 0);
+    return;
+  }
+  if (d.dtype == MOE_BF16)
+    router_dw_dx_t<__nv_bfloat16>(d, L, p, ws, s, shared_done, term_in_rows);
+  else
+    router_dw_dx_t<float>(d, L, p, ws, s, shared_done, term_in_rows);
+}
+
 void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs& p, int dg_n,
                             int dg_ld, void* ws, cudaStream_t s, cudaEvent_t shared_done) {
-  if (d.dtype == MOE_BF16)
-    router_backward_t<__nv_bfloat16>(d, L, p, dg_n, dg_ld, ws, s, shared_done);
-  else
-    router_backward_t<float>(d, L, p, dg_n, dg_ld, ws, s, shared_done);
+  launch_router_dsel(d, L, p, dg_n, dg_ld, ws, s, false);
+  launch_router_dw_dx(d, L, p, ws, s, shared_done, false);
 }
 
 bool router_backward_supported(const moe_dims& d) {

@@ -240,10 +240,12 @@ __global__ void __launch_bounds__(kThreads)
 // A capacity-dropped slot has no row but keeps its router term (the softmax
 // couples it to the kept slots); a rejected index (e outside [0, E)) has
 // neither.  The first KM slots' indices and logit gradients are loaded one
-// item ahead.
+// item ahead.  TERM_IN_ROWS: the pair rows already hold their router term
+// (the tensor-core input-gradient GEMM adds it), which is then added here
+// for the slots without a row only.
 constexpr int kNoRow = 1 << 16;  // router_dx: the slot's pair has no row (E <= 256)
 
-template <typename T, int KM>
+template <typename T, int KM, bool TERM_IN_ROWS>
 __global__ void __launch_bounds__(kThreads)
     router_dx_kernel(const int32_t* __restrict__ idx, const float* __restrict__ dsel,
                      const T* __restrict__ wt, const T* __restrict__ dxsort,
@@ -294,6 +296,12 @@ __global__ void __launch_bounds__(kThreads)
     auto add_slot = [&](int j) {
       if (ex[j] < 0) return;
       float fv[VE], fw[VE];
+      if (TERM_IN_ROWS && !(ex[j] & kNoRow)) {
+        cvt16<T>(v[j], fv);
+#pragma unroll
+        for (int q = 0; q < VE; ++q) acc[q] += fv[q];
+        return;
+      }
       if (ex[j] & kNoRow) {
 #pragma unroll
         for (int q = 0; q < VE; ++q) fv[q] = 0.f;
@@ -356,7 +364,7 @@ void combine_t(const moe_dims& d, const Layout& L, void* y, const void* G, float
 
 template <typename T>
 void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const float* dsel,
-                 const void* wt, void* ws, cudaStream_t s) {
+                 const void* wt, void* ws, cudaStream_t s, bool term_in_rows) {
   const T* dxs = d.shared_hidden > 0 ? at<const T>(ws, L.dxs) : nullptr;
   const int64_t items = d.tokens * (d.d_model / (16 / (int)sizeof(T)));
   const unsigned blocks = stream_grid(items, INT32_MAX);
@@ -368,10 +376,10 @@ void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const f
                    d.d_model, d.top_k, d.experts));
   };
   switch (slots_ahead(d.top_k)) {
-    case 1: launch(router_dx_kernel<T, 1>); break;
-    case 2: launch(router_dx_kernel<T, 2>); break;
-    case 4: launch(router_dx_kernel<T, 4>); break;
-    default: launch(router_dx_kernel<T, 8>); break;
+    case 1: term_in_rows ? launch(router_dx_kernel<T, 1, true>) : launch(router_dx_kernel<T, 1, false>); break;
+    case 2: term_in_rows ? launch(router_dx_kernel<T, 2, true>) : launch(router_dx_kernel<T, 2, false>); break;
+    case 4: term_in_rows ? launch(router_dx_kernel<T, 4, true>) : launch(router_dx_kernel<T, 4, false>); break;
+    default: term_in_rows ? launch(router_dx_kernel<T, 8, true>) : launch(router_dx_kernel<T, 8, false>); break;
   }
 }
 
@@ -408,10 +416,10 @@ void launch_combine(const moe_dims& d, const Layout& L, void* y, const void* ups
 }
 
 void launch_router_dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, const float* dsel,
-                      const void* wt, void* ws, cudaStream_t s) {
+                      const void* wt, void* ws, cudaStream_t s, bool term_in_rows) {
   if (d.tokens == 0) return;
-  if (d.dtype == MOE_BF16) router_dx_t<__nv_bfloat16>(d, L, p, dsel, wt, ws, s);
-  else router_dx_t<float>(d, L, p, dsel, wt, ws, s);
+  if (d.dtype == MOE_BF16) router_dx_t<__nv_bfloat16>(d, L, p, dsel, wt, ws, s, term_in_rows);
+  else router_dx_t<float>(d, L, p, dsel, wt, ws, s, term_in_rows);
 }
 
 }  // namespace moe

@@ -91,6 +91,9 @@ bool dx(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool r
     q.rowpair = at<int32_t>(ws, L.rowpair);
     q.top_k = d.top_k;
     q.brow_stride = dm;
+    // the router term: the logit gradient of each row's pair times W_r^T[e]
+    q.gates = at<float>(ws, L.rowdsel);
+    q.wrow = at<void>(ws, L.wrt);
     if constexpr (BN == 256) {
       if (pr) {
         launch_tc<Cfg<A_K_TMA, B_K_TMA, E_DX, BN, true, true>>(mp, q, L.MTcap / 2 * q.n_nt,
@@ -276,11 +279,13 @@ bool dw_gateup(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
   ((n) % 256 == 0 ? fn<256>(__VA_ARGS__)                    \
                   : (n) % 128 == 0 ? fn<128>(__VA_ARGS__) : fn<64>(__VA_ARGS__))
 
+// parts: 1 = dZ, 2 = dX and the weight gradients, 3 = both
 bool backward_one(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws, bool routed,
-                  cudaStream_t s) {
+                  cudaStream_t s, int parts = 3) {
   const int h = routed ? d.d_hidden : d.shared_hidden;
   const int dm = d.d_model;
-  if (!MOE_BN_DISPATCH(dz, h, d, L, p, ws, routed, s)) return false;
+  if ((parts & 1) && !MOE_BN_DISPATCH(dz, h, d, L, p, ws, routed, s)) return false;
+  if (!(parts & 2)) return true;
   if (!MOE_BN_DISPATCH(dx, dm, d, L, p, ws, routed, s)) return false;
   if (!MOE_BN_DISPATCH(dw_down, dm, d, L, p, ws, routed, s)) return false;
   return MOE_BN_DISPATCH(dw_gateup, h, d, L, p, ws, routed, s);
@@ -290,10 +295,15 @@ bool backward_one(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* 
 
 int tc_dz_bn(int h) { return pick_bn(h); }
 
-bool tc_backward_routed(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
-                        cudaStream_t s) {
+bool tc_backward_routed_dz(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                           cudaStream_t s) {
   launch_scatter_rows(d, L, p.dy, at<void>(ws, L.dys), ws, s, p.gates, nullptr);
-  return backward_one(d, L, p, ws, true, s);
+  return backward_one(d, L, p, ws, true, s, 1);
+}
+
+bool tc_backward_routed_rest(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
+                             cudaStream_t s) {
+  return backward_one(d, L, p, ws, true, s, 2);
 }
 
 bool tc_backward_shared(const moe_dims& d, const Layout& L, const LayerPtrs& p, void* ws,
