@@ -9,18 +9,43 @@
 // row per access).  An item's row indices are loaded one item ahead, and
 // every row load of an item is issued before the first use, so each thread
 // keeps k+2 loads in flight and no load waits on an index load.
+#include <mutex>
+
 #include "kernels.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kBlocksPerSm = 32;  // grid-stride launches: 4 full-occupancy waves
 
-// Grid of a grid-stride launch: up to kBlocksPerSm blocks per SM the launch
-// may fill (capped = false: per SM of the device, for a launch whose
-// reduction order follows its grid and must not depend on the SM limit).
-unsigned stream_grid(int64_t items, int64_t cap, bool capped = true) {
+// Resident blocks per SM of a kernel at kThreads threads (cached per kernel).
+int resident_blocks(const void* kernel) {
+  static std::mutex mu;
+  static const void* keys[64];
+  static int vals[64];
+  static int n = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (keys[i] == kernel) return vals[i];
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  if (n < 64) {
+    keys[n] = kernel;
+    vals[n++] = occ;
+  }
+  return occ;
+}
+
+// Grid of a grid-stride launch: `waves` whole waves of the kernel's resident
+// blocks on the SMs the launch may fill, every thread looping over its items
+// (no partial last wave; one wave measured fastest for the gathering sums,
+// four for the row copy).  capped = false: per SM of the device, for a
+// launch whose reduction order follows its grid and must not depend on the
+// SM limit.
+template <class K>
+unsigned stream_grid(K kernel, int64_t items, int64_t cap, bool capped = true, int waves = 1) {
   int sms = tcg_launch_sms();
   if (!capped) {
     int dev = 0;
@@ -28,7 +53,8 @@ unsigned stream_grid(int64_t items, int64_t cap, bool capped = true) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   }
   int64_t b = (items + kThreads - 1) / kThreads;
-  const int64_t full = (int64_t)sms * kBlocksPerSm;
+  const int64_t full =
+      (int64_t)sms * resident_blocks(reinterpret_cast<const void*>(kernel)) * waves;
   if (b > full) b = full;
   if (b > cap) b = cap;
   if (b < 1) b = 1;
@@ -345,8 +371,8 @@ void combine_t(const moe_dims& d, const Layout& L, void* y, const void* G, float
   const int64_t items = d.tokens * (d.d_model / (16 / (int)sizeof(T)));
   // the loss partials are summed in block order: the grid must not follow
   // the SM limit
-  const unsigned blocks = stream_grid(items, kLossBlocks, false);
   auto launch = [&](auto kernel) {
+    const unsigned blocks = stream_grid(kernel, items, kLossBlocks, false);
     MOE_LAUNCH("combine", s,
                kernel<<<blocks, kThreads, 0, s>>>(
                    at<const T>(ws, L.osort), at<const int32_t>(ws, L.pairrow), ys,
@@ -367,8 +393,8 @@ void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const f
                  const void* wt, void* ws, cudaStream_t s, bool term_in_rows) {
   const T* dxs = d.shared_hidden > 0 ? at<const T>(ws, L.dxs) : nullptr;
   const int64_t items = d.tokens * (d.d_model / (16 / (int)sizeof(T)));
-  const unsigned blocks = stream_grid(items, INT32_MAX);
   auto launch = [&](auto kernel) {
+    const unsigned blocks = stream_grid(kernel, items, INT32_MAX);
     MOE_LAUNCH("router_dx", s,
                kernel<<<blocks, kThreads, 0, s>>>(
                    p.topk_idx, dsel, reinterpret_cast<const T*>(wt), at<const T>(ws, L.dxsort),
@@ -393,7 +419,7 @@ void launch_scatter_rows(const moe_dims& d, const Layout& L, const void* src, vo
   const int64_t items = d.tokens * cpt + (int64_t)d.experts * (pad - 1) * cpt;
   auto launch = [&](auto kernel) {
     MOE_LAUNCH("scatter_rows", s,
-               kernel<<<stream_grid(items, INT32_MAX), kThreads, 0, s>>>(
+               kernel<<<stream_grid(kernel, items, INT32_MAX, true, 4), kThreads, 0, s>>>(
                    reinterpret_cast<const uint4*>(src), at<const int32_t>(ws, L.pairrow), gates,
                    reinterpret_cast<uint4*>(out), d.tokens, cpt, d.top_k,
                    at<const int32_t>(ws, L.poff), at<const int32_t>(ws, L.counts), d.experts,
