@@ -875,6 +875,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t wg[16], wu[16];
           stage_read_packed(stg, lane, wg);
           stage_read_packed(stg + 2048, lane, wu);
+          // the copies below overwrite these staging tiles: every lane's reads
+          // must have returned first, so an instruction that needs all of
+          // them (a branch that is never taken) stands before the barrier
+          {
+            uint32_t landed = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) landed ^= wg[j] ^ wu[j];
+            if (landed == 0x9e3779b9u && p.top_k < 0) sh->abort = sh->abort;
+          }
           __syncwarp();
           // the next input tiles of this warp: next chunk, or the first chunk
           // of the next tile
