@@ -393,8 +393,10 @@ void router_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, const f
                  const void* wt, void* ws, cudaStream_t s, bool term_in_rows) {
   const T* dxs = d.shared_hidden > 0 ? at<const T>(ws, L.dxs) : nullptr;
   const int64_t items = d.tokens * (d.d_model / (16 / (int)sizeof(T)));
+  // the whole device's wave: this sum runs after the shared expert's part
+  // (moe_backward_routed waits for it first), whatever the launch's SM limit
   auto launch = [&](auto kernel) {
-    const unsigned blocks = stream_grid(kernel, items, INT32_MAX);
+    const unsigned blocks = stream_grid(kernel, items, INT32_MAX, false);
     MOE_LAUNCH("router_dx", s,
                kernel<<<blocks, kThreads, 0, s>>>(
                    p.topk_idx, dsel, reinterpret_cast<const T*>(wt), at<const T>(ws, L.dxsort),

@@ -103,6 +103,35 @@ def test_train_step_is_deterministic(cfg):
         assert np.array_equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("name,shared_sms", [("decoder_bf16_16k", 0), ("decoder_bf16_16k", 48),
+                                             ("e8k2_bf16_32k", 0)])
+def test_repeated_train_steps_bit_identical(name, shared_sms):
+    # every kernel of the path is deterministic, so repeated train steps on
+    # the same inputs give the same bits; a race between a kernel's own
+    # stages (a buffer overwritten while still being read) shows up here as
+    # a difference between repeats, at sizes with hundreds of tiles per SM
+    from dropless_mixture_experts_gb300.synthetic import CONFIGS
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, cfg.dtype)
+    p = {k: dev[k] for k in params_of(inp)}
+    layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                     cfg.shared_hidden, cfg.dtype, train=True, shared_sms=shared_sms)
+    first = None
+    for _ in range(4):
+        loss, dx, grads = layer.train_step(dev["x"], p, dev["upstream"])
+        torch.cuda.synchronize()
+        cur = {"loss": loss.clone(), "dx": dx.clone(), "y": layer.y.clone()}
+        cur.update({k: v.clone() for k, v in grads.items() if v is not None})
+        if first is None:
+            first = cur
+            continue
+        for k, v in cur.items():
+            assert torch.equal(v, first[k]), k
+    assert layer.device_status()[0] == 0
+
+
 def _fed(cfg, logits):
     inp = make_inputs(cfg)
     dev = to_dev(inp, cfg.dtype)
