@@ -597,35 +597,39 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
     value = job_tokens_per_s(world, cfg.tokens, ms / 1e3)
     fwd_value = job_tokens_per_s(world, cfg.tokens, fms / 1e3)
 
-    # end to end through the public API with host buffers: H2D of the batch
-    # (x and the upstream gradient), D2H of the loss and of the input
-    # gradient dx inside the timed region (the layer's host-input step copies
-    # the upstream gradient on a side stream behind the forward pass); the
-    # weight gradients stay on the device for an optimizer step
-    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    dx_host = torch.empty(cfg.tokens, cfg.d_model, dtype=td).pin_memory()
+    # end to end through the public API with host buffers: every step's H2D
+    # of its batch (x and the upstream gradient) and D2H of its value and of
+    # the input gradient dx, in a pipelined sequence of steps (the copies of
+    # step i + 1's inputs and step i - 1's results run while step i computes);
+    # the weight gradients stay on the device for an optimizer step
+    loss_h = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(2)]
+    dx_h = [torch.empty(cfg.tokens, cfg.d_model, dtype=td).pin_memory() for _ in range(2)]
+    n_e2e = max(4, args.steps)
 
-    def e2e_step():
-        layer.train_step_from_host(host["x"], p, host["upstream"], loss_host, dx_host)
+    def e2e_steps(n):
+        layer.train_steps_from_host([host["x"]] * n, p, [host["upstream"]] * n,
+                                    [loss_h[i % 2] for i in range(n)],
+                                    [dx_h[i % 2] for i in range(n)])
 
-    e2e_step()  # first-call setup
-    run_e2e = layer.capture(e2e_step) if args.launch == "graph" else e2e_step
+    e2e_steps(2)  # first-call setup
     torch.cuda.synchronize()
     e2e_times = []
-    for _ in range(max(3, args.steps // 2)):
+    for _ in range(3):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        run_e2e()
+        e2e_steps(n_e2e)
         torch.cuda.synchronize()
-        e2e_times.append(time.perf_counter() - t0)
+        e2e_times.append((time.perf_counter() - t0) / n_e2e)
     e2e_s = statistics.median(e2e_times)
     h2d = host["x"].numel() * host["x"].element_size() * 2
-    d2h = loss_host.numel() * loss_host.element_size() + dx_host.numel() * dx_host.element_size()
+    d2h = loss_h[0].numel() * loss_h[0].element_size() + dx_h[0].numel() * dx_h[0].element_size()
     (e2e_s,) = max_over_ranks([e2e_s], "cuda")
     e2e = {"value": job_tokens_per_s(world, cfg.tokens, e2e_s), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "copies": "H2D x and the upstream gradient; D2H the loss and dx"}
+           "copies": "per step: H2D x and the upstream gradient, D2H the value and dx",
+           "steps": f"{n_e2e} pipelined steps of train_steps_from_host per timing (stream "
+                    "launches; each step's working set is larger than L2)"}
 
     # per-kernel device time and launch count of the forward and of the step
     # (stream launches with an event pair around each launch: a little

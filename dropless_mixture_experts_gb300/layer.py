@@ -250,6 +250,72 @@ class MoELayer:
             dx_host.copy_(self.dx, non_blocking=True)
         return self.loss, self.dx, self.grads
 
+    def train_steps_from_host(self, x_hosts, p, dy_hosts, loss_hosts=None, dx_hosts=None):
+        """Train steps on a sequence of batches in pinned host memory,
+        pipelined: while step i runs, the inputs of step i + 1 (x and the
+        upstream gradient) are copied in on one copy stream and the results
+        of step i - 1 (the value and dx, into ``loss_hosts[i - 1]`` [1] and
+        ``dx_hosts[i - 1]`` [T, d], each list optional) are copied out on
+        another.  Two device slots of the inputs, the value and dx alternate
+        between steps; a slot is refilled only after the step that read it
+        has finished.  Every step's results equal ``train_step``'s on the same
+        batch.  Returns after enqueuing (the current stream joins both copy
+        streams at the end): synchronize before reading the host buffers.
+        The weight gradients are those of the last step."""
+        if self.mode != abi.MOE_SAVE_FOR_BWD:
+            raise RuntimeError("layer was built with train=False")
+        n = len(x_hosts)
+        if n == 0 or len(dy_hosts) != n:
+            raise ValueError("one upstream gradient per batch")
+        if getattr(self, "slot_x", None) is None:
+            mk = lambda: torch.empty(self.T, self.d, dtype=self.tdtype, device=self.device)
+            self.slot_x = [mk(), mk()]
+            self.slot_dy = [mk(), mk()]
+            self.slot_dx = [self.dx, mk()]
+            self.slot_loss = [self.loss, torch.zeros_like(self.loss)]
+            self.h2d = torch.cuda.Stream(self.device)
+            self.d2h = torch.cuda.Stream(self.device)
+            self.slot_in = [torch.cuda.Event(), torch.cuda.Event()]
+            self.slot_done = [torch.cuda.Event(), torch.cuda.Event()]
+            self.slot_out = [torch.cuda.Event(), torch.cuda.Event()]
+        main = torch.cuda.current_stream(self.device)
+        self.h2d.wait_stream(main)  # earlier work on the slots has finished
+        self.d2h.wait_stream(main)
+
+        def load(i):
+            s = i % 2
+            with torch.cuda.stream(self.h2d):
+                if i >= 2:
+                    self.h2d.wait_event(self.slot_done[s])  # step i - 2 has read the slot
+                self.slot_x[s].copy_(x_hosts[i], non_blocking=True)
+                self.slot_dy[s].copy_(dy_hosts[i], non_blocking=True)
+                self.slot_in[s].record(self.h2d)
+
+        load(0)
+        try:
+            for i in range(n):
+                s = i % 2
+                if i + 1 < n:
+                    load(i + 1)
+                main.wait_event(self.slot_in[s])
+                if i >= 2:
+                    # the copies out of step i - 2 have read this slot's value and dx
+                    main.wait_event(self.slot_out[s])
+                self.dx, self.loss = self.slot_dx[s], self.slot_loss[s]
+                self.train_step(self.slot_x[s], p, self.slot_dy[s])
+                self.slot_done[s].record(main)
+                with torch.cuda.stream(self.d2h):
+                    self.d2h.wait_event(self.slot_done[s])
+                    if loss_hosts is not None:
+                        loss_hosts[i].copy_(self.loss, non_blocking=True)
+                    if dx_hosts is not None:
+                        dx_hosts[i].copy_(self.dx, non_blocking=True)
+                    self.slot_out[s].record(self.d2h)
+        finally:
+            main.wait_stream(self.h2d)
+            main.wait_stream(self.d2h)
+        return self.loss, self.dx, self.grads
+
     def capture(self, fn):
         """Records ``fn()`` -- a composed pass (``train_step``, ``forward``,
         ``train_step_from_host``) on fixed buffers -- into a CUDA graph and

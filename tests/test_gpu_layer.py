@@ -266,6 +266,45 @@ def test_train_step_from_host_matches_device_inputs():
             assert torch.equal(g2[k], v), k
 
 
+@pytest.mark.parametrize("shared_sms", [0, 48])
+def test_pipelined_host_steps_match_single_steps(shared_sms):
+    # the pipelined host-input steps (inputs of the next step copied in and
+    # results of the previous one copied out while a step runs, two device
+    # slots alternating) give each batch's single-step results bit for bit
+    cfg = MoEConfig(1500, 256, 256, 8, 2, 512, "bf16", "pipelined")
+    inp = make_inputs(cfg)
+    dev = to_dev(inp, "bf16")
+    p = {k: dev[k] for k in params_of(inp)}
+    from dropless_mixture_experts_gb300.layer import MoELayer
+    layer = MoELayer(cfg.tokens, cfg.d_model, cfg.d_hidden, cfg.experts, cfg.top_k,
+                     cfg.shared_hidden, "bf16", train=True, shared_sms=shared_sms)
+    n = 5
+    gen = torch.Generator().manual_seed(11)
+    xs = [(dev["x"].cpu().float() + 0.05 * i * torch.randn(dev["x"].shape, generator=gen))
+          .to(torch.bfloat16) for i in range(n)]
+    dys = [(dev["upstream"].cpu().float() * (1 + 0.1 * i)).to(torch.bfloat16) for i in range(n)]
+    refs = []
+    for i in range(n):
+        loss, dx, g = layer.train_step(xs[i].cuda(), p, dys[i].cuda())
+        torch.cuda.synchronize()
+        refs.append((loss.clone().cpu(), dx.clone().cpu(), g["dw_gate"].clone()))
+    xh = [x.pin_memory() for x in xs]
+    gh = [d.pin_memory() for d in dys]
+    lh = [torch.empty(1, dtype=torch.float32).pin_memory() for _ in range(n)]
+    dxh = [torch.empty(cfg.tokens, cfg.d_model, dtype=torch.bfloat16).pin_memory()
+           for _ in range(n)]
+    for _ in range(2):  # the second call reuses the slots
+        for t in lh + dxh:
+            t.zero_()
+        layer.train_steps_from_host(xh, p, gh, lh, dxh)
+        torch.cuda.synchronize()
+        for i in range(n):
+            assert torch.equal(lh[i], refs[i][0]), i
+            assert torch.equal(dxh[i], refs[i][1]), i
+        assert torch.equal(layer.grads["dw_gate"], refs[-1][2])
+    assert layer.device_status()[0] == 0
+
+
 def test_captured_train_step_replays_the_eager_results():
     # a CUDA graph of the train step (and of the host-input step) gives the
     # eager step's results bit for bit on every replay
