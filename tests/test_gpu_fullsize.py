@@ -35,6 +35,29 @@ def test_full_size_train_step(name):
     assert counts.max() / counts.sum() < 2.0 / cfg.experts
 
 
+@pytest.mark.parametrize("name", ["e8k2_bf16_32k", "decoder_bf16_16k"])
+def test_full_size_skewed_train_step(name):
+    # skewed routing (the router bias ramp of the bench's --skew 0.9) at a
+    # bench size: hot experts whose K ranges the weight-gradient schedule
+    # cuts into chunks (partials summed by the last chunk to finish), empty
+    # experts whose gradients must be exact zeros
+    import dataclasses
+    cfg = dataclasses.replace(CONFIGS[name], skew=0.9)
+    inp, layer, dev, res = run_layer(cfg, train=True)
+    assert res["status"] == 0
+    check_routing_bit_exact(res, cfg)
+    report = {}
+    errs = compare_layer(inp, res, cfg, train=True, report=report)
+    log_report(name + "/train_skew", report)
+    bad = {k: v for k, v in errs.items() if not v <= TOL[cfg.dtype]}
+    assert not bad, (name, errs)
+    counts = res["counts"]
+    assert counts.max() / counts.sum() > 2.0 / cfg.experts  # the routing is skewed
+    for k in ("dw_gate", "dw_up", "dw_down"):
+        for e in np.nonzero(counts == 0)[0]:
+            assert not np.any(res[k][e]), (k, e)
+
+
 @pytest.mark.parametrize("name", NAMES)
 def test_full_size_forward_only(name):
     # the forward-only mode (nothing saved for a backward) the forward
