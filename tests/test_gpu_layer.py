@@ -51,6 +51,11 @@ SMALL = [
     MoEConfig(2050, 256, 128, 64, 8, 256, "bf16", "bf16_decoder_skew", skew=0.9),
     MoEConfig(1000, 128, 64, 8, 2, 0, "f32", "f32_skew", skew=0.9),
     MoEConfig(2000, 128, 128, 8, 2, 0, "bf16", "bf16_skew_capacity", capacity=250, skew=0.9),
+    # degenerate routing: one expert (the layer is a dense SwiGLU MLP with
+    # gate 1), and two experts both taken by every token
+    MoEConfig(513, 128, 64, 1, 1, 0, "bf16", "bf16_one_expert"),
+    MoEConfig(513, 128, 64, 1, 1, 64, "f32", "f32_one_expert_shared"),
+    MoEConfig(700, 256, 128, 2, 2, 0, "bf16", "bf16_e2k2"),
 ]
 
 
