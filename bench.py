@@ -612,15 +612,22 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
                                     [dx_h[i % 2] for i in range(n)])
 
     e2e_steps(2)  # first-call setup
+    # graph mode: a CUDA graph of eight pipelined steps, replayed (the copies
+    # and the cross-stream events record into it like the kernels)
+    per_run = min(8, n_e2e) if args.launch == "graph" else n_e2e
+    runs = max(1, n_e2e // per_run)
+    run_steps = layer.capture(lambda: e2e_steps(per_run)) if args.launch == "graph" else \
+        (lambda: e2e_steps(per_run))
     torch.cuda.synchronize()
     e2e_times = []
     for _ in range(3):
         flush.zero_()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        e2e_steps(n_e2e)
+        for _ in range(runs):
+            run_steps()
         torch.cuda.synchronize()
-        e2e_times.append((time.perf_counter() - t0) / n_e2e)
+        e2e_times.append((time.perf_counter() - t0) / (runs * per_run))
     e2e_s = statistics.median(e2e_times)
     h2d = host["x"].numel() * host["x"].element_size() * 2
     d2h = loss_h[0].numel() * loss_h[0].element_size() + dx_h[0].numel() * dx_h[0].element_size()
@@ -628,8 +635,10 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
     e2e = {"value": job_tokens_per_s(world, cfg.tokens, e2e_s), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "copies": "per step: H2D x and the upstream gradient, D2H the value and dx",
-           "steps": f"{n_e2e} pipelined steps of train_steps_from_host per timing (stream "
-                    "launches; each step's working set is larger than L2)"}
+           "steps": f"{runs * per_run} steps of train_steps_from_host per timing, pipelined "
+                    f"in runs of {per_run}" + (" (each run a replayed CUDA graph)"
+                                               if args.launch == "graph" else "") +
+                    "; each step's working set is larger than L2"}
 
     # per-kernel device time and launch count of the forward and of the step
     # (stream launches with an event pair around each launch: a little
