@@ -307,6 +307,17 @@ def test_pipelined_host_steps_match_single_steps(shared_sms):
             assert torch.equal(lh[i], refs[i][0]), i
             assert torch.equal(dxh[i], refs[i][1]), i
         assert torch.equal(layer.grads["dw_gate"], refs[-1][2])
+    # a CUDA graph of the pipelined steps (copies and cross-stream events
+    # recorded with the kernels) replays the same results
+    replay = layer.capture(lambda: layer.train_steps_from_host(xh, p, gh, lh, dxh))
+    for _ in range(2):
+        for t in lh + dxh:
+            t.zero_()
+        replay()
+        torch.cuda.synchronize()
+        for i in range(n):
+            assert torch.equal(lh[i], refs[i][0]), i
+            assert torch.equal(dxh[i], refs[i][1]), i
     assert layer.device_status()[0] == 0
 
 
