@@ -107,9 +107,21 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   constexpr int R = TM / 16;   // micro-tile edge
   constexpr int U = TM / 64;   // 4 x 4 blocks per micro-tile edge; loads per thread per operand
 
-  __shared__ __align__(16) float As[BK][TM + 4];
-  __shared__ __align__(16) float Bs[BK][TM + 4];
-  __shared__ __align__(16) float Bs2[DUAL ? BK : 1][DUAL ? TM + 4 : 4];
+  // the operand tiles in dynamic shared memory; the weight-gradient and dZ
+  // kinds keep two buffers of each (the next K step's tile is stored into
+  // one while the other is read: one barrier per K step), the others one
+  // (measured faster for them)
+  constexpr int NB = (KIND == DWD || KIND == DWGU || KIND == DZ) ? 2 : 1;
+  typedef float Tile_[BK][TM + 4];
+  // one buffer: static arrays (fixed addresses); two: dynamic shared memory
+  constexpr int SR = NB == 1 ? BK : 1, SC = NB == 1 ? TM + 4 : 4;
+  __shared__ __align__(16) float As1[SR][SC];
+  __shared__ __align__(16) float Bs1[SR][SC];
+  __shared__ __align__(16) float Bs21[DUAL && NB == 1 ? BK : 1][DUAL && NB == 1 ? TM + 4 : 4];
+  extern __shared__ __align__(16) float simt_smem[];
+  Tile_* As = NB == 1 ? reinterpret_cast<Tile_*>(&As1[0][0]) : reinterpret_cast<Tile_*>(simt_smem);
+  Tile_* Bs = NB == 1 ? reinterpret_cast<Tile_*>(&Bs1[0][0]) : As + NB;
+  Tile_* Bs2 = NB == 1 ? reinterpret_cast<Tile_*>(&Bs21[0][0]) : Bs + NB;  // DUAL only
   __shared__ int s_tok[TM];  // source rows of the tile (row kinds)
 
   const int tid = threadIdx.x;
@@ -225,47 +237,61 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       }
     }
   };
-  auto sstore = [&]() {
+  auto sstore = [&](int buf) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       if constexpr (A_KCONTIG) {
         const int m = tid / 4 + 64 * u, k4 = (tid % 4) * 4;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) As[k4 + q][m] = comp(ra[u], q);
+        for (int q = 0; q < 4; ++q) As[buf][k4 + q][m] = comp(ra[u], q);
       } else {
         const int kl = tid / 16, m4 = (tid % 16) * 4 + 64 * u;
-        *reinterpret_cast<float4*>(&As[kl][m4]) = ra[u];
+        *reinterpret_cast<float4*>(&As[buf][kl][m4]) = ra[u];
       }
       if constexpr (!B_KCONTIG) {
         const int kl = tid / 16, n4 = (tid % 16) * 4 + 64 * u;
-        *reinterpret_cast<float4*>(&Bs[kl][n4]) = rb[u];
-        if constexpr (DUAL) *reinterpret_cast<float4*>(&Bs2[kl][n4]) = rb2[u];
+        *reinterpret_cast<float4*>(&Bs[buf][kl][n4]) = rb[u];
+        if constexpr (DUAL) *reinterpret_cast<float4*>(&Bs2[buf][kl][n4]) = rb2[u];
       } else {
         const int n = tid / 4 + 64 * u, k4 = (tid % 4) * 4;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) Bs[k4 + q][n] = comp(rb[u], q);
+        for (int q = 0; q < 4; ++q) Bs[buf][k4 + q][n] = comp(rb[u], q);
       }
     }
   };
 
   const int64_t klen = kend - kbeg;
-  if (klen > 0) gload(0);
+  int cur = 0;
+  if constexpr (NB == 2) {
+    if (klen > 0) {
+      gload(0);
+      sstore(0);
+    }
+    __syncthreads();
+  } else {
+    if (klen > 0) gload(0);
+  }
   for (int64_t kt = 0; kt < klen; kt += BK) {
-    __syncthreads();
-    sstore();
-    __syncthreads();
-    if (kt + BK < klen) gload(kt + BK);
+    // the next K step's operands: global loads now, their shared-memory
+    // stores after this step's FMAs (two buffers) or before them (one)
+    const bool more = kt + BK < klen;
+    if constexpr (NB == 1) {
+      __syncthreads();
+      sstore(0);
+      __syncthreads();
+    }
+    if (more) gload(kt + BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float am[R], bn[R], bn2[DUAL ? R : 1];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const float4 av = *reinterpret_cast<const float4*>(&As[kk][ty * 4 + 64 * u]);
-        const float4 bv = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4 + 64 * u]);
+        const float4 av = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4 + 64 * u]);
+        const float4 bv = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4 + 64 * u]);
         am[4 * u] = av.x; am[4 * u + 1] = av.y; am[4 * u + 2] = av.z; am[4 * u + 3] = av.w;
         bn[4 * u] = bv.x; bn[4 * u + 1] = bv.y; bn[4 * u + 2] = bv.z; bn[4 * u + 3] = bv.w;
         if constexpr (DUAL) {
-          const float4 b2 = *reinterpret_cast<const float4*>(&Bs2[kk][tx * 4 + 64 * u]);
+          const float4 b2 = *reinterpret_cast<const float4*>(&Bs2[cur][kk][tx * 4 + 64 * u]);
           bn2[4 * u] = b2.x; bn2[4 * u + 1] = b2.y; bn2[4 * u + 2] = b2.z; bn2[4 * u + 3] = b2.w;
         }
       }
@@ -279,6 +305,11 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 #pragma unroll
           for (int j = 0; j < R; ++j) acc2[i][j] = fmaf(am[i], bn2[j], acc2[i][j]);
       }
+    }
+    if constexpr (NB == 2) {
+      if (more) sstore(cur ^ 1);
+      __syncthreads();  // the other buffer is full; every thread has left this one
+      cur ^= 1;
     }
   }
 
@@ -382,6 +413,25 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 // `blocks` counts 64 x 64 tiles; with a.tm = 128 each block takes a
 // 128 x 128 tile (a quarter as many blocks; the routed row kinds, whose tile
 // list holds 128-row entries, half as many per column tile)
+// dynamic shared memory of a kernel instance: the two buffers of A and B of
+// the double-buffered kinds (the others keep static tiles)
+template <Kind KIND, int TM>
+constexpr size_t simt_smem_bytes() {
+  return (KIND == DWD || KIND == DWGU || KIND == DZ) ? sizeof(float) * BK * (TM + 4) * 2 * 2 : 0;
+}
+
+template <Kind KIND, typename T, bool ROUTED, int TM>
+void launch_tm(const SimtArgs& a, int64_t blocks, const char* name, cudaStream_t s) {
+  constexpr size_t smem = simt_smem_bytes<KIND, TM>();
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(simt_gemm_kernel<KIND, T, ROUTED, TM>,
+                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    attr = true;
+  }
+  MOE_LAUNCH(name, s, simt_gemm_kernel<KIND, T, ROUTED, TM><<<(unsigned)blocks, NT, smem, s>>>(a));
+}
+
 template <Kind KIND, typename T, bool ROUTED>
 void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
   if (blocks <= 0) return;
@@ -391,11 +441,9 @@ void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
       {"simt_logits", "simt_gateup", "simt_down", "simt_dz", "simt_dx", "simt_dw_down",
        "simt_dw_gateup"}};
   if (a.tm == 128)
-    MOE_LAUNCH(names[ROUTED ? 1 : 0][KIND], s,
-               simt_gemm_kernel<KIND, T, ROUTED, 128><<<(unsigned)blocks, NT, 0, s>>>(a));
+    launch_tm<KIND, T, ROUTED, 128>(a, blocks, names[ROUTED ? 1 : 0][KIND], s);
   else
-    MOE_LAUNCH(names[ROUTED ? 1 : 0][KIND], s,
-               simt_gemm_kernel<KIND, T, ROUTED, 64><<<(unsigned)blocks, NT, 0, s>>>(a));
+    launch_tm<KIND, T, ROUTED, 64>(a, blocks, names[ROUTED ? 1 : 0][KIND], s);
 }
 
 template <typename T>
