@@ -137,6 +137,25 @@ def test_repeated_train_steps_bit_identical(name, shared_sms):
     assert layer.device_status()[0] == 0
 
 
+@pytest.mark.parametrize("E,k", [(8, 2), (32, 4), (64, 8)])
+def test_tensor_core_router_ties(E, k):
+    # duplicated router columns give bit-equal logits (each output column of
+    # the router GEMM is accumulated alone), so the tensor-core router's
+    # selection meets exact ties: the lower expert index must win, and the
+    # selection must equal the oracle's on the device's own logits
+    cfg = MoEConfig(1500, 256, 128, E, k, 0, "bf16", f"router_ties_E{E}_k{k}")
+    inp = make_inputs(cfg)
+    w = inp["w_router"].copy()
+    for e in range(0, E - 1, 3):
+        w[:, e + 1] = w[:, e]
+    inp["w_router"] = w
+    _, _, _, res = run_layer(cfg, inputs=inp)
+    assert res["status"] == 0
+    lg = res["logits"]
+    assert any(np.array_equal(lg[:, e], lg[:, e + 1]) for e in range(0, E - 1, 3))
+    check_routing_bit_exact(res, cfg)
+
+
 def _fed(cfg, logits):
     inp = make_inputs(cfg)
     dev = to_dev(inp, cfg.dtype)
