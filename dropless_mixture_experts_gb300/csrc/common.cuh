@@ -21,6 +21,7 @@ constexpr int kMaxTopK = 32;
 constexpr int kLossBlocks = 2048;  // fixed partial count of the loss reduction
 constexpr int kRouterBwdRanges = 608;  // max token ranges of the router-weight gradient partials
 constexpr int kRouterBwdSmem = 200 * 1024;  // router backward: W_r^T + dW_r partial in shared memory
+constexpr int kSimtMaxSplit = 8;  // most K chunks of a strict-float32 weight-gradient GEMM
 
 // ---- element access ---------------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -206,6 +207,11 @@ inline Layout make_layout(const moe_dims& d, int mode) {
       pfs = std::max(pfs, need(1, dm, 2 * hs, pick_bn((int)hs), false));
     }
     pf = std::max(pf, (int64_t)router_dw_split_bound((dm + 127) / 128) * dm * 64);
+    if (d.dtype != MOE_BF16) {
+      // the strict-float32 weight gradients' K-chunk partials [chunk][E * M][N]
+      pf = std::max(pf, (int64_t)kSimtMaxSplit * E * std::max(h * dm, dm * 2 * h));
+      if (hs > 0) pfs = std::max(pfs, (int64_t)kSimtMaxSplit * std::max(hs * dm, dm * 2 * hs));
+    }
     L.dwpart = take(sizeof(float) * pf);
     L.dwpart_sh = take(sizeof(float) * pfs);
     L.dw_tick_n = std::max(E * ((h + 127) / 128) * (dm / pick_bn((int)dm)),

@@ -17,6 +17,8 @@
 // expert.  The method these follow: the experts_grouped_swiglu and
 // unpermute_combine pieces of kernel_gmm_gpu.json and the value_and_grad
 // train step of gpu_moe_h100.json.
+#include <cmath>
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -65,6 +67,13 @@ struct SimtArgs {
   int ldo = 0;
   int n_ntiles = 1, n_mtiles = 1;
   int tm = 64;                   // tile edge: 64, or 128 where the dimensions divide
+  // DW kinds: each expert's K range cut into ksplit chunks of whole K steps
+  // (more blocks, so that the last wave of tiles is nearly full); chunk s
+  // writes its partial tile to part + s * part_sstride, rows e * M + m, row
+  // stride n_ntiles * TM, summed afterwards in chunk order
+  int ksplit = 1;
+  float* part = nullptr;
+  int64_t part_sstride = 0;
 };
 
 template <typename T>
@@ -86,6 +95,20 @@ __device__ __forceinline__ float load1(const T* p, bool ok) {
   return ok ? to_f32(*p) : 0.f;
 }
 
+// four consecutive elements (16 bytes of float, 8 of bf16; 4-element aligned)
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+  } else {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+    uint2 u;
+    u.x = *reinterpret_cast<uint32_t*>(&lo);
+    u.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+}
+
 __device__ __forceinline__ float comp(const float4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
@@ -98,7 +121,7 @@ __device__ __forceinline__ float comp(const float4& v, int q) {
 // The 8 x 8 micro-tile issues 64 FFMAs per 4 float4 loads of each k step,
 // the 4 x 4 one 16 per 2.
 template <Kind KIND, typename T, bool ROUTED, int TM>
-__global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
+__device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
   constexpr bool A_KCONTIG = (KIND == LOGITS || KIND == GU || KIND == DOWN || KIND == DZ ||
                               KIND == DX);
   constexpr bool B_KCONTIG = (KIND == DZ || KIND == DX);
@@ -133,6 +156,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   int64_t row0 = 0;     // first output row (row kinds) / first K row (DW kinds)
   int nvalid = 0;       // row kinds: valid rows in this tile
   int m0 = 0;           // DW kinds: first output row
+  int chunk = 0;        // DW kinds: chunk of the expert's K range
   int64_t kbeg = 0, kend = 0;
 
   if constexpr (!DW) {
@@ -164,16 +188,26 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
     kbeg = 0;
     kend = a.K;
   } else {
+    // blocks in the order (expert, chunk, row tile, column tile): the
+    // blocks that run together read the same K rows
     const int mt = rest % a.n_mtiles;
-    e = rest / a.n_mtiles;
+    const int es = rest / a.n_mtiles;
+    e = es / a.ksplit;
+    chunk = es % a.ksplit;
     m0 = mt * TM;
+    int64_t k0, n;
     if constexpr (ROUTED) {
-      kbeg = a.poff[e];
-      kend = kbeg + a.counts[e];
+      k0 = a.poff[e];
+      n = a.counts[e];
     } else {
-      kbeg = 0;
-      kend = a.rows;
+      k0 = 0;
+      n = a.rows;
     }
+    const int64_t steps = (n + BK - 1) / BK;
+    kbeg = k0 + BK * (steps * chunk / a.ksplit);
+    kend = k0 + BK * (steps * (chunk + 1) / a.ksplit);
+    if (kend > k0 + n) kend = k0 + n;
+    if (kend < kbeg) kend = kbeg;
   }
   __syncthreads();
 
@@ -185,6 +219,16 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   float acc2[DUAL ? R : 1][DUAL ? R : 1] = {};
   const int ty = tid / 16, tx = tid % 16;
 
+  // routed DW kinds gather token rows along K: this thread's K row (the same
+  // for A and B) maps to its token through rowpair, read one K step before
+  // the operand loads that use it
+  constexpr bool GATHER_K = DW && ROUTED;
+  int64_t ktok = 0;      // token row of the step being loaded
+  int32_t pair_next = 0; // rowpair entry of the step after it
+  auto kpair = [&](int64_t kt) -> int32_t {
+    const int64_t r = kbeg + kt + tid / 16;
+    return r < kend ? __ldg(a.rowpair + r) : 0;
+  };
   float4 ra[U], rb[U], rb2[DUAL ? U : 1];
   auto gload = [&](int64_t kt) {
 #pragma unroll
@@ -200,8 +244,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
         const int kl = tid / 16, m4 = (tid % 16) * 4 + 64 * u;
         const int64_t r = kbeg + kt + kl;
         const bool ok = r < kend;
-        int64_t src = r;
-        if (KIND == DWGU && ROUTED && ok) src = a.rowpair[r] / a.top_k;
+        const int64_t src = KIND == DWGU && ROUTED ? ktok : r;
         ra[u] = load4(A + src * a.lda + m0 + m4, ok);
       }
       // ---- B ----
@@ -216,8 +259,7 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
         } else if constexpr (DW) {
           const int64_t r = kbeg + kt + kl;
           const bool ok = r < kend;
-          int64_t src = r;
-          if (KIND == DWD && ROUTED && ok) src = a.rowpair[r] / a.top_k;
+          const int64_t src = KIND == DWD && ROUTED ? ktok : r;
           rb[u] = load4(B + src * a.ldb + n0 + n4, ok);
         } else {
           const int64_t kk = kt + kl;
@@ -262,6 +304,12 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 
   const int64_t klen = kend - kbeg;
   int cur = 0;
+  if constexpr (GATHER_K) {
+    if (klen > 0) {
+      ktok = kpair(0) / a.top_k;
+      pair_next = kpair(BK);
+    }
+  }
   if constexpr (NB == 2) {
     if (klen > 0) {
       gload(0);
@@ -280,7 +328,13 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       sstore(0);
       __syncthreads();
     }
-    if (more) gload(kt + BK);
+    if (more) {
+      if constexpr (GATHER_K) {
+        ktok = pair_next / a.top_k;
+        pair_next = kpair(kt + 2 * BK);
+      }
+      gload(kt + BK);
+    }
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float am[R], bn[R], bn2[DUAL ? R : 1];
@@ -315,7 +369,8 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
 
   // ---------------- epilogues ----------------
   // micro-tile element (i, j): row ty*4 + (i % 4) + 64*(i / 4), column
-  // tx*4 + (j % 4) + 64*(j / 4) of the tile
+  // tx*4 + (j % 4) + 64*(j / 4) of the tile; the four columns of a j block
+  // are consecutive and move as one vector
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     const int m = ty * 4 + (i & 3) + 64 * (i >> 2);
@@ -333,16 +388,21 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       T* AG = reinterpret_cast<T*>(a.ag_out);
       T* AU = reinterpret_cast<T*>(a.au_out);
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
+      for (int jb = 0; jb < U; ++jb) {
+        const int64_t o = r * a.ldo + n0 + tx * 4 + 64 * jb;
         // round to the storage type first, so H is computed from exactly the
         // values a backward pass reads back
-        const float g = to_f32(from_f32<T>(acc[i][j]));
-        const float u = to_f32(from_f32<T>(acc2[i][j]));
-        H[r * a.ldo + n] = from_f32<T>(g * sigmoidf_(g) * u);
+        float g[4], u[4], hv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          g[c] = to_f32(from_f32<T>(acc[i][4 * jb + c]));
+          u[c] = to_f32(from_f32<T>(acc2[i][4 * jb + c]));
+          hv[c] = g[c] * sigmoidf_(g[c]) * u[c];
+        }
+        store4(H + o, hv[0], hv[1], hv[2], hv[3]);
         if (AG) {
-          AG[r * a.ldo + n] = from_f32<T>(g);
-          AU[r * a.ldo + n] = from_f32<T>(u);
+          store4(AG + o, g[0], g[1], g[2], g[3]);
+          store4(AU + o, u[0], u[1], u[2], u[3]);
         }
       }
     } else if constexpr (KIND == DOWN || KIND == DX) {
@@ -391,23 +451,48 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
       for (int o = 8; o > 0; o >>= 1) dgp += __shfl_xor_sync(0xffffffffu, dgp, o);
       if (ROUTED && tx == 0 && valid)
         a.dg_part[(int64_t)a.rowpair[r] * a.dg_ld + ntile] = gt * dgp;
-    } else {  // DWD / DWGU: plain stores of the expert's gradient tile
+    } else {  // DWD / DWGU: the expert's gradient tile, or a K chunk's partial of it
       const int64_t om = m0 + m;
       const int64_t eoff = (int64_t)e * a.n_mtiles * TM;  // expert offset in rows
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
-        if constexpr (KIND == DWGU) {
-          if (n < a.h)
-            a.acc_out[(eoff + om) * a.h + n] = acc[i][j];
-          else
-            a.acc_out2[(eoff + om) * a.h + (n - a.h)] = acc[i][j];
+      for (int jb = 0; jb < U; ++jb) {
+        const int n = n0 + tx * 4 + 64 * jb;
+        float* dst;
+        if (a.ksplit > 1) {
+          dst = a.part + chunk * a.part_sstride + (eoff + om) * ((int64_t)a.n_ntiles * TM) + n;
+        } else if constexpr (KIND == DWGU) {
+          // a 4-column block never straddles the gate | up boundary (h % 4 == 0)
+          dst = n < a.h ? a.acc_out + (eoff + om) * a.h + n
+                        : a.acc_out2 + (eoff + om) * a.h + (n - a.h);
         } else {
-          a.acc_out[(eoff + om) * a.ldo + n] = acc[i][j];
+          dst = a.acc_out + (eoff + om) * a.ldo + n;
         }
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[i][4 * jb], acc[i][4 * jb + 1],
+                                                      acc[i][4 * jb + 2], acc[i][4 * jb + 3]);
       }
     }
   }
+}
+
+// The kernels: the weight-gradient kinds and dX keep two 128-wide (four
+// 64-wide) tiles resident per SM (at most 128 / 64 registers a thread:
+// measured 0.63 -> 0.68 of the FFMA rate for dX at 131072 tokens); the
+// other kinds take the registers the compiler gives them (the routed down
+// projection and dZ already fit two, the gate/up projection's two
+// accumulator sets do not).
+template <Kind KIND, typename T, bool ROUTED, int TM>
+__global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
+  simt_gemm_body<KIND, T, ROUTED, TM>(a);
+}
+template <Kind KIND, typename T, bool ROUTED, int TM>
+__global__ void __launch_bounds__(NT, TM == 64 ? 4 : 2) simt_gemm2_kernel(const SimtArgs a) {
+  simt_gemm_body<KIND, T, ROUTED, TM>(a);
+}
+template <Kind KIND, typename T, bool ROUTED, int TM>
+constexpr auto simt_kernel() {
+  if constexpr (KIND == DWD || KIND == DWGU || KIND == DX)
+    return simt_gemm2_kernel<KIND, T, ROUTED, TM>;
+  else return simt_gemm_kernel<KIND, T, ROUTED, TM>;
 }
 
 // `blocks` counts 64 x 64 tiles; with a.tm = 128 each block takes a
@@ -425,11 +510,49 @@ void launch_tm(const SimtArgs& a, int64_t blocks, const char* name, cudaStream_t
   constexpr size_t smem = simt_smem_bytes<KIND, TM>();
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(simt_gemm_kernel<KIND, T, ROUTED, TM>,
+    cudaFuncSetAttribute(simt_kernel<KIND, T, ROUTED, TM>(),
                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     attr = true;
   }
-  MOE_LAUNCH(name, s, simt_gemm_kernel<KIND, T, ROUTED, TM><<<(unsigned)blocks, NT, smem, s>>>(a));
+  MOE_LAUNCH(name, s, simt_kernel<KIND, T, ROUTED, TM>()<<<(unsigned)blocks, NT, smem, s>>>(a));
+}
+
+// Blocks of a kernel instance resident on one SM times the device's SMs
+// (the device's, not the launch limit's: the K chunks a weight gradient is
+// cut into, and so its summation order, depend on this number alone).
+template <Kind KIND, typename T, bool ROUTED, int TM>
+int64_t resident_slots() {
+  static int64_t slots = 0;
+  if (!slots) {
+    int dev = 0, sms = 0, per = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, simt_kernel<KIND, T, ROUTED, TM>(), NT,
+                                                  simt_smem_bytes<KIND, TM>());
+    slots = (int64_t)(sms > 0 ? sms : 1) * (per > 0 ? per : 1);
+  }
+  return slots;
+}
+
+// K chunks for a weight-gradient GEMM of `tiles` output tiles whose experts
+// hold about `krows` rows each: the count (<= kSimtMaxSplit, chunks of at
+// least 256 rows) whose blocks fill their last wave of `slots` best; more
+// chunks only where that gains at least 2 % (each adds a partial tile).
+inline int dw_chunks(int64_t tiles, int64_t krows, int64_t slots) {
+  auto fill = [&](int c) {
+    const double w = (double)(tiles * c) / (double)slots;
+    return w / std::ceil(w);
+  };
+  int best = 1;
+  double best_fill = fill(1);
+  for (int c = 2; c <= kSimtMaxSplit && krows / c >= 256; ++c) {
+    const double f = fill(c);
+    if (f > best_fill + 0.02) {
+      best = c;
+      best_fill = f;
+    }
+  }
+  return best;
 }
 
 template <Kind KIND, typename T, bool ROUTED>
@@ -444,6 +567,29 @@ void launch(const SimtArgs& a, int64_t blocks, cudaStream_t s) {
     launch_tm<KIND, T, ROUTED, 128>(a, blocks, names[ROUTED ? 1 : 0][KIND], s);
   else
     launch_tm<KIND, T, ROUTED, 64>(a, blocks, names[ROUTED ? 1 : 0][KIND], s);
+}
+
+// A weight-gradient GEMM (DWD / DWGU) of `tiles` output tiles over
+// experts of about `krows` rows: cut into K chunks where that fills the
+// GPU's last wave better, the chunks' partial tiles (in `part`, room for
+// kSimtMaxSplit of them) then summed in chunk order into the outputs.
+template <Kind KIND, typename T, bool ROUTED>
+void launch_dw(SimtArgs a, int64_t tiles, int64_t krows, float* part, cudaStream_t s) {
+  if (tiles <= 0) return;
+  const int64_t slots = a.tm == 128 ? resident_slots<KIND, T, ROUTED, 128>()
+                                    : resident_slots<KIND, T, ROUTED, 64>();
+  const int c = dw_chunks(tiles, krows, slots);
+  const int64_t M = (int64_t)a.n_mtiles * a.tm, N = (int64_t)a.n_ntiles * a.tm;
+  const int64_t EM = tiles / ((int64_t)a.n_mtiles * a.n_ntiles) * M;
+  if (c > 1) {
+    a.ksplit = c;
+    a.part = part;
+    a.part_sstride = EM * N;
+  }
+  launch<KIND, T, ROUTED>(a, tiles * c, s);
+  if (c > 1)
+    launch_split_reduce(part, c, EM, (int)N, (int)N, KIND == DWGU ? a.h : 0, a.acc_out,
+                        KIND == DWGU ? a.acc_out2 : nullptr, s);
 }
 
 template <typename T>
@@ -595,7 +741,8 @@ void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
     w.tm = tile_of(dm, hs);
     w.n_mtiles = hs / w.tm;
     w.n_ntiles = dm / w.tm;
-    launch<DWD, T, false>(w, (int64_t)w.n_ntiles * w.n_mtiles, s);
+    launch_dw<DWD, T, false>(w, (int64_t)w.n_ntiles * w.n_mtiles, d.tokens,
+                             at<float>(ws, L.dwpart_sh), s);
     SimtArgs g;
     g.rows = d.tokens;
     g.A = p.x;
@@ -608,7 +755,8 @@ void backward_shared_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
     g.tm = tile_of(2 * hs, dm);
     g.n_mtiles = dm / g.tm;
     g.n_ntiles = 2 * hs / g.tm;
-    launch<DWGU, T, false>(g, (int64_t)g.n_ntiles * g.n_mtiles, s);
+    launch_dw<DWGU, T, false>(g, (int64_t)g.n_ntiles * g.n_mtiles, d.tokens,
+                              at<float>(ws, L.dwpart_sh), s);
   }
 }
 
@@ -672,7 +820,9 @@ void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
   w.tm = tile_of(dm, h);
   w.n_mtiles = h / w.tm;
   w.n_ntiles = dm / w.tm;
-  launch<DWD, T, true>(w, (int64_t)w.n_ntiles * w.n_mtiles * E, s);
+  const int64_t krows = d.tokens * (int64_t)d.top_k / E;  // rows of an expert on average
+  launch_dw<DWD, T, true>(w, (int64_t)w.n_ntiles * w.n_mtiles * E, krows,
+                          at<float>(ws, L.dwpart), s);
 
   SimtArgs g = base;
   g.A = p.x;
@@ -685,7 +835,8 @@ void backward_routed_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, v
   g.tm = tile_of(2 * h, dm);
   g.n_mtiles = dm / g.tm;
   g.n_ntiles = 2 * h / g.tm;
-  launch<DWGU, T, true>(g, (int64_t)g.n_ntiles * g.n_mtiles * E, s);
+  launch_dw<DWGU, T, true>(g, (int64_t)g.n_ntiles * g.n_mtiles * E, krows,
+                           at<float>(ws, L.dwpart), s);
 }
 
 }  // namespace

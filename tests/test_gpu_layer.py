@@ -56,6 +56,11 @@ SMALL = [
     MoEConfig(513, 128, 64, 1, 1, 0, "bf16", "bf16_one_expert"),
     MoEConfig(513, 128, 64, 1, 1, 64, "f32", "f32_one_expert_shared"),
     MoEConfig(700, 256, 128, 2, 2, 0, "bf16", "bf16_e2k2"),
+    # float32 weight gradients cut into K chunks (experts of 1024-2048 rows
+    # over few output tiles: up to eight chunks, summed in chunk order), with
+    # a shared expert, and with skewed routing (empty experts: empty chunks)
+    MoEConfig(4096, 128, 128, 4, 2, 128, "f32", "f32_dw_chunks_shared"),
+    MoEConfig(4096, 128, 64, 8, 2, 0, "f32", "f32_dw_chunks_skew", skew=0.9),
 ]
 
 
@@ -109,7 +114,7 @@ def test_train_step_is_deterministic(cfg):
 
 
 @pytest.mark.parametrize("name,shared_sms", [("decoder_bf16_16k", 0), ("decoder_bf16_16k", 48),
-                                             ("e8k2_bf16_32k", 0)])
+                                             ("e8k2_bf16_32k", 0), ("e8k2_f32_4k", 0)])
 def test_repeated_train_steps_bit_identical(name, shared_sms):
     # every kernel of the path is deterministic, so repeated train steps on
     # the same inputs give the same bits; a race between a kernel's own
