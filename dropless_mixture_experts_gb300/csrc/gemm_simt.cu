@@ -31,6 +31,8 @@ constexpr int BK = 16, NT = 256;
 // The tile edge of a GEMM whose output has N columns and (weight
 // gradients) M rows: 128 where both divide, else 64.
 inline int tile_of(int64_t N, int64_t M = 128) { return N % 128 == 0 && M % 128 == 0 ? 128 : 64; }
+// Columns of W_gate (and of W_up) per gate/up tile of `tm` rows.
+inline int gu_cols(int tm) { return tm == 128 ? 64 : tm; }
 
 struct SimtArgs {
   // operands
@@ -129,6 +131,11 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
   constexpr bool DW = (KIND == DWD || KIND == DWGU);
   constexpr int R = TM / 16;   // micro-tile edge
   constexpr int U = TM / 64;   // 4 x 4 blocks per micro-tile edge; loads per thread per operand
+  // the tile's column extent: the gate/up projection's 128-row tiles take 64
+  // columns of each of its two weight matrices (two 8 x 4 accumulator sets
+  // per thread, so that two blocks fit an SM); every other tile is square
+  constexpr int TN = DUAL && TM == 128 ? 64 : TM;
+  constexpr int RN = TN / 16, UN = TN / 64;  // micro-tile columns; B loads per thread
 
   // the operand tiles in dynamic shared memory; the weight-gradient and dZ
   // kinds keep two buffers of each (the next K step's tile is stored into
@@ -150,7 +157,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
   const int tid = threadIdx.x;
   const int ntile = blockIdx.x % a.n_ntiles;
   const int rest = blockIdx.x / a.n_ntiles;
-  const int n0 = ntile * TM;
+  const int n0 = ntile * TN;
 
   int e = 0;
   int64_t row0 = 0;     // first output row (row kinds) / first K row (DW kinds)
@@ -215,8 +222,8 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
   const T* B = reinterpret_cast<const T*>(a.B) + (ROUTED ? a.b_estride * e : 0);
   const T* B2 = a.B2 ? reinterpret_cast<const T*>(a.B2) + (ROUTED ? a.b_estride * e : 0) : nullptr;
 
-  float acc[R][R] = {};
-  float acc2[DUAL ? R : 1][DUAL ? R : 1] = {};
+  float acc[R][RN] = {};
+  float acc2[DUAL ? R : 1][DUAL ? RN : 1] = {};
   const int ty = tid / 16, tx = tid % 16;
 
   // routed DW kinds gather token rows along K: this thread's K row (the same
@@ -229,7 +236,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
     const int64_t r = kbeg + kt + tid / 16;
     return r < kend ? __ldg(a.rowpair + r) : 0;
   };
-  float4 ra[U], rb[U], rb2[DUAL ? U : 1];
+  float4 ra[U], rb[UN], rb2[DUAL ? UN : 1];
   auto gload = [&](int64_t kt) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -248,6 +255,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
         ra[u] = load4(A + src * a.lda + m0 + m4, ok);
       }
       // ---- B ----
+      if (u >= UN) continue;
       if constexpr (!B_KCONTIG) {
         const int kl = tid / 16, n4 = (tid % 16) * 4 + 64 * u;
         if constexpr (KIND == LOGITS) {
@@ -290,6 +298,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
         const int kl = tid / 16, m4 = (tid % 16) * 4 + 64 * u;
         *reinterpret_cast<float4*>(&As[buf][kl][m4]) = ra[u];
       }
+      if (u >= UN) continue;
       if constexpr (!B_KCONTIG) {
         const int kl = tid / 16, n4 = (tid % 16) * 4 + 64 * u;
         *reinterpret_cast<float4*>(&Bs[buf][kl][n4]) = rb[u];
@@ -337,12 +346,13 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
     }
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
-      float am[R], bn[R], bn2[DUAL ? R : 1];
+      float am[R], bn[RN], bn2[DUAL ? RN : 1];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const float4 av = *reinterpret_cast<const float4*>(&As[cur][kk][ty * 4 + 64 * u]);
-        const float4 bv = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4 + 64 * u]);
         am[4 * u] = av.x; am[4 * u + 1] = av.y; am[4 * u + 2] = av.z; am[4 * u + 3] = av.w;
+        if (u >= UN) continue;
+        const float4 bv = *reinterpret_cast<const float4*>(&Bs[cur][kk][tx * 4 + 64 * u]);
         bn[4 * u] = bv.x; bn[4 * u + 1] = bv.y; bn[4 * u + 2] = bv.z; bn[4 * u + 3] = bv.w;
         if constexpr (DUAL) {
           const float4 b2 = *reinterpret_cast<const float4*>(&Bs2[cur][kk][tx * 4 + 64 * u]);
@@ -352,12 +362,12 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
 #pragma unroll
       for (int i = 0; i < R; ++i)
 #pragma unroll
-        for (int j = 0; j < R; ++j) acc[i][j] = fmaf(am[i], bn[j], acc[i][j]);
+        for (int j = 0; j < RN; ++j) acc[i][j] = fmaf(am[i], bn[j], acc[i][j]);
       if constexpr (DUAL) {
 #pragma unroll
         for (int i = 0; i < R; ++i)
 #pragma unroll
-          for (int j = 0; j < R; ++j) acc2[i][j] = fmaf(am[i], bn2[j], acc2[i][j]);
+          for (int j = 0; j < RN; ++j) acc2[i][j] = fmaf(am[i], bn2[j], acc2[i][j]);
       }
     }
     if constexpr (NB == 2) {
@@ -378,7 +388,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
     if constexpr (KIND == LOGITS) {
       if (r < a.rows)
 #pragma unroll
-        for (int j = 0; j < R; ++j) {
+        for (int j = 0; j < RN; ++j) {
           const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
           if (n < a.N) a.acc_out[r * a.ldo + n] = acc[i][j] + (a.col_bias ? a.col_bias[n] : 0.f);
         }
@@ -388,7 +398,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
       T* AG = reinterpret_cast<T*>(a.ag_out);
       T* AU = reinterpret_cast<T*>(a.au_out);
 #pragma unroll
-      for (int jb = 0; jb < U; ++jb) {
+      for (int jb = 0; jb < UN; ++jb) {
         const int64_t o = r * a.ldo + n0 + tx * 4 + 64 * jb;
         // round to the storage type first, so H is computed from exactly the
         // values a backward pass reads back
@@ -414,7 +424,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
       if constexpr (ROUTED && KIND == DOWN) sc = a.gates[a.rowpair[r]];
       T* out = reinterpret_cast<T*>(a.slot_out);
 #pragma unroll
-      for (int j = 0; j < R; ++j)
+      for (int j = 0; j < RN; ++j)
         out[r * a.ldo + n0 + tx * 4 + (j & 3) + 64 * (j >> 2)] = from_f32<T>(sc * acc[i][j]);
     } else if constexpr (KIND == DZ) {
       const bool exists = ROUTED || r < a.rows;
@@ -428,7 +438,7 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
       const int64_t h = a.h;
       float dgp = 0.f;
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
+      for (int j = 0; j < RN; ++j) {
         const int n = n0 + tx * 4 + (j & 3) + 64 * (j >> 2);
         const float z = acc[i][j];
         const float ag = valid ? to_f32(AG[r * h + n]) : 0.f;
@@ -455,11 +465,11 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
       const int64_t om = m0 + m;
       const int64_t eoff = (int64_t)e * a.n_mtiles * TM;  // expert offset in rows
 #pragma unroll
-      for (int jb = 0; jb < U; ++jb) {
+      for (int jb = 0; jb < UN; ++jb) {
         const int n = n0 + tx * 4 + 64 * jb;
         float* dst;
         if (a.ksplit > 1) {
-          dst = a.part + chunk * a.part_sstride + (eoff + om) * ((int64_t)a.n_ntiles * TM) + n;
+          dst = a.part + chunk * a.part_sstride + (eoff + om) * ((int64_t)a.n_ntiles * TN) + n;
         } else if constexpr (KIND == DWGU) {
           // a 4-column block never straddles the gate | up boundary (h % 4 == 0)
           dst = n < a.h ? a.acc_out + (eoff + om) * a.h + n
@@ -490,7 +500,7 @@ __global__ void __launch_bounds__(NT, TM == 64 ? 4 : 2) simt_gemm2_kernel(const 
 }
 template <Kind KIND, typename T, bool ROUTED, int TM>
 constexpr auto simt_kernel() {
-  if constexpr (KIND == DWD || KIND == DWGU || KIND == DX)
+  if constexpr (KIND == DWD || KIND == DWGU || KIND == DX || (KIND == GU && TM == 128))
     return simt_gemm2_kernel<KIND, T, ROUTED, TM>;
   else return simt_gemm_kernel<KIND, T, ROUTED, TM>;
 }
@@ -633,7 +643,7 @@ void grouped_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs
   a.au_out = mode == MOE_SAVE_FOR_BWD ? p.a_up : nullptr;
   a.ldo = h;
   a.tm = tile_of(h);
-  a.n_ntiles = h / a.tm;
+  a.n_ntiles = h / gu_cols(a.tm);
   launch<GU, T, true>(a, a.n_ntiles * (128 / a.tm) * L.MTcap, s);
   // down projection with the gate-weighted combine
   SimtArgs b = a;
@@ -670,7 +680,7 @@ void shared_fwd_t(const moe_dims& d, const Layout& L, int mode, const LayerPtrs&
   a.au_out = mode == MOE_SAVE_FOR_BWD ? p.as_up : nullptr;
   a.ldo = hs;
   a.tm = tile_of(hs);
-  a.n_ntiles = hs / a.tm;
+  a.n_ntiles = hs / gu_cols(a.tm);
   launch<GU, T, false>(a, a.n_ntiles * ((d.tokens + a.tm - 1) / a.tm), s);
   SimtArgs b = a;
   b.A = p.hs_buf;
