@@ -92,11 +92,16 @@ void launch_topk_softmax(const float* logits, int64_t T, int E, int k, int32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// Fused router: one thread per token computes its EN logits (float32
-// accumulate, W_r staged in shared memory and read by broadcast), selects
-// the top k among them in registers and writes idx / gates (and the logits
-// when asked).  Persistent blocks loop over 128-token groups.
+// Fused router: a group of G = 8 lanes per token computes its EN logits
+// (float32 accumulate; lane g takes the model dimensions g, g + 8, ...,
+// W_r staged in shared memory with rows padded to EN + 4 floats, so that
+// the group's eight rows fall in distinct banks), sums the lanes' partials
+// by a butterfly over the group, and the group's first lane selects the top
+// k in registers and writes idx / gates (and the logits when asked).
+// Persistent blocks loop over 16-token groups.
 // ---------------------------------------------------------------------------
+constexpr int kRouterLanes = 8;  // lanes per token
+
 template <typename T, int EN>
 __global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__ x,
                                                            const T* __restrict__ w_router,
@@ -105,47 +110,54 @@ __global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__
                                                            float* __restrict__ logits_out,
                                                            int32_t* __restrict__ idx_out,
                                                            float* __restrict__ gates_out) {
-  extern __shared__ __align__(16) float s_w[];  // [d][EN]
-  for (int i = threadIdx.x; i < d * EN; i += blockDim.x) s_w[i] = to_f32(w_router[i]);
+  constexpr int G = kRouterLanes, LD = EN + 4;
+  extern __shared__ __align__(16) float s_w[];  // [d][EN + 4]
+  // W_r in 16-byte (float) / 8-byte (bf16) pieces of four, loads unrolled
+#pragma unroll 4
+  for (int i = threadIdx.x; i < d * EN / 4; i += blockDim.x) {
+    float4 v;
+    if constexpr (sizeof(T) == 4) {
+      v = __ldg(reinterpret_cast<const float4*>(w_router) + i);
+    } else {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(w_router) + i);
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+      v = make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    *reinterpret_cast<float4*>(s_w + (4 * i / EN) * LD + 4 * i % EN) = v;
+  }
   __syncthreads();
-  constexpr int VE = 16 / sizeof(T);  // elements per 16-byte load
-  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < Tn + 0;
-       t += (int64_t)gridDim.x * blockDim.x) {
+  const int g = threadIdx.x % G;
+  const int tpb = blockDim.x / G;  // tokens per block and pass
+  // the loop bound is the same for every thread of the block, so every lane
+  // of a warp takes part in each pass's shuffles
+  for (int64_t t0 = (int64_t)blockIdx.x * tpb; t0 < Tn; t0 += (int64_t)gridDim.x * tpb) {
+    const int64_t t = t0 + threadIdx.x / G;
+    const bool valid = t < Tn;
     float acc[EN];
 #pragma unroll
     for (int e = 0; e < EN; ++e) acc[e] = 0.f;
-    const uint4* xr = reinterpret_cast<const uint4*>(x + t * d);
-#pragma unroll 1
-    for (int c = 0; c < d / VE; ++c) {
-      const uint4 u = __ldg(xr + c);
-      float xv[VE];
-      if constexpr (sizeof(T) == 2) {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
-          xv[2 * j] = f.x;
-          xv[2 * j + 1] = f.y;
-        }
-      } else {
-        xv[0] = __uint_as_float(u.x);
-        xv[1] = __uint_as_float(u.y);
-        xv[2] = __uint_as_float(u.z);
-        xv[3] = __uint_as_float(u.w);
-      }
-#pragma unroll
-      for (int j = 0; j < VE; ++j) {
-        const float4* wr = reinterpret_cast<const float4*>(s_w + (c * VE + j) * EN);
+    if (valid) {
+      const T* xr = x + t * d;
+#pragma unroll 16
+      for (int kk = g; kk < d; kk += G) {
+        const float xv = to_f32(__ldg(xr + kk));
+        const float4* wr = reinterpret_cast<const float4*>(s_w + kk * LD);
 #pragma unroll
         for (int e4 = 0; e4 < EN / 4; ++e4) {
           const float4 w4 = wr[e4];
-          acc[4 * e4 + 0] = fmaf(xv[j], w4.x, acc[4 * e4 + 0]);
-          acc[4 * e4 + 1] = fmaf(xv[j], w4.y, acc[4 * e4 + 1]);
-          acc[4 * e4 + 2] = fmaf(xv[j], w4.z, acc[4 * e4 + 2]);
-          acc[4 * e4 + 3] = fmaf(xv[j], w4.w, acc[4 * e4 + 3]);
+          acc[4 * e4 + 0] = fmaf(xv, w4.x, acc[4 * e4 + 0]);
+          acc[4 * e4 + 1] = fmaf(xv, w4.y, acc[4 * e4 + 1]);
+          acc[4 * e4 + 2] = fmaf(xv, w4.z, acc[4 * e4 + 2]);
+          acc[4 * e4 + 3] = fmaf(xv, w4.w, acc[4 * e4 + 3]);
         }
       }
     }
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1)
+#pragma unroll
+      for (int e = 0; e < EN; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+    if (!valid || g != 0) continue;
     if (bias) {
 #pragma unroll
       for (int e = 0; e < EN; ++e) acc[e] += __ldg(bias + e);
@@ -183,14 +195,14 @@ __global__ void __launch_bounds__(128) router_fused_kernel(const T* __restrict__
 template <typename T, int EN>
 static void router_fused_t(const moe_dims& dm, const void* x, const void* w, const float* bias,
                            float* logits_out, int32_t* idx, float* gates, cudaStream_t s) {
-  const size_t smem = sizeof(float) * dm.d_model * EN;
+  const size_t smem = sizeof(float) * dm.d_model * (EN + 4);
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(router_fused_kernel<T, EN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          160 * 1024);
     attr = true;
   }
-  int64_t blocks = (dm.tokens + 127) / 128;
+  int64_t blocks = (dm.tokens + 128 / kRouterLanes - 1) / (128 / kRouterLanes);
   const int64_t cap = EN >= 32 ? 152 : 152 * 8;  // amortise the W_r staging for wide routers
   if (blocks > cap) blocks = cap;
   MOE_LAUNCH("router_fused", s,
@@ -202,7 +214,7 @@ static void router_fused_t(const moe_dims& dm, const void* x, const void* w, con
 bool router_fused_supported(const moe_dims& d) {
   const int E = d.experts;
   return (E == 8 || E == 16 || E == 32 || E == 64) &&
-         (size_t)d.d_model * E * sizeof(float) <= 160 * 1024;
+         (size_t)d.d_model * (E + 4) * sizeof(float) <= 160 * 1024;
 }
 
 void launch_router_fused(const moe_dims& d, const void* x, const void* w, const float* bias,
