@@ -121,7 +121,8 @@ __device__ __forceinline__ float comp(const float4& v, int q) {
 // columns tx*4 + j + 64*v), so that every shared-memory operand read is a
 // conflict-free float4 and the 16 threads of a row are 16 consecutive lanes.
 // The 8 x 8 micro-tile issues 64 FFMAs per 4 float4 loads of each k step,
-// the 4 x 4 one 16 per 2.
+// the 4 x 4 one 16 per 2.  The gate/up projection's 128-row tiles are 64
+// columns wide in each of its two weights (8 x 4 micro-tiles, two of them).
 template <Kind KIND, typename T, bool ROUTED, int TM>
 __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
   constexpr bool A_KCONTIG = (KIND == LOGITS || KIND == GU || KIND == DOWN || KIND == DZ ||
@@ -490,12 +491,12 @@ __device__ __forceinline__ void simt_gemm_body(const SimtArgs& a) {
   }
 }
 
-// The kernels: the weight-gradient kinds and dX keep two 128-wide (four
-// 64-wide) tiles resident per SM (at most 128 / 64 registers a thread:
-// measured 0.63 -> 0.68 of the FFMA rate for dX at 131072 tokens); the
-// other kinds take the registers the compiler gives them (the routed down
-// projection and dZ already fit two, the gate/up projection's two
-// accumulator sets do not).
+// The kernels: the weight-gradient kinds, dX and the 128-row gate/up tiles
+// are compiled for two resident 128-row blocks (four 64-row) per SM, at most
+// 128 / 64 registers a thread (measured 0.63 -> 0.68 of the FFMA rate for
+// dX at 131072 tokens); the other kinds take the registers the compiler
+// gives them (the routed down projection and dZ fit two blocks as they are;
+// the dense down projection spills under the bound).
 template <Kind KIND, typename T, bool ROUTED, int TM>
 __global__ void __launch_bounds__(NT) simt_gemm_kernel(const SimtArgs a) {
   simt_gemm_body<KIND, T, ROUTED, TM>(a);
@@ -511,11 +512,8 @@ constexpr auto simt_kernel() {
   else return simt_gemm_kernel<KIND, T, ROUTED, TM>;
 }
 
-// `blocks` counts 64 x 64 tiles; with a.tm = 128 each block takes a
-// 128 x 128 tile (a quarter as many blocks; the routed row kinds, whose tile
-// list holds 128-row entries, half as many per column tile)
-// dynamic shared memory of a kernel instance: the two buffers of A and B of
-// the double-buffered kinds (the others keep static tiles)
+// Dynamic shared memory of a kernel instance: the two buffers of A and B of
+// the double-buffered kinds (the others keep static tiles).
 template <Kind KIND, int TM>
 constexpr size_t simt_smem_bytes() {
   return (KIND == DWD || KIND == DWGU || KIND == DZ) ? sizeof(float) * BK * (TM + 4) * 2 * 2 : 0;
