@@ -56,3 +56,17 @@ def test_traffic_key_ignores_comments_only():
     assert bench.code_text(a) == bench.code_text(b)
     assert bench.code_text(a) != bench.code_text(a.replace("return 1", "return 2"))
     assert bench.code_text('"a /* b */"') == '"a /* b */"'  # inside a string: code
+
+
+def test_traffic_key_covers_every_source_but_the_fp32_gemms(tmp_path):
+    # the key changes with any .cu / .cuh file's code except the strict-fp32
+    # GEMMs' file, which no bf16 step runs
+    for name, body in (("a.cu", "int a;"), ("b.cuh", "int b;"), ("gemm_simt.cu", "int c;"),
+                       ("notes.txt", "x")):
+        (tmp_path / name).write_text(body)
+    key = bench.src_hash(str(tmp_path))
+    (tmp_path / "gemm_simt.cu").write_text("int c2;")
+    (tmp_path / "notes.txt").write_text("y")
+    assert bench.src_hash(str(tmp_path)) == key
+    (tmp_path / "b.cuh").write_text("int b2;")
+    assert bench.src_hash(str(tmp_path)) != key
