@@ -618,10 +618,13 @@ def measure(cfg, args, world, rank, local, barrier, peaks, cpu_baseline):
                                     [dx_h[i % 2] for i in range(n)])
 
     e2e_steps(2)  # first-call setup
-    # graph mode: a CUDA graph of eight pipelined steps, replayed (the copies
-    # and the cross-stream events record into it like the kernels)
-    per_run = min(8, n_e2e) if args.launch == "graph" else n_e2e
-    runs = max(1, n_e2e // per_run)
+    # one pipelined sequence of all the timed steps, as a training loop runs
+    # them (the first step's input copy and the last step's result copy are
+    # the only ones not hidden behind a step); graph mode: the sequence
+    # captured as one CUDA graph and replayed (the copies and the
+    # cross-stream events record into it like the kernels)
+    per_run = n_e2e
+    runs = 1
     run_steps = layer.capture(lambda: e2e_steps(per_run)) if args.launch == "graph" else \
         (lambda: e2e_steps(per_run))
     torch.cuda.synchronize()
