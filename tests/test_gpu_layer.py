@@ -61,6 +61,7 @@ SMALL = [
     # a shared expert, and with skewed routing (empty experts: empty chunks)
     MoEConfig(4096, 128, 128, 4, 2, 128, "f32", "f32_dw_chunks_shared"),
     MoEConfig(4096, 128, 64, 8, 2, 0, "f32", "f32_dw_chunks_skew", skew=0.9),
+    MoEConfig(4096, 128, 128, 4, 2, 0, "f32", "f32_dw_chunks_capacity", capacity=700),
 ]
 
 
