@@ -77,21 +77,24 @@ __global__ void __launch_bounds__(256) router_dsel_kernel(const float* __restric
   }
 }
 
-// dW_r partial of one token range: thread i owns input dimension i and its
-// column of the shared accumulator [E][256], so the order of the adds is
-// fixed; the range's (expert, dsel) pairs are staged in shared memory.
+// dW_r partial of one token range and one group of experts (blockIdx.z:
+// experts [z * EG, z * EG + EG) of E): thread i owns input dimension i and
+// its column of the shared accumulator [EG][256], so the order of the adds
+// is fixed; the range's (expert, dsel) pairs are staged in shared memory.
 template <typename T>
 __global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
                                                         const int32_t* __restrict__ idx,
                                                         const float* __restrict__ dsel,
-                                                        int64_t Tn, int d, int E, int k,
+                                                        int64_t Tn, int d, int E, int EG, int k,
                                                         int64_t per_range, float* part) {
-  extern __shared__ __align__(16) float s_acc[];  // [E][256]
+  extern __shared__ __align__(16) float s_acc[];  // [EG][256]
   __shared__ int s_e[256];
   __shared__ float s_ds[256];
   const int tid = threadIdx.x;
   const int i = blockIdx.y * 256 + tid;
-  for (int e = 0; e < E; ++e) s_acc[e * 256 + tid] = 0.f;
+  const int e0 = blockIdx.z * EG;
+  const int ne = E - e0 < EG ? E - e0 : EG;  // experts of this group
+  for (int e = 0; e < ne; ++e) s_acc[e * 256 + tid] = 0.f;
   const int64_t t0 = blockIdx.x * per_range;
   const int64_t t1 = t0 + per_range < Tn ? t0 + per_range : Tn;
   const int CH = 256 / k;
@@ -99,9 +102,10 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
     const int nt = (int)(t1 - tc < CH ? t1 - tc : CH);
     __syncthreads();
     if (tid < nt * k) {
+      // a rejected index, or an expert of another group, contributes nothing
       const int e = idx[tc * k + tid];
-      const bool ok = e >= 0 && e < E;  // a rejected index contributes nothing
-      s_e[tid] = ok ? e : 0;
+      const bool ok = e >= e0 && e < e0 + ne;
+      s_e[tid] = ok ? e - e0 : 0;
       s_ds[tid] = ok ? dsel[tc * k + tid] : 0.f;
     }
     __syncthreads();
@@ -128,8 +132,8 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const T* __restrict__ x,
     }
   }
   if (i < d) {
-    float* out = part + ((int64_t)blockIdx.x * d + i) * E;
-    for (int e = 0; e < E; ++e) out[e] = s_acc[e * 256 + tid];
+    float* out = part + ((int64_t)blockIdx.x * d + i) * E + e0;
+    for (int e = 0; e < ne; ++e) out[e] = s_acc[e * 256 + tid];
   }
 }
 
@@ -203,10 +207,15 @@ void router_dw_dx_t(const moe_dims& d, const Layout& L, const LayerPtrs& p, void
   if (ranges > kRouterBwdRanges) ranges = kRouterBwdRanges;
   if (ranges < 1) ranges = 1;
   const int64_t per_range = (d.tokens + ranges - 1) / ranges;
+  // experts in groups whose accumulators fit the shared-memory budget
+  const int eg_max = (int)(kRouterBwdSmem / (sizeof(float) * 256));
+  const int groups = (E + eg_max - 1) / eg_max;
+  const int EG = (E + groups - 1) / groups;
   MOE_LAUNCH("router_dw", s,
-             router_dw_kernel<T><<<dim3((unsigned)ranges, ny), 256, sizeof(float) * E * 256, s>>>(
-                 reinterpret_cast<const T*>(p.x), p.topk_idx, dsel, d.tokens, dm, E, k, per_range,
-                 part));
+             router_dw_kernel<T><<<dim3((unsigned)ranges, ny, groups), 256,
+                                   sizeof(float) * EG * 256, s>>>(
+                 reinterpret_cast<const T*>(p.x), p.topk_idx, dsel, d.tokens, dm, E, EG, k,
+                 per_range, part));
   const int64_t n = (int64_t)dm * E;
   MOE_LAUNCH("router_dw_reduce", s,
              router_dw_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
@@ -243,8 +252,9 @@ void launch_router_backward(const moe_dims& d, const Layout& L, const LayerPtrs&
 }
 
 bool router_backward_supported(const moe_dims& d) {
-  // the CUDA-core dW_r path keeps one [E][256] f32 accumulator per block
-  return tc_router_dw_supported(d) || (size_t)d.experts * 256 * 4 <= (size_t)kRouterBwdSmem;
+  // the CUDA-core dW_r path takes the experts in groups that fit its
+  // shared-memory accumulator, so every E the layer takes
+  return d.experts >= 1 && d.experts <= kMaxExperts;
 }
 
 }  // namespace moe

@@ -62,6 +62,11 @@ SMALL = [
     MoEConfig(4096, 128, 128, 4, 2, 128, "f32", "f32_dw_chunks_shared"),
     MoEConfig(4096, 128, 64, 8, 2, 0, "f32", "f32_dw_chunks_skew", skew=0.9),
     MoEConfig(4096, 128, 128, 4, 2, 0, "f32", "f32_dw_chunks_capacity", capacity=700),
+    # more experts than the tensor-core router takes (E > 64): the logits
+    # GEMM, the selection and the router backward on their general paths;
+    # the most experts the counting sort takes (256)
+    MoEConfig(1000, 128, 64, 128, 4, 64, "bf16", "bf16_e128k4_shared"),
+    MoEConfig(1500, 128, 64, 256, 2, 0, "f32", "f32_e256k2"),
 ]
 
 
