@@ -67,6 +67,7 @@ SMALL = [
     # the most experts the counting sort takes (256)
     MoEConfig(1000, 128, 64, 128, 4, 64, "bf16", "bf16_e128k4_shared"),
     MoEConfig(1500, 128, 64, 256, 2, 0, "f32", "f32_e256k2"),
+    MoEConfig(1000, 128, 64, 256, 2, 0, "bf16", "bf16_e256k2"),
 ]
 
 
@@ -214,12 +215,12 @@ def test_fed_logits_routing_and_layer(case):
         assert np.all(layer.grads["dw_down"][4:].cpu().numpy() == 0)
 
 
-def test_zero_tokens():
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_zero_tokens(dtype):
     from dropless_mixture_experts_gb300.layer import MoELayer
-    cfg = MoEConfig(0, 128, 64, 4, 2, 64, "bf16", "empty")
-    layer = MoELayer(0, 128, 64, 4, 2, 64, "bf16", train=True)
-    inp = make_inputs(MoEConfig(1, 128, 64, 4, 2, 64, "bf16"))
-    dev = to_dev(inp, "bf16")
+    layer = MoELayer(0, 128, 64, 4, 2, 64, dtype, train=True)
+    inp = make_inputs(MoEConfig(1, 128, 64, 4, 2, 64, dtype))
+    dev = to_dev(inp, dtype)
     p = {k: dev[k] for k in params_of(inp)}
     x = dev["x"][:0]
     loss, dx, grads = layer.train_step(x, p, dev["upstream"][:0])
