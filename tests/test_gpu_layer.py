@@ -68,6 +68,10 @@ SMALL = [
     MoEConfig(1000, 128, 64, 128, 4, 64, "bf16", "bf16_e128k4_shared"),
     MoEConfig(1500, 128, 64, 256, 2, 0, "f32", "f32_e256k2"),
     MoEConfig(1000, 128, 64, 256, 2, 0, "bf16", "bf16_e256k2"),
+    # a model width and a shared width that are multiples of 64 but not of
+    # 128 (64-wide tiles and K blocks of the operand rows)
+    MoEConfig(900, 192, 128, 8, 2, 192, "bf16", "bf16_d192_shared192"),
+    MoEConfig(900, 192, 128, 8, 2, 192, "f32", "f32_d192_shared192"),
 ]
 
 
