@@ -72,6 +72,10 @@ SMALL = [
     # 128 (64-wide tiles and K blocks of the operand rows)
     MoEConfig(900, 192, 128, 8, 2, 192, "bf16", "bf16_d192_shared192"),
     MoEConfig(900, 192, 128, 8, 2, 192, "f32", "f32_d192_shared192"),
+    # the narrowest widths (64) on the tensor-core path, every expert taken
+    # by every token; the largest k with the most experts
+    MoEConfig(500, 64, 64, 4, 4, 64, "bf16", "bf16_d64_k_eq_E_shared"),
+    MoEConfig(300, 128, 64, 256, 32, 0, "bf16", "bf16_e256k32"),
 ]
 
 
