@@ -22,6 +22,9 @@ constexpr int kLossBlocks = 2048;  // fixed partial count of the loss reduction
 constexpr int kRouterBwdRanges = 608;  // max token ranges of the router-weight gradient partials
 constexpr int kRouterBwdSmem = 200 * 1024;  // router backward: W_r^T + dW_r partial in shared memory
 constexpr int kSimtMaxSplit = 8;  // most K chunks of a strict-float32 weight-gradient GEMM
+// most (output tile x chunk) blocks of a chunked strict-float32 weight
+// gradient: bounds its partials to this many 128 x 128 float tiles (256 MiB)
+constexpr int kSimtChunkTiles = 4096;
 
 // ---- element access ---------------------------------------------------------
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -209,8 +212,11 @@ inline Layout make_layout(const moe_dims& d, int mode) {
     pf = std::max(pf, (int64_t)router_dw_split_bound((dm + 127) / 128) * dm * 64);
     if (d.dtype != MOE_BF16) {
       // the strict-float32 weight gradients' K-chunk partials [chunk][E * M][N]
-      pf = std::max(pf, (int64_t)kSimtMaxSplit * E * std::max(h * dm, dm * 2 * h));
-      if (hs > 0) pfs = std::max(pfs, (int64_t)kSimtMaxSplit * std::max(hs * dm, dm * 2 * hs));
+      // (chunks only where tiles x chunks <= kSimtChunkTiles)
+      const int64_t cap = (int64_t)kSimtChunkTiles * 128 * 128;
+      pf = std::max(pf, std::min(cap, (int64_t)kSimtMaxSplit * E * std::max(h * dm, dm * 2 * h)));
+      if (hs > 0)
+        pfs = std::max(pfs, std::min(cap, (int64_t)kSimtMaxSplit * std::max(hs * dm, dm * 2 * hs)));
     }
     L.dwpart = take(sizeof(float) * pf);
     L.dwpart_sh = take(sizeof(float) * pfs);

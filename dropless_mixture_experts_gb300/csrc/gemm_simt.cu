@@ -550,8 +550,9 @@ int64_t resident_slots() {
 
 // K chunks for a weight-gradient GEMM of `tiles` output tiles whose experts
 // hold about `krows` rows each: the count (<= kSimtMaxSplit, chunks of at
-// least 256 rows) whose blocks fill their last wave of `slots` best; more
-// chunks only where that gains at least 2 % (each adds a partial tile).
+// least 256 rows, tiles x chunks <= kSimtChunkTiles, the partials' room)
+// whose blocks fill their last wave of `slots` best; more chunks only where
+// that gains at least 2 % (each adds a partial tile).
 inline int dw_chunks(int64_t tiles, int64_t krows, int64_t slots) {
   auto fill = [&](int c) {
     const double w = (double)(tiles * c) / (double)slots;
@@ -559,7 +560,7 @@ inline int dw_chunks(int64_t tiles, int64_t krows, int64_t slots) {
   };
   int best = 1;
   double best_fill = fill(1);
-  for (int c = 2; c <= kSimtMaxSplit && krows / c >= 256; ++c) {
+  for (int c = 2; c <= kSimtMaxSplit && krows / c >= 256 && tiles * c <= kSimtChunkTiles; ++c) {
     const double f = fill(c);
     if (f > best_fill + 0.02) {
       best = c;
