@@ -593,7 +593,9 @@ void launch_dw(SimtArgs a, int64_t tiles, int64_t krows, float* part, cudaStream
   if (tiles <= 0) return;
   const int64_t slots = a.tm == 128 ? resident_slots<KIND, T, ROUTED, 128>()
                                     : resident_slots<KIND, T, ROUTED, 64>();
-  const int c = dw_chunks(tiles, krows, slots);
+  // the workspace holds chunk partials for float32 layers (the bf16 layer's
+  // weight gradients run on the tensor cores)
+  const int c = sizeof(T) == 4 ? dw_chunks(tiles, krows, slots) : 1;
   const int64_t M = (int64_t)a.n_mtiles * a.tm, N = (int64_t)a.n_ntiles * a.tm;
   const int64_t EM = tiles / ((int64_t)a.n_mtiles * a.n_ntiles) * M;
   if (c > 1) {
