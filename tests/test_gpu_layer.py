@@ -76,6 +76,10 @@ SMALL = [
     # by every token; the largest k with the most experts
     MoEConfig(500, 64, 64, 4, 4, 64, "bf16", "bf16_d64_k_eq_E_shared"),
     MoEConfig(300, 128, 64, 256, 32, 0, "bf16", "bf16_e256k32"),
+    # one token on the tensor-core path with a shared expert; float32
+    # capacity routing beside a shared expert
+    MoEConfig(1, 128, 64, 4, 1, 64, "bf16", "bf16_one_token_shared"),
+    MoEConfig(1500, 128, 64, 16, 4, 128, "f32", "f32_capacity_shared", capacity=300),
 ]
 
 
